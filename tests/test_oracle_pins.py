@@ -1,0 +1,294 @@
+"""Pins of the fp64 oracle against things other than itself (CPU only).
+
+* library special cases: torch.nn.LSTM / torch.nn.GRU in fp64 with W_ih = I
+  and W_hh = R[h]^T reproduce the head-wise cells, forward and autograd;
+* closed forms: R = 0 reduces each cell to a per-step formula written out here
+  as explicit sums/products; T = 1 from zero state;
+* invariants: saturated gates hold state, head and batch permutation,
+  chunking through the carried state, NH heads == one block-diagonal RNN,
+  sLSTM == its unstabilised form;
+* central finite differences for every gradient of every cell.
+
+The FlashRNN pages ("FlashRNN: I/O-Aware Optimization of Traditional RNNs on
+modern hardware", abstract) name LSTM, GRU and sLSTM and the head-wise split;
+the blog page ("re-examining RNNs from a GPU programming perspective",
+head-wise paragraph) states that the heads form a block-diagonal recurrent
+matrix.  These pins check exactly those statements plus the cell equations.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import rnn_oracle as O
+from synth import make_inputs
+
+pytestmark = pytest.mark.filterwarnings("ignore::UserWarning")
+
+
+def _inp(cell, T=7, B=3, NH=2, Dh=5, seed=1, states="random", bias="normal", backward=False):
+    return make_inputs(cell, "f32", T, B, NH, Dh, seed=seed, bias=bias, states=states,
+                       backward=backward)
+
+
+# ----------------------------------------------------------- torch pins ----
+def _torch_cell(cell, x, Rh, bh, h0, c0, dh=None):
+    """Run one head through torch.nn.LSTM/GRU (fp64); optionally backprop."""
+    T, B, GD = x.shape
+    Dh = Rh.shape[0]
+    mod = (torch.nn.LSTM if cell == "lstm" else torch.nn.GRU)(GD, Dh, dtype=torch.float64)
+    with torch.no_grad():
+        mod.weight_ih_l0.copy_(torch.eye(GD, dtype=torch.float64))
+        mod.weight_hh_l0.copy_(torch.from_numpy(Rh.T.astype(np.float64)))
+        mod.bias_ih_l0.zero_()
+        mod.bias_hh_l0.copy_(torch.from_numpy(bh.astype(np.float64)))
+    xt = torch.from_numpy(x.astype(np.float64)).requires_grad_(True)
+    h0t = torch.from_numpy(h0.astype(np.float64))[None].requires_grad_(True)
+    if cell == "lstm":
+        c0t = torch.from_numpy(c0.astype(np.float64))[None].requires_grad_(True)
+        out, (hn, cn) = mod(xt, (h0t, c0t))
+    else:
+        out, hn = mod(xt, h0t)
+        cn = None
+    res = {"h_seq": out.detach().numpy(), "hT": hn[0].detach().numpy()}
+    if cn is not None:
+        res["cT"] = cn[0].detach().numpy()
+    if dh is not None:
+        (out * torch.from_numpy(dh.astype(np.float64))).sum().backward()
+        res["dWx"] = xt.grad.numpy()
+        res["dR"] = mod.weight_hh_l0.grad.numpy().T
+        res["db"] = mod.bias_hh_l0.grad.numpy()
+        res["dh0"] = h0t.grad[0].numpy()
+        if cell == "lstm":
+            res["dc0"] = c0t.grad[0].numpy()
+    return res
+
+
+@pytest.mark.parametrize("cell", ["lstm", "gru"])
+def test_forward_matches_torch(cell):
+    d = _inp(cell)
+    o = O.forward(cell, d["Wx"], d["R"], d["b"], d["h0"], d["c0"])
+    for h in range(d["NH"]):
+        ref = _torch_cell(cell, d["Wx"][:, :, h], d["R"][h], d["b"][h], d["h0"][:, h], d["c0"][:, h])
+        np.testing.assert_allclose(o["h_seq"][:, :, h], ref["h_seq"], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(o["hT"][:, h], ref["hT"], rtol=0, atol=1e-12)
+        if cell == "lstm":
+            np.testing.assert_allclose(o["cT"][:, h], ref["cT"], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("cell", ["lstm", "gru"])
+def test_backward_matches_torch_autograd(cell):
+    d = _inp(cell, backward=True)
+    g = O.backward(cell, d["Wx"], d["R"], d["b"], d["h0"], d["c0"], dh_seq=d["dh"])
+    for h in range(d["NH"]):
+        ref = _torch_cell(cell, d["Wx"][:, :, h], d["R"][h], d["b"][h], d["h0"][:, h],
+                          d["c0"][:, h], dh=d["dh"][:, :, h])
+        np.testing.assert_allclose(g["dWx"][:, :, h], ref["dWx"], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(g["dR"][h], ref["dR"], rtol=0, atol=1e-11)
+        np.testing.assert_allclose(g["db"][h], ref["db"], rtol=0, atol=1e-11)
+        np.testing.assert_allclose(g["dh0"][:, h], ref["dh0"], rtol=0, atol=1e-12)
+        if cell == "lstm":
+            np.testing.assert_allclose(g["dc0"][:, h], ref["dc0"], rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------- closed forms ----
+def _sig(x):
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def test_lstm_R0_closed_form():
+    d = _inp("lstm", T=6)
+    R0 = np.zeros_like(d["R"])
+    o = O.lstm_forward(d["Wx"], R0, d["b"], d["h0"], d["c0"])
+    pre = d["Wx"].astype(np.float64) + d["b"]
+    Dh = d["Dh"]
+    gi, gf, gz, go = (pre[..., k * Dh:(k + 1) * Dh] for k in range(4))
+    i, f, z, og = _sig(gi), _sig(gf), np.tanh(gz), _sig(go)
+    for t in range(d["T"]):
+        # c_t = prod_{u<=t} f_u * c0 + sum_s (prod_{s<u<=t} f_u) i_s z_s
+        c = np.prod(f[:t + 1], axis=0) * d["c0"]
+        for s in range(t + 1):
+            c = c + np.prod(f[s + 1:t + 1], axis=0) * i[s] * z[s]
+        np.testing.assert_allclose(o["h_seq"][t], og[t] * np.tanh(c), atol=1e-13, rtol=0)
+
+
+def test_gru_R0_closed_form():
+    d = _inp("gru", T=6)
+    R0 = np.zeros_like(d["R"])
+    o = O.gru_forward(d["Wx"], R0, d["b"], d["h0"])
+    Dh = d["Dh"]
+    x = d["Wx"].astype(np.float64)
+    b = d["b"].astype(np.float64)
+    r = _sig(x[..., :Dh] + b[:, :Dh])
+    z = _sig(x[..., Dh:2 * Dh] + b[:, Dh:2 * Dh])
+    n = np.tanh(x[..., 2 * Dh:] + r * b[:, 2 * Dh:])
+    for t in range(d["T"]):
+        h = np.prod(z[:t + 1], axis=0) * d["h0"]
+        for s in range(t + 1):
+            h = h + np.prod(z[s + 1:t + 1], axis=0) * (1 - z[s]) * n[s]
+        np.testing.assert_allclose(o["h_seq"][t], h, atol=1e-13, rtol=0)
+
+
+def test_slstm_R0_weighted_average():
+    """R=0, zero state: c/n is a softmax-weighted average of tanh(z~)."""
+    d = _inp("slstm", T=9, states="zero")
+    R0 = np.zeros_like(d["R"])
+    o = O.slstm_forward(d["Wx"], R0, d["b"])
+    Dh = d["Dh"]
+    pre = d["Wx"].astype(np.float64) + d["b"]
+    gi, gf, gz, go = (pre[..., k * Dh:(k + 1) * Dh] for k in range(4))
+    for t in range(d["T"]):
+        logw = np.stack([gi[s] + gf[s + 1:t + 1].sum(axis=0) for s in range(t + 1)])
+        w = np.exp(logw - logw.max(axis=0))
+        avg = (w * np.tanh(gz[:t + 1])).sum(axis=0) / w.sum(axis=0)
+        np.testing.assert_allclose(o["h_seq"][t], _sig(go[t]) * avg, atol=1e-13, rtol=0)
+
+
+def test_T1_scalar_closed_forms():
+    """T=1 from zero state, written with scalar math (no numpy vector ops)."""
+    wx = [0.5, -0.25, 1.0, 2.0]
+    b = [0.1, 1.0, -0.3, 0.0]
+    s = lambda v: 1.0 / (1.0 + math.exp(-v))  # noqa: E731
+    p = [wx[k] + b[k] for k in range(4)]
+    args = (np.array(wx).reshape(1, 1, 1, 4), np.full((1, 1, 4), 0.7), np.array(b).reshape(1, 4))
+    lstm = O.lstm_forward(*args)["hT"].item()
+    assert lstm == pytest.approx(s(p[3]) * math.tanh(s(p[0]) * math.tanh(p[2])), abs=1e-15)
+    sl = O.slstm_forward(*args)["hT"].item()
+    m = max(p[1], p[0])
+    i = math.exp(p[0] - m)
+    assert sl == pytest.approx(s(p[3]) * (i * math.tanh(p[2])) / i, abs=1e-15)
+    g = O.gru_forward(np.array(wx[:3]).reshape(1, 1, 1, 3), np.full((1, 1, 3), 0.7),
+                      np.array(b[:3]).reshape(1, 3))["hT"].item()
+    r, z = s(wx[0] + b[0]), s(wx[1] + b[1])
+    assert g == pytest.approx((1 - z) * math.tanh(wx[2] + r * b[2]), abs=1e-15)
+
+
+# ----------------------------------------------------------- invariants ----
+def test_saturated_gates_hold_state():
+    d = _inp("lstm", Dh=4)
+    Dh = d["Dh"]
+    Wx = d["Wx"].astype(np.float64)
+    Wx[..., :Dh] = -80.0            # input gate shut
+    Wx[..., Dh:2 * Dh] = 80.0       # forget gate open
+    o = O.lstm_forward(Wx, d["R"], d["b"], d["h0"], d["c0"])
+    go = Wx[..., 3 * Dh:]
+    for t in range(d["T"]):
+        hp = d["h0"] if t == 0 else o["h_seq"][t - 1]
+        pre_o = go[t] + np.einsum("bhj,hjk->bhk", hp, d["R"][..., 3 * Dh:]) + d["b"][:, 3 * Dh:]
+        np.testing.assert_allclose(o["h_seq"][t], _sig(pre_o) * np.tanh(d["c0"]), atol=1e-13)
+    np.testing.assert_allclose(o["cT"], d["c0"], atol=1e-13)
+
+    g = _inp("gru", Dh=4)
+    Wx = g["Wx"].astype(np.float64)
+    Wx[..., Dh:2 * Dh] = 80.0       # update gate z = 1 keeps h
+    og = O.gru_forward(Wx, g["R"], g["b"], g["h0"])
+    for t in range(g["T"]):
+        np.testing.assert_allclose(og["h_seq"][t], g["h0"], atol=1e-13)
+
+    s = _inp("slstm", Dh=4)
+    R = s["R"].astype(np.float64).copy()
+    R[..., :2 * Dh] = 0.0           # no recurrent input into i~, f~
+    Wx = s["Wx"].astype(np.float64)
+    Wx[..., :Dh] = -80.0            # i~ = -80
+    Wx[..., Dh:2 * Dh] = 0.0        # f~ = 0 -> f = 1
+    b = s["b"].astype(np.float64).copy()
+    b[:, :2 * Dh] = 0.0
+    os_ = O.slstm_forward(Wx, R, b, s["h0"], s["c0"], s["n0"], s["m0"])
+    np.testing.assert_allclose(os_["cT"], s["c0"], atol=1e-13)
+    np.testing.assert_allclose(os_["nT"], s["n0"], atol=1e-13)
+
+
+@pytest.mark.parametrize("cell", ["lstm", "gru", "slstm"])
+def test_head_and_batch_permutation(cell):
+    d = _inp(cell, NH=4, B=5)
+    o = O.forward(cell, d["Wx"], d["R"], d["b"], d["h0"], d["c0"], d["n0"], d["m0"])
+    ph = np.array([2, 0, 3, 1])
+    pb = np.array([4, 1, 0, 3, 2])
+    op = O.forward(cell, d["Wx"][:, pb][:, :, ph], d["R"][ph], d["b"][ph],
+                   d["h0"][pb][:, ph], d["c0"][pb][:, ph], d["n0"][pb][:, ph], d["m0"][pb][:, ph])
+    np.testing.assert_array_equal(op["h_seq"], o["h_seq"][:, pb][:, :, ph])
+
+
+@pytest.mark.parametrize("cell", ["lstm", "gru", "slstm"])
+def test_chunking_through_state(cell):
+    d = _inp(cell, T=10)
+    full = O.forward(cell, d["Wx"], d["R"], d["b"], d["h0"], d["c0"], d["n0"], d["m0"])
+    a = O.forward(cell, d["Wx"][:4], d["R"], d["b"], d["h0"], d["c0"], d["n0"], d["m0"])
+    b = O.forward(cell, d["Wx"][4:], d["R"], d["b"], a["hT"], a.get("cT"), a.get("nT"), a.get("mT"))
+    np.testing.assert_array_equal(np.concatenate([a["h_seq"], b["h_seq"]]), full["h_seq"])
+
+
+@pytest.mark.parametrize("cell", ["lstm", "gru", "slstm"])
+def test_heads_equal_block_diagonal_rnn(cell):
+    """NH heads == one RNN of size NH*Dh whose R is block-diagonal."""
+    d = _inp(cell, NH=3, Dh=4)
+    NH, Dh, G = d["NH"], d["Dh"], O.GATES[cell]
+    D = NH * Dh
+    Rf = np.zeros((1, D, G * D))
+    Wf = np.zeros(d["Wx"].shape[:2] + (1, G * D))
+    bf = np.zeros((1, G * D))
+    for h in range(NH):
+        for g in range(G):
+            cols = slice(g * D + h * Dh, g * D + (h + 1) * Dh)
+            Rf[0, h * Dh:(h + 1) * Dh, cols] = d["R"][h][:, g * Dh:(g + 1) * Dh]
+            Wf[:, :, 0, cols] = d["Wx"][:, :, h, g * Dh:(g + 1) * Dh]
+            bf[0, cols] = d["b"][h, g * Dh:(g + 1) * Dh]
+    st = {k: d[k].reshape(d["B"], 1, D) for k in ("h0", "c0", "n0", "m0")}
+    o = O.forward(cell, d["Wx"], d["R"], d["b"], d["h0"], d["c0"], d["n0"], d["m0"])
+    of = O.forward(cell, Wf, Rf, bf, st["h0"], st["c0"], st["n0"], st["m0"])
+    np.testing.assert_allclose(of["h_seq"].reshape(o["h_seq"].shape), o["h_seq"], atol=1e-13)
+
+
+def test_slstm_equals_unstabilised_form():
+    """h from the stabilised recurrence == exp-gated recurrence without m."""
+    d = _inp("slstm", T=12, states="zero")
+    o = O.slstm_forward(d["Wx"], d["R"], d["b"])
+    Dh = d["Dh"]
+    Wx = d["Wx"].astype(np.float64)
+    R = d["R"].astype(np.float64)
+    h = np.zeros_like(d["h0"], dtype=np.float64)
+    C = np.zeros_like(h)
+    N = np.zeros_like(h)
+    for t in range(d["T"]):
+        pre = Wx[t] + np.einsum("bhj,hjk->bhk", h, R) + d["b"]
+        gi, gf, gz, go = (pre[..., k * Dh:(k + 1) * Dh] for k in range(4))
+        C = np.exp(gf) * C + np.exp(gi) * np.tanh(gz)
+        N = np.exp(gf) * N + np.exp(gi)
+        h = _sig(go) * C / N
+        np.testing.assert_allclose(o["h_seq"][t], h, atol=1e-12)
+    # with c0 = n0 = 0 the outputs do not depend on m0
+    o2 = O.slstm_forward(d["Wx"], d["R"], d["b"], m0=np.full(d["h0"].shape, 3.0))
+    np.testing.assert_allclose(o2["h_seq"], o["h_seq"], atol=1e-12)
+
+
+# --------------------------------------------------- finite differences ----
+def _loss(cell, d, Wx, R, b, h0, c0, n0):
+    o = O.forward(cell, Wx, R, b, h0, c0, n0, d["m0"])
+    return float((o["h_seq"] * d["dh"]).sum())
+
+
+@pytest.mark.parametrize("cell", ["lstm", "gru", "slstm"])
+def test_backward_finite_differences(cell):
+    d = _inp(cell, T=5, B=2, NH=2, Dh=3, seed=3, backward=True)
+    args = {k: d[k].astype(np.float64).copy() for k in ("Wx", "R", "b", "h0", "c0", "n0")}
+    g = O.backward(cell, args["Wx"], args["R"], args["b"], args["h0"], args["c0"],
+                   args["n0"], d["m0"], dh_seq=d["dh"])
+    names = {"Wx": "dWx", "R": "dR", "b": "db", "h0": "dh0", "c0": "dc0"}
+    if cell == "gru":
+        names.pop("c0")
+    rng = np.random.default_rng(0)
+    eps = 1e-6
+    for src, gname in names.items():
+        x = args[src]
+        for flat in rng.choice(x.size, size=min(12, x.size), replace=False):
+            idx = np.unravel_index(flat, x.shape)
+            old = x[idx]
+            x[idx] = old + eps
+            lp = _loss(cell, d, **args)
+            x[idx] = old - eps
+            lm = _loss(cell, d, **args)
+            x[idx] = old
+            fd = (lp - lm) / (2 * eps)
+            an = g[gname][idx]
+            assert abs(fd - an) <= 1e-7 * max(1.0, abs(an)), (src, idx, fd, an)
