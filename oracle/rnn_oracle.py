@@ -35,7 +35,7 @@ Backward passes are textbook backpropagation through time of exactly these
 forward graphs (the sLSTM stabiliser m is a reparametrisation the output does
 not depend on, so it carries no gradient).
 
-Everything is fp64 numpy; a library matmul (einsum) is the only "primitive".
+Everything is fp64 numpy; a library batched matmul is the only "primitive".
 Optionally ``emulate_bf16_h`` rounds h_{t-1} to bf16 before the contraction,
 mirroring a bf16 MMA operand; it is a diagnosis aid, parity is judged against
 the plain fp64 run.
@@ -56,13 +56,18 @@ def _sigmoid(x):
 
 
 def _recurrent(h_prev, R):
-    """h_prev [B,NH,Dh] @ R [NH,Dh,G*Dh] per head -> [B,NH,G*Dh]."""
-    return np.einsum("bhj,hjk->bhk", h_prev, R)
+    """h_prev [B,NH,Dh] @ R [NH,Dh,G*Dh] per head -> [B,NH,G*Dh] (batched matmul)."""
+    return np.matmul(h_prev.transpose(1, 0, 2), R).transpose(1, 0, 2)
 
 
 def _recurrent_T(dpre, R):
-    """dpre [B,NH,G*Dh] @ R[h]^T per head -> [B,NH,Dh]."""
-    return np.einsum("bhk,hjk->bhj", dpre, R)
+    """dpre [B,NH,G*Dh] @ R[h]^T per head -> [B,NH,Dh] (batched matmul)."""
+    return np.matmul(dpre.transpose(1, 0, 2), R.transpose(0, 2, 1)).transpose(1, 0, 2)
+
+
+def _outer_sum(h_prev, dpre):
+    """sum_b h_prev[b,h,:]^T dpre[b,h,:] per head -> [NH,Dh,G*Dh] (batched matmul)."""
+    return np.matmul(h_prev.transpose(1, 2, 0), dpre.transpose(1, 0, 2))
 
 
 def _split(x, G):
@@ -206,7 +211,7 @@ def lstm_backward(Wx, R, b=None, h0=None, c0=None, dh_seq=None, dhT=None, dcT=No
         dpre = np.concatenate([d_i * i * (1.0 - i), d_f * f * (1.0 - f),
                                d_z * (1.0 - z * z), d_o * o * (1.0 - o)], axis=-1)
         dWx[t] = dpre
-        dR += np.einsum("bhj,bhk->hjk", h_prev, dpre)
+        dR += _outer_sum(h_prev, dpre)
         db += dpre.sum(axis=0)
         dh_next = _recurrent_T(dpre, R)
     return {"dWx": dWx, "dR": dR, "db": db, "dh0": dh_next, "dc0": dc_next}
@@ -235,7 +240,7 @@ def gru_backward(Wx, R, b=None, h0=None, dh_seq=None, dhT=None):
         dz_pre = dz * z * (1.0 - z)
         dWx[t] = np.concatenate([dr_pre, dz_pre, dn_pre], axis=-1)
         drec = np.concatenate([dr_pre, dz_pre, dn_pre * r], axis=-1)
-        dR += np.einsum("bhj,bhk->hjk", h_prev, drec)
+        dR += _outer_sum(h_prev, drec)
         db += drec.sum(axis=0)
         dh_next = dh * z + _recurrent_T(drec, R)
     return {"dWx": dWx, "dR": dR, "db": db, "dh0": dh_next}
@@ -270,7 +275,7 @@ def slstm_backward(Wx, R, b=None, h0=None, c0=None, n0=None, m0=None, dh_seq=Non
         dpre = np.concatenate([d_i * i, d_f * f, d_z * (1.0 - z * z), d_o * o * (1.0 - o)],
                               axis=-1)
         dWx[t] = dpre
-        dR += np.einsum("bhj,bhk->hjk", h_prev, dpre)
+        dR += _outer_sum(h_prev, dpre)
         db += dpre.sum(axis=0)
         dh_next = _recurrent_T(dpre, R)
     return {"dWx": dWx, "dR": dR, "db": db, "dh0": dh_next, "dc0": dc_next, "dn0": dn_next}

@@ -30,7 +30,7 @@ MUTANTS = {
     "no_recurrence": ("_recurrent", lambda o: (lambda h, R: 0.0 * o(h, R))),
     # transposed gradient operand: R instead of R^T in the backward contraction
     "bwd_transpose": ("_recurrent_T",
-                      lambda o: (lambda dp, R: np.einsum("bhk,hjk->bhj", dp, R[..., ::-1]))),
+                      lambda o: (lambda dp, R: o(dp, R[..., ::-1]))),
 }
 
 PINS = {
