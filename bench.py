@@ -1,0 +1,431 @@
+"""Benchmark of the head-wise RNN recurrence (forward; forward+backward for the
+training workload) on GB300.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole recurrence over one synthetic batch of the
+workload (default: LSTM, 12 heads x 64, B=16, T=1024, bf16 inputs / fp32
+state), inputs resident in HBM.  L2 is flushed (a write larger than L2)
+before every timed step, outside the timed events.  ``value`` is recurrent
+TFLOP/s = 2*B*NH*Dh*G*Dh*T / step time (backward counts twice that), summed
+over ranks (weak scaling: every rank runs its own independent batch).
+``e2e`` repeats the measurement through the same C ABI with pinned host
+buffers: host->device copy of the step's inputs and device->host copy of
+h_seq inside the timed region.  ``--impl reference`` times the fp64 CPU
+oracle (the reference arm) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth import WORKLOADS, workload_inputs  # noqa: E402
+
+DEFAULT_WORKLOAD = "lstm_bf16_12x64_b16_t1024"
+METRIC = "fwd recurrent TFLOP/s & steps/s, LSTM 12x64 heads B=16 T=1024; % roofline"
+GATES = {"lstm": 4, "gru": 3, "slstm": 4}
+
+
+def flops_per_step(w):
+    f = 2.0 * w["B"] * w["NH"] * w["Dh"] * GATES[w["cell"]] * w["Dh"] * w["T"]
+    return f * (3.0 if w["backward"] else 1.0)  # bwd: dh_rec + dR contractions
+
+
+def algorithmic_bytes_fwd(w):
+    """Bytes the forward must move: Wx in, h_seq out, R, bias, final states."""
+    e = 2 if w["dtype"] == "bf16" else 4
+    G, T, B, NH, Dh = GATES[w["cell"]], w["T"], w["B"], w["NH"], w["Dh"]
+    per_step = B * NH * G * Dh * e + B * NH * Dh * e
+    once = NH * Dh * G * Dh * e + NH * G * Dh * 4 + 2 * B * NH * Dh * 4
+    if w["backward"]:  # training stash written: gate activations + c_t, fp32
+        per_step += B * NH * Dh * 5 * 4
+    return per_step, per_step * T + once
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_rate(w, d, budget_s=10.0):
+    """fp64 oracle forward (+backward) on the host cores: TFLOP/s over a bounded sample."""
+    from oracle import rnn_oracle as O
+    f_full = flops_per_step(w)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        if w["backward"]:
+            O.backward(w["cell"], d["Wx"], d["R"], d["b"], d["h0"], d["c0"], dh_seq=d["dh"])
+        else:
+            O.forward(w["cell"], d["Wx"], d["R"], d["b"], d["h0"], d["c0"], d["n0"], d["m0"])
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 1000:
+            break
+    return f_full * reps / el / 1e12, reps, el
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def sample_workload(w, max_T):
+    """Same workload with the time axis cut to max_T steps (CPU sample)."""
+    s = dict(w)
+    s["T"] = min(w["T"], max_T)
+    return s
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return None
+    # bounded sample: the full batch/head shape, time axis cut so a step is ~seconds
+    sw = sample_workload(w, 256 if w["Dh"] <= 256 else 64)
+    d = workload_inputs(args.workload, T=sw["T"])
+    for _ in range(args.warmup):
+        oracle_rate(sw, d, budget_s=0.0)
+    times = []
+    for _ in range(args.steps):
+        rate, reps, el = oracle_rate(sw, d, budget_s=0.0)
+        times.append(el)
+    t = sum(times) / len(times)
+    value = flops_per_step(sw) / t / 1e12
+    cores = blas_threads()
+    sample = f"{args.workload} with T cut to {sw['T']} steps, one oracle pass per step"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, **{k: w[k] for k in ("cell", "NH", "Dh", "B", "T")},
+                       "sample_T": sw["T"]},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def kernel_source_hash():
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "sequential_rnn_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per launch from a committed ncu summary, if it matches these sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        j = json.load(f)
+    e = j.get(workload)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+    import sequential_rnn_gb300 as S
+    from sequential_rnn_gb300 import build as B
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    d = workload_inputs(args.workload, seed=rank)
+    cell = w["cell"]
+    dt = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
+    g = {k: torch.from_numpy(np.ascontiguousarray(d[k])).to(dev, dt) for k in ("Wx", "R")}
+    for k in ("b", "h0", "c0", "n0", "m0"):
+        g[k] = torch.from_numpy(np.ascontiguousarray(d[k])).to(dev, torch.float32)
+    if w["backward"]:
+        g["dh"] = torch.from_numpy(np.ascontiguousarray(d["dh"])).to(dev, dt)
+    T, Bsz, NH, Dh = w["T"], w["B"], w["NH"], w["Dh"]
+    G = GATES[cell]
+    flags = S.RNN_FLAG_TRAIN if w["backward"] else 0
+    desc = S.make_desc(cell, w["dtype"], T, Bsz, NH, Dh, flags, args.cluster)
+    cfg = S.rnn_fwd_config(desc)
+    f32 = dict(dtype=torch.float32, device=dev)
+    h_seq = torch.empty((T, Bsz, NH, Dh), dtype=dt, device=dev)
+    hT = torch.empty((Bsz, NH, Dh), **f32)
+    cT = torch.empty((Bsz, NH, Dh), **f32) if cell != "gru" else None
+    nT = torch.empty((Bsz, NH, Dh), **f32) if cell == "slstm" else None
+    mT = torch.empty((Bsz, NH, Dh), **f32) if cell == "slstm" else None
+    ws = torch.zeros(S.rnn_workspace_size(desc, 0), dtype=torch.uint8, device=dev)
+    stash = torch.empty(max(S.rnn_stash_size(desc) // 4, 1), **f32) if w["backward"] else None
+    if w["backward"]:
+        gr = {"dWx": torch.empty_like(g["Wx"]), "dR": torch.empty((NH, Dh, G * Dh), **f32),
+              "db": torch.empty((NH, G * Dh), **f32), "dh0": torch.empty((Bsz, NH, Dh), **f32),
+              "dc0": torch.empty((Bsz, NH, Dh), **f32)}
+        wsb = torch.zeros(S.rnn_workspace_size(desc, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    launches_per_step = 1
+
+    def step(Wx=None, R=None):
+        st = S.rnn_fwd(desc, g["Wx"] if Wx is None else Wx, g["R"] if R is None else R, g["b"],
+                       g["h0"], g["c0"], g["n0"] if cell == "slstm" else None,
+                       g["m0"] if cell == "slstm" else None, h_seq, hT, cT, nT, mT, stash, ws,
+                       stream)
+        if st:
+            raise S.RnnError(st, "rnn_fwd")
+        if w["backward"]:
+            st = S.rnn_bwd(desc, g["R"] if R is None else R, g["h0"], h_seq, stash, g["dh"], None,
+                           None, gr["dWx"], gr["dR"], gr["db"], gr["dh0"], gr["dc0"], wsb, stream)
+            if st:
+                raise S.RnnError(st, "rnn_bwd")
+
+    if w["backward"]:
+        launches_per_step = 5  # fwd, h0->bf16, bwd recurrence, dR GEMM, db reduce
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    w0 = time.perf_counter()
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if S.rnn_read_status(ws):
+        raise S.RnnError(S.rnn_read_status(ws), "warm-up (device)")
+    if args.steps is None:  # ~2 s of timed work so the clock samples see it
+        t1 = (time.perf_counter() - w0) / max(args.warmup, 3)
+        args.steps = int(min(3000, max(20, 2.0 / max(t1, 1e-5))))
+
+    # ---- device-resident timing: events around each step, L2 flushed between
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier()
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    with ClockSampler(uuid if uuid.startswith("GPU-") else f"GPU-{uuid}") as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        barrier()
+        wall = time.perf_counter() - wall0
+    per = [a.elapsed_time(b) for a, b in ev]  # ms
+    t_step = sum(per) / len(per) / 1e3
+    # max over ranks
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([t_step], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step = float(tt.item())
+    if S.rnn_read_status(ws):
+        raise S.RnnError(S.rnn_read_status(ws), "timed region (device)")
+
+    # ---- sync floor of the same launch shape
+    fl_ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    fdesc = S.make_desc(cell, w["dtype"], T, Bsz, NH, Dh, 0, args.cluster)
+    fe = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    for _ in range(3):
+        S.rnn_sync_floor(fdesc, T, fl_ws, stream)
+    fl = []
+    for _ in range(10):
+        fe[0].record(stream)
+        st = S.rnn_sync_floor(fdesc, T, fl_ws, stream)
+        fe[1].record(stream)
+        torch.cuda.synchronize(dev)
+        if st:
+            raise S.RnnError(st, "rnn_sync_floor")
+        fl.append(fe[0].elapsed_time(fe[1]) / 1e3)
+    t_floor = statistics.median(fl) / T
+
+    # ---- end to end through the C ABI with pinned host buffers
+    hWx = g["Wx"].cpu().pin_memory()
+    hR = g["R"].cpu().pin_memory()
+    hh = torch.empty(h_seq.shape, dtype=dt).pin_memory()
+    dWx = torch.empty_like(g["Wx"])
+    dR = torch.empty_like(g["R"])
+    e2e_steps = max(3, min(args.steps, 50))
+    ee = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    for _ in range(2):
+        dWx.copy_(hWx, non_blocking=True)
+        dR.copy_(hR, non_blocking=True)
+        step(dWx, dR)
+        hh.copy_(h_seq, non_blocking=True)
+    barrier()
+    ee[0].record(stream)
+    for _ in range(e2e_steps):
+        dWx.copy_(hWx, non_blocking=True)
+        dR.copy_(hR, non_blocking=True)
+        step(dWx, dR)
+        hh.copy_(h_seq, non_blocking=True)
+    ee[1].record(stream)
+    barrier()
+    t_e2e = ee[0].elapsed_time(ee[1]) / 1e3 / e2e_steps
+    h2d = hWx.numel() * hWx.element_size() + hR.numel() * hR.element_size()
+    d2h = hh.numel() * hh.element_size()
+
+    fl_step = flops_per_step(w)
+    hbm, tflops_peak, peak_kind = load_peaks()
+    per_step_bytes, total_bytes = algorithmic_bytes_fwd(w)
+    # per-step roofline: slower of bytes at HBM and flops at the tensor pipe, plus the floor
+    t_bytes = per_step_bytes / (hbm * 1e9)
+    t_flop = 2.0 * Bsz * NH * Dh * G * Dh / (tflops_peak * 1e12)
+    t_roof = max(t_bytes, t_flop) + t_floor
+    t_meas_step = t_step / T
+    achieved_gbs = total_bytes / t_step / 1e9 if not w["backward"] else None
+    res = {
+        "metric": METRIC, "value": world * fl_step / t_step / 1e12, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
+        "config": {"workload": args.workload, "cell": cell, "NH": NH, "Dh": Dh, "B": Bsz, "T": T,
+                   "l2": "flushed before every timed step (2x L2 write, outside the events)",
+                   "launch": cfg, "parallelism": f"weak x{world}: one independent batch per GPU"},
+        "steps_per_s": world * T / t_step,
+        "per_step_ns": t_meas_step * 1e9,
+        "per_step_roofline": {
+            "bytes_ns": t_bytes * 1e9, "flops_ns": t_flop * 1e9, "sync_floor_ns": t_floor * 1e9,
+            "roofline_ns": t_roof * 1e9, "frac": t_roof / t_meas_step,
+            "peaks": f"{peak_kind}: {hbm} GB/s, {tflops_peak} TFLOP/s bf16"},
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": (achieved_gbs / hbm) if achieved_gbs else None,
+                     "traffic": ncu_traffic(args.workload),
+                     "note": f"algorithmic bytes {total_bytes} per launch / event time; "
+                             f"peak {peak_kind} HBM copy bandwidth"},
+        "e2e": {"value": world * fl_step / t_e2e / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clk.summary(),
+        "wall_timed_s": wall,
+    }
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for ~2 s of timed work, 20..3000)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cluster", type=int, default=0, help="CTAs per head (0 = automatic)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = dict(WORKLOADS[args.workload])
+
+    if args.impl == "reference":
+        if args.steps is None:
+            args.steps = 3
+        res = run_reference(args, w, rank)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
+
+    # CPU baseline first (before any GPU work): the oracle on the host cores
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        sw = sample_workload(w, 256 if w["Dh"] <= 256 else 64)
+        d = workload_inputs(args.workload, T=sw["T"])
+        rate, reps, el = oracle_rate(sw, d, budget_s=10.0)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{args.workload} with T cut to {sw['T']}, {reps} oracle passes in {el:.1f} s"}
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_ours(args, w, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        res["cpu_baseline"] = cpu
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,132 @@
+/*
+ * sequential_rnn_gb300 -- C ABI of the head-wise RNN recurrence on GB300 (sm_103a).
+ *
+ * What is computed (FlashRNN pages: "FlashRNN: I/O-Aware Optimization of
+ * Traditional RNNs on modern hardware", abstract -- LSTM, GRU and sLSTM
+ * processed as many small heads; blog page "re-examining RNNs from a GPU
+ * programming perspective", register-caching and head-wise paragraphs -- the
+ * recurrent matrix R stays on chip across the time loop, heads form a
+ * block-diagonal R and map to separate thread blocks):
+ *
+ *   for each head h, batch row b, step t = 0..T-1:
+ *     pre_t = Wx[t,b,h,:] + h_{t-1}[b,h,:] @ R[h] + bias[h]        (row vectors)
+ *     cell update (below) -> h_t, c_t (, n_t, m_t)
+ *
+ *   LSTM  gates (i,f,z,o): i,f,o = sigmoid, z = tanh; c = f*c + i*z; h = o*tanh(c)
+ *   GRU   gates (r,z,n):   rec = h_{t-1}@R + bias; r = sigm(Wx_r+rec_r);
+ *                          z = sigm(Wx_z+rec_z); n = tanh(Wx_n + r*rec_n);
+ *                          h = (1-z)*n + z*h_{t-1}
+ *   sLSTM gates (i,f,z,o): m_t = max(f~+m, i~); i = exp(i~-m_t); f = exp(f~+m-m_t);
+ *                          c = f*c + i*tanh(z~); n = f*n + i; h = sigm(o~)*c/n
+ *
+ * Layouts (all row-major, contiguous; G = 4 for LSTM/sLSTM, 3 for GRU):
+ *   Wx     [T, B, NH, G*Dh]  input dtype     gate-major: column g*Dh + j = gate g, unit j
+ *   R      [NH, Dh, G*Dh]    input dtype
+ *   bias   [NH, G*Dh]        fp32            (NULL = zeros)
+ *   h0,c0,n0,m0 [B, NH, Dh]  fp32            (NULL = zeros; c0 unused by GRU, n0/m0 sLSTM only)
+ *   h_seq  [T, B, NH, Dh]    input dtype     h_t for every step (bf16: rounded to nearest even)
+ *   hT,cT,nT,mT [B, NH, Dh]  fp32            final states (NULL = not written)
+ *
+ * Numerics: RNN_F32 computes in fp32 throughout (fp32 FMA contraction,
+ * accurate exp/tanh).  RNN_BF16 feeds bf16(h_{t-1}) and bf16 R to the tensor
+ * cores with fp32 accumulation; gate math and all states are fp32.
+ *
+ * Ownership: the caller allocates and owns every buffer (device memory),
+ * including the workspace and the training stash.  Nothing is allocated by
+ * the library.  All calls are asynchronous on `stream` (a cudaStream_t,
+ * NULL = legacy default stream).  Host-side checks fail fast with a status
+ * and launch nothing.  Device-side failures (a bounded wait that ran out) are
+ * recorded in the status word at the start of the workspace; read it with
+ * rnn_read_status().
+ */
+#ifndef SEQUENTIAL_RNN_GB300_RNN_H
+#define SEQUENTIAL_RNN_GB300_RNN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { RNN_LSTM = 0, RNN_GRU = 1, RNN_SLSTM = 2 } rnn_cell_t;
+typedef enum { RNN_F32 = 0, RNN_BF16 = 1 } rnn_dtype_t;
+
+/* desc.flags */
+enum {
+  RNN_FLAG_TRAIN = 1,              /* forward also writes the stash rnn_bwd needs */
+  RNN_FLAG_TEST_TIMEOUT = 1 << 30  /* test only: the kernel waits on a barrier that nothing
+                                      completes, gives up after ~50 ms and reports
+                                      RNN_ERR_TIMEOUT in the status word */
+};
+
+typedef struct {
+  int32_t cell;    /* rnn_cell_t */
+  int32_t dtype;   /* rnn_dtype_t: type of Wx, R, h_seq, dh_seq, dWx */
+  int32_t T, B, NH, Dh;
+  int32_t flags;   /* RNN_FLAG_* */
+  int32_t cluster; /* 0 = automatic; else CTAs per head for bf16 (1,2,4,8,16) */
+} rnn_desc_t;
+
+typedef enum {
+  RNN_OK = 0,
+  RNN_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad enum, small workspace */
+  RNN_ERR_UNSUPPORTED = 2, /* shape/dtype/cell combination without a kernel */
+  RNN_ERR_MISALIGNED = 3,  /* a pointer violates the alignment stated below */
+  RNN_ERR_LAUNCH = 4,      /* the CUDA launch itself failed */
+  RNN_ERR_TIMEOUT = 5,     /* device status: a bounded wait ran out, outputs invalid */
+  RNN_ERR_NO_CLUSTER = 6   /* the device cannot co-schedule the needed thread-block cluster */
+} rnn_status_t;
+
+/* Bytes of device workspace rnn_fwd (pass 0) / rnn_bwd (pass 1) need.
+ * Always >= 256 (the status word lives at offset 0).  0 on invalid desc. */
+size_t rnn_workspace_size(const rnn_desc_t* desc, int pass);
+
+/* Bytes of the training stash rnn_fwd writes with RNN_FLAG_TRAIN (LSTM:
+ * gate activations fp32 [T,B,NH,4*Dh] then c_t fp32 [T,B,NH,Dh]).  Opaque to
+ * the caller; pass the same buffer to rnn_bwd.  0 for cells without backward. */
+size_t rnn_stash_size(const rnn_desc_t* desc);
+
+/* Forward recurrence.  Alignment: Wx, R 16 bytes; h_seq 4 bytes; fp32
+ * pointers 4 bytes.  Supported: RNN_F32 with Dh in {16,32,64};
+ * RNN_BF16 with Dh in {32,64,128,256,768} (Dh > 128 runs as a thread-block
+ * cluster per head).  T == 0 copies the initial states to the final ones;
+ * B == 0 or NH == 0 is a no-op.  Returns rnn_status_t. */
+int rnn_fwd(const rnn_desc_t* desc, const void* Wx, const void* R, const float* bias,
+            const float* h0, const float* c0, const float* n0, const float* m0, void* h_seq,
+            float* hT, float* cT, float* nT, float* mT, void* stash, void* workspace,
+            size_t workspace_bytes, void* stream);
+
+/* Backward through time of the LSTM (RNN_BF16, the same Dh set), from the
+ * stash of a RNN_FLAG_TRAIN forward with the same desc, inputs and h_seq.
+ * Gradients of L = sum(h_seq*dh_seq) + sum(hT*dhT) + sum(cT*dcT):
+ *   dWx [T,B,NH,4Dh] input dtype, dR [NH,Dh,4Dh] fp32, db [NH,4Dh] fp32,
+ *   dh0, dc0 [B,NH,Dh] fp32 (any of dR/db/dh0/dc0 may be NULL).
+ * dhT, dcT NULL = zero.  dh_seq: input dtype, 16-byte aligned. */
+int rnn_bwd(const rnn_desc_t* desc, const void* R, const float* h0, const void* h_seq,
+            const void* stash, const void* dh_seq, const float* dhT, const float* dcT, void* dWx,
+            float* dR, float* db, float* dh0, float* dc0, void* workspace, size_t workspace_bytes,
+            void* stream);
+
+/* Synchronises `stream`, reads the device status word of `workspace` into
+ * *device_status (RNN_OK or RNN_ERR_TIMEOUT).  Returns RNN_OK if the read
+ * itself worked, else RNN_ERR_LAUNCH. */
+int rnn_read_status(const void* workspace, void* stream, int* device_status);
+
+/* Measurement aid: runs `iters` iterations of only the per-step
+ * synchronisation of the rnn_fwd launch `desc` selects (same grid, cluster
+ * shape and barrier kind, no loads and no math).  Its time / iters is the
+ * sync floor of one step. */
+int rnn_sync_floor(const rnn_desc_t* desc, int iters, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
+/* Launch geometry rnn_fwd would use: out[0..5] = grid CTAs, threads per CTA,
+ * cluster size, batch rows per CTA, dynamic smem bytes, kernel id. */
+int rnn_fwd_config(const rnn_desc_t* desc, int32_t* out6);
+
+const char* rnn_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SEQUENTIAL_RNN_GB300_RNN_H */

@@ -1,0 +1,170 @@
+"""sequential_rnn_gb300: head-wise LSTM / GRU / sLSTM recurrence on GB300 (sm_103a).
+
+Python binding of the C ABI in include/rnn.h.  The functions named like the C
+entry points (``rnn_fwd``, ``rnn_bwd``, ...) take torch tensors (or None) and
+only marshal arguments: device pointers, sizes and the current CUDA stream.
+``forward`` / ``backward`` additionally allocate the outputs with torch and
+raise ``RnnError`` on a non-OK status.  Every step of the recurrence runs in
+the library's CUDA kernels; there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import (CELLS, DTYPES, RNN_BF16, RNN_F32, RNN_FLAG_TEST_TIMEOUT, RNN_FLAG_TRAIN,
+                   STATUS, rnn_desc_t)
+
+__all__ = ["RnnError", "make_desc", "rnn_workspace_size", "rnn_stash_size", "rnn_fwd", "rnn_bwd",
+           "rnn_read_status", "rnn_sync_floor", "rnn_fwd_config", "rnn_status_str", "forward",
+           "backward", "GATES"]
+
+GATES = {"lstm": 4, "gru": 3, "slstm": 4}
+
+
+class RnnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({rnn_status_str(status)})")
+
+
+def make_desc(cell: str, dtype: str, T: int, B: int, NH: int, Dh: int, flags: int = 0,
+              cluster: int = 0) -> rnn_desc_t:
+    return rnn_desc_t(CELLS[cell], DTYPES[dtype], T, B, NH, Dh, flags, cluster)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor or None")
+    if t.numel() and not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+# ------------------------------------------------------ C-named wrappers --
+def rnn_status_str(status: int) -> str:
+    return _lib.load().rnn_status_str(int(status)).decode()
+
+
+def rnn_workspace_size(desc: rnn_desc_t, pass_: int = 0) -> int:
+    return int(_lib.load().rnn_workspace_size(ctypes.byref(desc), int(pass_)))
+
+
+def rnn_stash_size(desc: rnn_desc_t) -> int:
+    return int(_lib.load().rnn_stash_size(ctypes.byref(desc)))
+
+
+def rnn_fwd_config(desc: rnn_desc_t):
+    out = (ctypes.c_int32 * 6)()
+    st = _lib.load().rnn_fwd_config(ctypes.byref(desc), out)
+    if st:
+        raise RnnError(st, "rnn_fwd_config")
+    return dict(zip(("grid", "threads", "cluster", "nb", "smem", "kernel_id"), list(out)))
+
+
+def rnn_fwd(desc, Wx, R, bias, h0, c0, n0, m0, h_seq, hT, cT, nT, mT, stash, workspace,
+            stream=None) -> int:
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return int(_lib.load().rnn_fwd(
+        ctypes.byref(desc), _ptr(Wx), _ptr(R), _ptr(bias), _ptr(h0), _ptr(c0), _ptr(n0), _ptr(m0),
+        _ptr(h_seq), _ptr(hT), _ptr(cT), _ptr(nT), _ptr(mT), _ptr(stash), _ptr(workspace),
+        ws_bytes, _stream(stream)))
+
+
+def rnn_bwd(desc, R, h0, h_seq, stash, dh_seq, dhT, dcT, dWx, dR, db, dh0, dc0, workspace,
+            stream=None) -> int:
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return int(_lib.load().rnn_bwd(
+        ctypes.byref(desc), _ptr(R), _ptr(h0), _ptr(h_seq), _ptr(stash), _ptr(dh_seq), _ptr(dhT),
+        _ptr(dcT), _ptr(dWx), _ptr(dR), _ptr(db), _ptr(dh0), _ptr(dc0), _ptr(workspace), ws_bytes,
+        _stream(stream)))
+
+
+def rnn_read_status(workspace, stream=None) -> int:
+    v = ctypes.c_int(0)
+    st = _lib.load().rnn_read_status(_ptr(workspace), _stream(stream), ctypes.byref(v))
+    if st:
+        raise RnnError(st, "rnn_read_status")
+    return int(v.value)
+
+
+def rnn_sync_floor(desc, iters: int, workspace, stream=None) -> int:
+    ws_bytes = workspace.numel() * workspace.element_size()
+    return int(_lib.load().rnn_sync_floor(ctypes.byref(desc), int(iters), _ptr(workspace), ws_bytes,
+                                          _stream(stream)))
+
+
+# ------------------------------------------------------- conveniences ----
+def _dtype_name(t: torch.Tensor) -> str:
+    if t.dtype == torch.bfloat16:
+        return "bf16"
+    if t.dtype == torch.float32:
+        return "f32"
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def forward(cell: str, Wx, R, bias=None, h0=None, c0=None, n0=None, m0=None, *, train=False,
+            cluster=0, test_timeout=False, stream=None, check=True):
+    """Allocate outputs and run rnn_fwd.  Wx [T,B,NH,G*Dh], R [NH,Dh,G*Dh]."""
+    T, B, NH, _ = Wx.shape
+    Dh = R.shape[1]
+    flags = (RNN_FLAG_TRAIN if train else 0) | (RNN_FLAG_TEST_TIMEOUT if test_timeout else 0)
+    desc = make_desc(cell, _dtype_name(Wx), T, B, NH, Dh, flags, cluster)
+    dev = Wx.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = {"desc": desc,
+           "h_seq": torch.empty((T, B, NH, Dh), dtype=Wx.dtype, device=dev),
+           "hT": torch.empty((B, NH, Dh), **f32)}
+    if cell != "gru":
+        out["cT"] = torch.empty((B, NH, Dh), **f32)
+    if cell == "slstm":
+        out["nT"] = torch.empty((B, NH, Dh), **f32)
+        out["mT"] = torch.empty((B, NH, Dh), **f32)
+    out["workspace"] = torch.zeros(max(rnn_workspace_size(desc, 0), 256), dtype=torch.uint8, device=dev)
+    out["stash"] = (torch.empty(max(rnn_stash_size(desc) // 4, 1), **f32) if train else None)
+    st = rnn_fwd(desc, Wx, R, bias, h0, c0, n0, m0, out["h_seq"], out["hT"], out.get("cT"),
+                 out.get("nT"), out.get("mT"), out["stash"], out["workspace"], stream)
+    if st:
+        raise RnnError(st, "rnn_fwd")
+    if check:
+        dst = rnn_read_status(out["workspace"], stream)
+        if dst:
+            raise RnnError(dst, "rnn_fwd (device)")
+    return out
+
+
+def backward(fwd: dict, R, h0, dh_seq, dhT=None, dcT=None, *, stream=None, check=True):
+    """Run rnn_bwd after ``forward(..., train=True)``; returns the gradients."""
+    desc = fwd["desc"]
+    T, B, NH, Dh = desc.T, desc.B, desc.NH, desc.Dh
+    G = 4
+    dev = R.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = {"dWx": torch.empty((T, B, NH, G * Dh), dtype=R.dtype, device=dev),
+         "dR": torch.empty((NH, Dh, G * Dh), **f32), "db": torch.empty((NH, G * Dh), **f32),
+         "dh0": torch.empty((B, NH, Dh), **f32), "dc0": torch.empty((B, NH, Dh), **f32)}
+    ws = torch.zeros(rnn_workspace_size(desc, 1), dtype=torch.uint8, device=dev)
+    st = rnn_bwd(desc, R, h0, fwd["h_seq"], fwd["stash"], dh_seq, dhT, dcT, g["dWx"], g["dR"],
+                 g["db"], g["dh0"], g["dc0"], ws, stream)
+    if st:
+        raise RnnError(st, "rnn_bwd")
+    if check:
+        dst = rnn_read_status(ws, stream)
+        if dst:
+            raise RnnError(dst, "rnn_bwd (device)")
+    g["workspace"] = ws
+    return g

@@ -1,0 +1,264 @@
+// C ABI of the head-wise RNN recurrence (declared in include/rnn.h):
+// argument checks, kernel-variant selection, launch geometry and launches on
+// the caller's stream.  The library allocates no device memory.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/rnn.h"
+#include "kernels.h"
+
+using namespace srnn;
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;
+constexpr unsigned long long kTimeoutNs = 2000000000ull;      // 2 s per wait
+constexpr unsigned long long kTestTimeoutNs = 50000000ull;    // 50 ms under the test flag
+
+int gates_of(int cell) { return cell == RNN_GRU ? 3 : 4; }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int check_desc(const rnn_desc_t* d) {
+  if (d == nullptr) return RNN_ERR_INVALID_ARG;
+  if (d->cell < RNN_LSTM || d->cell > RNN_SLSTM) return RNN_ERR_INVALID_ARG;
+  if (d->dtype != RNN_F32 && d->dtype != RNN_BF16) return RNN_ERR_INVALID_ARG;
+  if (d->T < 0 || d->B < 0 || d->NH < 0 || d->Dh <= 0) return RNN_ERR_INVALID_ARG;
+  if (d->cluster < 0) return RNN_ERR_INVALID_ARG;
+  return RNN_OK;
+}
+
+// Default CTAs per head for the bf16 kernels: as few as hold R on chip.
+int default_cluster(int cell, int Dh) {
+  if (Dh <= 64) return 1;
+  if (Dh == 128) return cell == RNN_GRU ? 1 : 2;
+  if (Dh == 256) return 8;
+  return 16;
+}
+
+bool bf16_dh_supported(int Dh) {
+  return Dh == 32 || Dh == 64 || Dh == 128 || Dh == 256 || Dh == 768;
+}
+
+struct Plan {
+  bool f32;
+  int CS, U, NT, NB, nbslices;
+};
+
+int make_plan(const rnn_desc_t* d, Plan* pl) {
+  if (d->dtype == RNN_F32) {
+    if (d->Dh != 16 && d->Dh != 32 && d->Dh != 64) return RNN_ERR_UNSUPPORTED;
+    if (d->cluster > 1) return RNN_ERR_UNSUPPORTED;
+    pl->f32 = true;
+    pl->CS = 1;
+    pl->U = d->Dh;
+    pl->NT = 1;
+    pl->NB = 8;
+  } else {
+    if (!bf16_dh_supported(d->Dh)) return RNN_ERR_UNSUPPORTED;
+    const int cs = d->cluster ? d->cluster : default_cluster(d->cell, d->Dh);
+    if (cs != 1 && cs != 2 && cs != 4 && cs != 8 && cs != 16) return RNN_ERR_UNSUPPORTED;
+    if (d->Dh % cs) return RNN_ERR_UNSUPPORTED;
+    const int U = d->Dh / cs;
+    if (U % bf16_unit_group(d->cell)) return RNN_ERR_UNSUPPORTED;
+    pl->f32 = false;
+    pl->CS = cs;
+    pl->U = U;
+    pl->NT = 1;
+    pl->NB = 8;
+  }
+  pl->nbslices = (d->B + pl->NB - 1) / pl->NB;
+  return RNN_OK;
+}
+
+int map_launch_error(int e) {
+  if (e == 0) return RNN_OK;
+  if (e == -1) return RNN_ERR_NO_CLUSTER;
+  if (e == (int)cudaErrorInvalidConfiguration || e == (int)cudaErrorInvalidValue)
+    return RNN_ERR_UNSUPPORTED;
+  return RNN_ERR_LAUNCH;
+}
+
+int launch_forward(const rnn_desc_t* d, const Plan& pl, const FwdParams& p, cudaStream_t s,
+                   bool query_only, LaunchInfo* info) {
+  if (pl.f32) return launch_fwd_f32(p, d->cell, d->Dh, s, query_only, info);
+  switch (d->cell) {
+    case RNN_LSTM: return launch_fwd_bf16_lstm(p, d->Dh, pl.NT, s, query_only, info);
+    case RNN_GRU: return launch_fwd_bf16_gru(p, d->Dh, pl.NT, s, query_only, info);
+    default: return launch_fwd_bf16_slstm(p, d->Dh, pl.NT, s, query_only, info);
+  }
+}
+
+FwdParams base_params(const rnn_desc_t* d, const Plan& pl) {
+  FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.T = d->T;
+  p.B = d->B;
+  p.NH = d->NH;
+  p.CS = pl.CS;
+  p.U = pl.U;
+  p.NS = 2;
+  p.nbslices = pl.nbslices;
+  p.flags = d->flags;
+  p.timeout_ns = (d->flags & RNN_FLAG_TEST_TIMEOUT) ? kTestTimeoutNs : kTimeoutNs;
+  return p;
+}
+
+// Final state <- initial state (or zero) for a zero-length sequence.
+int copy_state(float* dst, const float* src, size_t n, cudaStream_t s) {
+  if (dst == nullptr) return RNN_OK;
+  cudaError_t e = src ? cudaMemcpyAsync(dst, src, n * sizeof(float), cudaMemcpyDeviceToDevice, s)
+                      : cudaMemsetAsync(dst, 0, n * sizeof(float), s);
+  return e == cudaSuccess ? RNN_OK : RNN_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rnn_status_str(int status) {
+  switch (status) {
+    case RNN_OK: return "ok";
+    case RNN_ERR_INVALID_ARG: return "invalid argument";
+    case RNN_ERR_UNSUPPORTED: return "unsupported shape, dtype or cell";
+    case RNN_ERR_MISALIGNED: return "misaligned pointer";
+    case RNN_ERR_LAUNCH: return "CUDA launch failed";
+    case RNN_ERR_TIMEOUT: return "device wait timed out";
+    case RNN_ERR_NO_CLUSTER: return "thread-block cluster cannot be scheduled";
+    default: return "unknown status";
+  }
+}
+
+size_t rnn_stash_size(const rnn_desc_t* d) {
+  if (check_desc(d) != RNN_OK || d->cell != RNN_LSTM) return 0;
+  const size_t cells = (size_t)d->T * d->B * d->NH * d->Dh;
+  return cells * 5 * sizeof(float);  // activations (4 gates) + c_t
+}
+
+size_t rnn_workspace_size(const rnn_desc_t* d, int pass) {
+  if (check_desc(d) != RNN_OK) return 0;
+  if (pass == 0) return kStatusBytes;
+  // backward: status | bf16(h0) [B,NH,Dh] | bias-gradient partials [slices,NH,4Dh] fp32
+  const size_t nb = (size_t)((d->B + 7) / 8);
+  size_t o = kStatusBytes;
+  o += align_up((size_t)d->B * d->NH * d->Dh * 2, 256);
+  o += align_up(nb * d->NH * 4 * d->Dh * sizeof(float), 256);
+  return o;
+}
+
+int rnn_fwd_config(const rnn_desc_t* d, int32_t* out6) {
+  int st = check_desc(d);
+  if (st != RNN_OK) return st;
+  if (out6 == nullptr) return RNN_ERR_INVALID_ARG;
+  Plan pl;
+  if ((st = make_plan(d, &pl)) != RNN_OK) return st;
+  LaunchInfo li{};
+  FwdParams p = base_params(d, pl);
+  int e = launch_forward(d, pl, p, nullptr, true, &li);
+  if (e != 0) return map_launch_error(e);
+  out6[0] = li.grid;
+  out6[1] = li.threads;
+  out6[2] = li.cluster;
+  out6[3] = li.nb;
+  out6[4] = li.smem;
+  out6[5] = li.kernel_id;
+  return RNN_OK;
+}
+
+int rnn_fwd(const rnn_desc_t* d, const void* Wx, const void* R, const float* bias,
+            const float* h0, const float* c0, const float* n0, const float* m0, void* h_seq,
+            float* hT, float* cT, float* nT, float* mT, void* stash, void* workspace,
+            size_t workspace_bytes, void* stream) {
+  int st = check_desc(d);
+  if (st != RNN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d->B == 0 || d->NH == 0) return RNN_OK;
+  Plan pl;
+  if ((st = make_plan(d, &pl)) != RNN_OK) return st;
+  if (workspace == nullptr || workspace_bytes < rnn_workspace_size(d, 0)) return RNN_ERR_INVALID_ARG;
+  const bool train = (d->flags & RNN_FLAG_TRAIN) != 0;
+  if (train && (d->cell != RNN_LSTM || d->dtype != RNN_BF16)) return RNN_ERR_UNSUPPORTED;
+  if (train && stash == nullptr) return RNN_ERR_INVALID_ARG;
+  if (!aligned(workspace, 16)) return RNN_ERR_MISALIGNED;
+  const size_t nstate = (size_t)d->B * d->NH * d->Dh;
+  if (d->T == 0) {
+    int r;
+    if ((r = copy_state(hT, h0, nstate, s)) != RNN_OK) return r;
+    if (d->cell != RNN_GRU && (r = copy_state(cT, c0, nstate, s)) != RNN_OK) return r;
+    if (d->cell == RNN_SLSTM) {
+      if ((r = copy_state(nT, n0, nstate, s)) != RNN_OK) return r;
+      if ((r = copy_state(mT, m0, nstate, s)) != RNN_OK) return r;
+    }
+    return RNN_OK;
+  }
+  if (Wx == nullptr || R == nullptr || h_seq == nullptr) return RNN_ERR_INVALID_ARG;
+  if (!aligned(Wx, 16) || !aligned(R, 16) || !aligned(h_seq, 4) || !aligned(stash, 16))
+    return RNN_ERR_MISALIGNED;
+  const float* fp[] = {bias, h0, c0, n0, m0, hT, cT, nT, mT};
+  for (const float* q : fp)
+    if (!aligned(q, 4)) return RNN_ERR_MISALIGNED;
+
+  FwdParams p = base_params(d, pl);
+  p.Wx = Wx;
+  p.R = R;
+  p.bias = bias;
+  p.h0 = h0;
+  p.c0 = c0;
+  p.n0 = n0;
+  p.m0 = m0;
+  p.h_seq = h_seq;
+  p.hT = hT;
+  p.cT = cT;
+  p.nT = nT;
+  p.mT = mT;
+  if (train) {
+    p.stash_gates = static_cast<float*>(stash);
+    p.stash_c = p.stash_gates + (size_t)d->T * nstate * 4;
+  }
+  p.status = static_cast<int*>(workspace);
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return RNN_ERR_LAUNCH;
+  return map_launch_error(launch_forward(d, pl, p, s, false, nullptr));
+}
+
+int rnn_read_status(const void* workspace, void* stream, int* device_status) {
+  if (workspace == nullptr || device_status == nullptr) return RNN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return RNN_ERR_LAUNCH;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RNN_ERR_LAUNCH;
+  *device_status = (v & kStatusTimeout) ? RNN_ERR_TIMEOUT : RNN_OK;
+  return RNN_OK;
+}
+
+int rnn_sync_floor(const rnn_desc_t* d, int iters, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  int st = check_desc(d);
+  if (st != RNN_OK) return st;
+  if (iters < 0 || workspace == nullptr || workspace_bytes < kStatusBytes) return RNN_ERR_INVALID_ARG;
+  if (d->B == 0 || d->NH == 0 || iters == 0) return RNN_OK;
+  Plan pl;
+  if ((st = make_plan(d, &pl)) != RNN_OK) return st;
+  LaunchInfo li{};
+  FwdParams p = base_params(d, pl);
+  int e = launch_forward(d, pl, p, nullptr, true, &li);
+  if (e != 0) return map_launch_error(e);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return RNN_ERR_LAUNCH;
+  return map_launch_error(launch_sync_floor(li, iters, static_cast<int*>(workspace), s));
+}
+
+int rnn_bwd(const rnn_desc_t* d, const void* R, const float* h0, const void* h_seq,
+            const void* stash, const void* dh_seq, const float* dhT, const float* dcT, void* dWx,
+            float* dR, float* db, float* dh0, float* dc0, void* workspace, size_t workspace_bytes,
+            void* stream) {
+  (void)R; (void)h0; (void)h_seq; (void)stash; (void)dh_seq; (void)dhT; (void)dcT; (void)dWx;
+  (void)dR; (void)db; (void)dh0; (void)dc0; (void)workspace; (void)workspace_bytes; (void)stream;
+  int st = check_desc(d);
+  if (st != RNN_OK) return st;
+  return RNN_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

@@ -1,0 +1,517 @@
+// Persistent bf16 forward of the head-wise recurrence (LSTM / GRU / sLSTM).
+//
+// FlashRNN pages: the recurrent matrix stays on chip for the whole time loop
+// (blog page, register-caching paragraph) and heads are independent blocks of
+// a block-diagonal R mapped to separate thread blocks (blog page, head-wise
+// paragraph).  On sm_103a one head (or one batch slice of a head) is one CTA;
+// a head too large for one SM is split by hidden unit over the CTAs of a
+// thread-block cluster, which exchange h_t through distributed shared memory.
+//
+// Per CTA: U = Dh / CS hidden units, all G gates of each unit.  Warp w owns UG
+// units (G*UG gate rows = MT m16 tiles).  The contraction is "swap-AB":
+//     acc[gate rows, batch] = R^T[gate rows, Dh] * h_{t-1}^T[Dh, batch]
+// with R^T as the mma.sync A operand (fragments resident in registers; for
+// very large heads the k-steps >= KREG sit in shared memory in fragment order)
+// and h_{t-1} (bf16) as the B operand read by ldmatrix from a double buffer.
+// A producer warp streams Wx_t with bulk async copies into a ring of NS stages
+// (full/empty mbarriers).  Gate math runs on the accumulator registers; each
+// thread owns whole (unit, batch) cells, so no gate exchange is needed.
+//
+// Exchange of h_t: CS == 1 -> shared memory + one named barrier per step.
+// CS > 1 -> every thread st.async's its bf16 pair of h_t into every cluster
+// CTA's buffer, completing bytes on that CTA's mbarrier; a CTA proceeds to step
+// t+1 when all Dh*NB*2 bytes have landed.  Receiving all of h_t from a peer also
+// proves the peer finished reading the buffer being overwritten next, so one
+// double buffer suffices without a cluster barrier in the loop.
+//
+// Every wait is bounded (globaltimer); on expiry the kernel records
+// kStatusTimeout in the status word, stops, lets in-flight copies land and
+// exits through the same final barriers as a normal run.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace srnn {
+
+template <int CELL, int DH, int UG, int NT, int KREG>
+struct FwdCfg {
+  static constexpr int G = CELL == kGRU ? 3 : 4;
+  static constexpr int GD = G * DH;
+  static constexpr int MT = UG * G / 16;  // m16 tiles per warp
+  static constexpr int KS = DH / 16;      // k16 steps
+  static constexpr int KSM = KS - KREG;   // k-steps whose A fragments live in smem
+  static constexpr int NB = NT * 8;       // batch rows per CTA
+  // h row pitch in bytes: 16-byte chunks per row odd -> ldmatrix conflict-free
+  static constexpr int HPB = ((DH * 2 / 16) % 2 == 0) ? DH * 2 + 16 : DH * 2;
+  static constexpr int NSLOT = UG == 16 ? 2 : 1;  // units per thread
+  static constexpr int NE = NSLOT * NT * 2;       // (unit, batch) cells per thread
+  // register estimate per compute thread -> largest CTA the register file holds
+  static constexpr int REG_EST = MT * KREG * 4 + MT * NT * 8 + 88;
+  static constexpr int MAXT_R = (65536 / REG_EST) / 32 * 32;
+  static constexpr int MAXT = MAXT_R < 17 * 32 ? MAXT_R : 17 * 32;
+  static_assert(UG == 8 || UG == 16, "unit group");
+  static_assert(UG * G % 16 == 0, "gate rows per warp must fill m16 tiles");
+  static_assert(DH % 32 == 0, "Dh multiple of 32");
+  static_assert(KREG >= 0 && KREG <= KS, "KREG");
+};
+
+struct FwdSmem {
+  uint32_t h, wx, rf, bar, flag, total;
+};
+
+template <class C>
+__host__ __device__ inline FwdSmem fwd_smem_layout(int U, int NS) {
+  FwdSmem L;
+  const int NW = U / (C::MT * 16 / C::G);
+  L.h = 0;
+  uint32_t o = 2u * C::NB * C::HPB;
+  o = (o + 127) & ~127u;
+  L.wx = o;
+  o += (uint32_t)NS * C::NB * C::G * U * 2;
+  o = (o + 127) & ~127u;
+  L.rf = o;
+  o += (uint32_t)NW * C::MT * C::KSM * 512;
+  o = (o + 15) & ~15u;
+  L.bar = o;
+  o += (uint32_t)(2 * NS + 3) * 8;
+  L.flag = o;
+  o += 16;
+  L.total = o;
+  return L;
+}
+
+// Bounded wait on an mbarrier phase.  False: gave up (abort recorded).
+template <bool CLUSTER_ACQ>
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           int* status, unsigned long long limit_ns) {
+  if (CLUSTER_ACQ ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (CLUSTER_ACQ ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+template <int CELL, int DH, int UG, int NT, int KREG>
+__global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG>::MAXT, 1) fwd_bf16_kernel(const FwdParams p) {
+  using C = FwdCfg<CELL, DH, UG, NT, KREG>;
+  constexpr int G = C::G, GD = C::GD, MT = C::MT, KS = C::KS, KSM = C::KSM, NB = C::NB;
+  constexpr int HPB = C::HPB, NE = C::NE, NSLOT = C::NSLOT;
+  extern __shared__ __align__(128) uint8_t smem[];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int U = p.U, NW = U / UG, CS = p.CS, NS = p.NS, T = p.T, B = p.B, NH = p.NH;
+  const uint32_t crank = CS > 1 ? cluster_ctarank() : 0u;
+  const int cid = blockIdx.x / CS;
+  const int head = cid / p.nbslices, bslice = cid % p.nbslices;
+  const int u0 = (int)crank * U;
+  const int b0 = bslice * NB;
+  const int nvalid = min(NB, B - b0);
+
+  const FwdSmem L = fwd_smem_layout<C>(U, NS);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t s_h = sbase + L.h, s_wx = sbase + L.wx, s_rf = sbase + L.rf;
+  const uint32_t bar_full = sbase + L.bar, bar_empty = bar_full + 8 * NS;
+  const uint32_t bar_h = bar_empty + 8 * NS;  // two: hfull[0], hfull[1]
+  const uint32_t bar_dummy = bar_h + 16;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flag);
+  const uint32_t stage_bytes = (uint32_t)NB * G * U * 2;
+
+  // ------------------------------------------------------------- set-up --
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, NW);
+    }
+    mbar_init(bar_h, 1);
+    mbar_init(bar_h + 8, 1);
+    mbar_init(bar_dummy, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // batch rows past B: their ring rows stay zero forever (never copied into)
+  if (nvalid < NB) {
+    const int row_bytes = G * U * 2;
+    for (int i = tid; i < NS * (NB - nvalid) * row_bytes / 4; i += blockDim.x) {
+      const int per = (NB - nvalid) * row_bytes / 4;
+      const int s = i / per, r = i % per;
+      *reinterpret_cast<uint32_t*>(smem + L.wx + s * stage_bytes + nvalid * row_bytes + r * 4) = 0u;
+    }
+  }
+  // h_{-1} = bf16(h0) for all Dh units of this batch slice into buffer 0
+  for (int i = tid; i < NB * DH / 2; i += blockDim.x) {
+    const int n = i / (DH / 2), j = 2 * (i % (DH / 2));
+    float v0 = 0.f, v1 = 0.f;
+    if (p.h0 != nullptr && n < nvalid) {
+      const float* src = p.h0 + ((size_t)(b0 + n) * NH + head) * DH + j;
+      v0 = src[0];
+      v1 = src[1];
+    }
+    *reinterpret_cast<uint32_t*>(smem + L.h + n * HPB + j * 2) = pack_bf16x2(v0, v1);
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncthreads();
+  if (tid == 0 && CS > 1) {
+    // h_0 lands in buffer 1, h_1 in buffer 0 (first phase of each)
+    if (T >= 2) mbar_arrive_expect_tx(bar_h + 8, (uint32_t)NB * DH * 2);
+    if (T >= 3) mbar_arrive_expect_tx(bar_h, (uint32_t)NB * DH * 2);
+  }
+  if (CS > 1) cluster_sync();
+  else __syncthreads();
+
+  const unsigned long long tlim = p.timeout_ns;
+
+  if (warp == NW) {
+    // ------------------------------------------------ Wx producer warp --
+    if (lane == 0) {
+      const __nv_bfloat16* Wx = static_cast<const __nv_bfloat16*>(p.Wx);
+      int t = 0;
+      for (; t < T; ++t) {
+        const int s = t % NS, k = t / NS;
+        if (t >= NS && !wait_phase<false>(bar_empty + 8 * s, (k - 1) & 1, abort_flag, p.status, tlim))
+          break;
+        if (*abort_flag) break;
+        mbar_arrive_expect_tx(bar_full + 8 * s, (uint32_t)nvalid * G * U * 2);
+        const uint32_t dst0 = s_wx + s * stage_bytes;
+        for (int n = 0; n < nvalid; ++n) {
+          const __nv_bfloat16* row = Wx + (((size_t)t * B + b0 + n) * NH + head) * GD;
+          if (U == DH) {
+            bulk_g2s(dst0 + n * GD * 2, row, GD * 2, bar_full + 8 * s);
+          } else {
+            for (int g = 0; g < G; ++g)
+              bulk_g2s(dst0 + (n * G + g) * U * 2, row + g * DH + u0, U * 2, bar_full + 8 * s);
+          }
+        }
+      }
+      // let every issued copy land before the CTA can exit
+      for (int tt = max(0, t - NS); tt < t; ++tt) {
+        const int s = tt % NS;
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar_full + 8 * s, (tt / NS) & 1)) {
+          if (globaltimer_ns() - t0 > tlim) break;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------- compute warps --
+    const __nv_bfloat16* Rh = static_cast<const __nv_bfloat16*>(p.R) + (size_t)head * DH * GD;
+    const uint16_t* Rb = reinterpret_cast<const uint16_t*>(Rh);
+    const int ub = warp * UG;  // first CTA-local unit of this warp
+
+    // A fragments of R^T: rows = (gate g, unit u) with row = g*UG + u.
+    uint32_t areg[MT][KREG > 0 ? KREG : 1][4];
+    const uint32_t rf_warp = s_rf + (uint32_t)warp * MT * KSM * 512 + lane * 16;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int ra = mt * 16 + (lane >> 2), rb = ra + 8;
+      const int ca = (ra / UG) * DH + u0 + ub + (ra % UG);
+      const int cb = (rb / UG) * DH + u0 + ub + (rb % UG);
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int k0 = ks * 16 + 2 * (lane & 3);
+        uint32_t a[4];
+        a[0] = (uint32_t)Rb[(size_t)k0 * GD + ca] | ((uint32_t)Rb[(size_t)(k0 + 1) * GD + ca] << 16);
+        a[1] = (uint32_t)Rb[(size_t)k0 * GD + cb] | ((uint32_t)Rb[(size_t)(k0 + 1) * GD + cb] << 16);
+        a[2] = (uint32_t)Rb[(size_t)(k0 + 8) * GD + ca] |
+               ((uint32_t)Rb[(size_t)(k0 + 9) * GD + ca] << 16);
+        a[3] = (uint32_t)Rb[(size_t)(k0 + 8) * GD + cb] |
+               ((uint32_t)Rb[(size_t)(k0 + 9) * GD + cb] << 16);
+        if (ks < KREG) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) areg[mt][ks < KREG ? ks : 0][q] = a[q];
+        } else {
+          const uint32_t addr = rf_warp + (uint32_t)(mt * KSM + (ks - KREG)) * 512;
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a[0]), "r"(a[1]),
+                       "r"(a[2]), "r"(a[3])
+                       : "memory");
+        }
+      }
+    }
+
+    // per-thread cells: slot us (unit), n-tile nt, column e -> index (us*NT+nt)*2+e
+    float bias_v[G][NSLOT];
+#pragma unroll
+    for (int us = 0; us < NSLOT; ++us) {
+      const int j = u0 + ub + (lane >> 2) + 8 * us;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        bias_v[g][us] = p.bias ? p.bias[(size_t)head * GD + g * DH + j] : 0.f;
+    }
+    float st_c[NE], st_n[NE], st_m[NE], st_h[NE];
+#pragma unroll
+    for (int us = 0; us < NSLOT; ++us)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int ei = (us * NT + nt) * 2 + e;
+          const int n = nt * 8 + 2 * (lane & 3) + e;
+          const int j = u0 + ub + (lane >> 2) + 8 * us;
+          const size_t si = ((size_t)(b0 + n) * NH + head) * DH + j;
+          const bool ok = n < nvalid;
+          st_c[ei] = (ok && p.c0) ? p.c0[si] : 0.f;
+          st_n[ei] = (ok && p.n0) ? p.n0[si] : 0.f;
+          st_m[ei] = (ok && p.m0) ? p.m0[si] : 0.f;
+          st_h[ei] = (ok && p.h0) ? p.h0[si] : 0.f;
+        }
+
+    // ldmatrix: lane supplies row (lane & 7) of 8x8 matrix (lane >> 3)
+    const uint32_t lm_off = (uint32_t)(lane & 7) * HPB + (uint32_t)(lane >> 3) * 16;
+    __nv_bfloat16* hseq = static_cast<__nv_bfloat16*>(p.h_seq);
+    const bool train = (p.flags & 1) && CELL == kLSTM && p.stash_gates != nullptr;
+
+    bool dead = false;
+    if (p.flags & (1 << 30)) {  // test hook: a barrier nothing ever completes
+      if (!wait_phase<false>(bar_dummy, 0, abort_flag, p.status, tlim)) dead = true;
+    }
+
+    for (int t = 0; t < T; ++t) {
+      // ---- wait for h_{t-1} (cluster) and Wx_t
+      if (!dead && CS > 1 && t > 0) {
+        if (!wait_phase<true>(bar_h + 8 * (t & 1), ((t - 1) >> 1) & 1, abort_flag, p.status, tlim))
+          dead = true;
+        else if (tid == 0 && t + 1 <= T - 2)
+          mbar_arrive_expect_tx(bar_h + 8 * (t & 1), (uint32_t)NB * DH * 2);  // for h_{t+1}
+      }
+      const int s = t % NS;
+      if (!dead && !wait_phase<false>(bar_full + 8 * s, (t / NS) & 1, abort_flag, p.status, tlim))
+        dead = true;
+
+      if (!dead) {
+        // ---- Wx_t values of this thread's cells
+        float wx[G][NE];
+        const uint8_t* stage = smem + L.wx + s * stage_bytes;
+#pragma unroll
+        for (int us = 0; us < NSLOT; ++us)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int ei = (us * NT + nt) * 2 + e;
+              const int n = nt * 8 + 2 * (lane & 3) + e;
+              const int ul = ub + (lane >> 2) + 8 * us;
+#pragma unroll
+              for (int g = 0; g < G; ++g)
+                wx[g][ei] = bf16_to_f32(
+                    *reinterpret_cast<const uint16_t*>(stage + ((n * G + g) * U + ul) * 2));
+            }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+
+        // ---- acc = R^T h_{t-1}: two accumulator sets halve the k chain
+        float acc[MT][NT][4], acc2[MT][NT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[mt][nt][q] = acc2[mt][nt][q] = 0.f;
+        const uint32_t hb = s_h + (uint32_t)(t & 1) * NB * HPB + lm_off;
+#pragma unroll
+        for (int kp = 0; kp < KS / 2; ++kp) {
+          uint32_t bfr[NT][4];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) ldmatrix_x4(bfr[nt], hb + nt * 8 * HPB + kp * 64);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int ks = 2 * kp + hf;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              uint32_t a[4];
+              if (ks < KREG) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) a[q] = areg[mt][ks < KREG ? ks : 0][q];
+              } else {
+                lds128(a, rf_warp + (uint32_t)(mt * KSM + (ks - KREG)) * 512);
+              }
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                if (hf == 0) mma_bf16_16816(acc[mt][nt], a, bfr[nt][0], bfr[nt][1]);
+                else mma_bf16_16816(acc2[mt][nt], a, bfr[nt][2], bfr[nt][3]);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[mt][nt][q] += acc2[mt][nt][q];
+
+        // ---- gate math and state update, one (unit, batch) cell at a time
+        float hv[NE];
+#pragma unroll
+        for (int us = 0; us < NSLOT; ++us)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int ei = (us * NT + nt) * 2 + e;
+              float r[G];
+#pragma unroll
+              for (int g = 0; g < G; ++g)
+                r[g] = (UG == 16 ? acc[g][nt][us * 2 + e] : acc[g / 2][nt][(g % 2) * 2 + e]) +
+                       bias_v[g][us];
+              float h;
+              if (CELL == kLSTM) {
+                const float ig = sigmoid_fast(r[0] + wx[0][ei]);
+                const float fg = sigmoid_fast(r[1] + wx[1][ei]);
+                const float zg = tanh_fast(r[2] + wx[2][ei]);
+                const float og = sigmoid_fast(r[3] + wx[3][ei]);
+                const float c = fmaf(fg, st_c[ei], ig * zg);
+                st_c[ei] = c;
+                h = og * tanh_fast(c);
+                if (train) {
+                  const int n = nt * 8 + 2 * (lane & 3) + e;
+                  if (n < nvalid) {
+                    const int j = u0 + ub + (lane >> 2) + 8 * us;
+                    const size_t row = ((size_t)t * B + b0 + n) * NH + head;
+                    float* sg = p.stash_gates + row * GD + j;
+                    sg[0] = ig;
+                    sg[DH] = fg;
+                    sg[2 * DH] = zg;
+                    sg[3 * DH] = og;
+                    p.stash_c[row * DH + j] = c;
+                  }
+                }
+              } else if (CELL == kGRU) {
+                const float rg = sigmoid_fast(wx[0][ei] + r[0]);
+                const float zg = sigmoid_fast(wx[1][ei] + r[1]);
+                const float ng = tanh_fast(fmaf(rg, r[2], wx[2][ei]));
+                h = fmaf(zg, st_h[ei] - ng, ng);
+                st_h[ei] = h;
+              } else {
+                const float pi = r[0] + wx[0][ei], pf = r[1] + wx[1][ei];
+                const float pz = r[2] + wx[2][ei], po = r[3] + wx[3][ei];
+                const float mn = fmaxf(pf + st_m[ei], pi);
+                const float ig = __expf(pi - mn);
+                const float fg = __expf(pf + st_m[ei] - mn);
+                const float c = fmaf(fg, st_c[ei], ig * tanh_fast(pz));
+                const float nn = fmaf(fg, st_n[ei], ig);
+                st_c[ei] = c;
+                st_n[ei] = nn;
+                st_m[ei] = mn;
+                h = sigmoid_fast(po) * (c / nn);
+              }
+              hv[ei] = h;
+              st_h[ei] = h;
+            }
+
+        // ---- publish h_t: bf16 pairs (unit 2k, 2k+1) of one batch row
+        const bool ueven = ((lane >> 2) & 1) == 0;
+        const uint32_t nbuf = s_h + (uint32_t)((t + 1) & 1) * NB * HPB;
+        const bool send = t + 1 < T;
+#pragma unroll
+        for (int us = 0; us < NSLOT; ++us)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const int e0 = (us * NT + nt) * 2;
+            const float mine = ueven ? hv[e0 + 1] : hv[e0];
+            const float other = __shfl_xor_sync(0xffffffffu, mine, 4);
+            const uint32_t pk = ueven ? pack_bf16x2(hv[e0], other) : pack_bf16x2(other, hv[e0 + 1]);
+            const int n = nt * 8 + 2 * (lane & 3) + (ueven ? 0 : 1);
+            const int j = u0 + ub + (lane >> 2) + 8 * us - (ueven ? 0 : 1);
+            if (send) {
+              const uint32_t laddr = nbuf + (uint32_t)n * HPB + (uint32_t)j * 2;
+              if (CS == 1) {
+                asm volatile("st.shared.u32 [%0], %1;" ::"r"(laddr), "r"(pk) : "memory");
+              } else {
+                const uint32_t lbar = bar_h + 8 * ((t + 1) & 1);
+                for (int rk = 0; rk < CS; ++rk) st_async_b32(mapa(laddr, rk), pk, mapa(lbar, rk));
+              }
+            }
+            if (n < nvalid)
+              *reinterpret_cast<uint32_t*>(hseq + (((size_t)t * B + b0 + n) * NH + head) * DH + j) =
+                  pk;
+          }
+        if (t == T - 1) {
+#pragma unroll
+          for (int us = 0; us < NSLOT; ++us)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int ei = (us * NT + nt) * 2 + e;
+                const int n = nt * 8 + 2 * (lane & 3) + e;
+                if (n >= nvalid) continue;
+                const int j = u0 + ub + (lane >> 2) + 8 * us;
+                const size_t si = ((size_t)(b0 + n) * NH + head) * DH + j;
+                if (p.hT) p.hT[si] = hv[ei];
+                if (p.cT && CELL != kGRU) p.cT[si] = st_c[ei];
+                if (p.nT && CELL == kSLSTM) p.nT[si] = st_n[ei];
+                if (p.mT && CELL == kSLSTM) p.mT[si] = st_m[ei];
+              }
+        }
+      }
+      if (CS == 1) {
+        // h_t visible to every compute warp; a dead warp stops all of them together
+        if (bar_red_or(1, NW * 32, dead)) break;
+      } else if (dead) {
+        break;
+      }
+    }
+  }
+  // peers may still st.async into this CTA until they pass this point
+  if (CS > 1) cluster_sync();
+}
+
+template <int CELL, int DH, int UG, int NT, int KREG>
+int launch_fwd_bf16_t(const FwdParams& p_in, cudaStream_t stream, bool query_only,
+                      LaunchInfo* info) {
+  using C = FwdCfg<CELL, DH, UG, NT, KREG>;
+  FwdParams p = p_in;
+  auto kern = fwd_bf16_kernel<CELL, DH, UG, NT, KREG>;
+  const int NW = p.U / UG;
+  const int threads = (NW + 1) * 32;
+  if (p.U % UG != 0 || NW < 1 || threads > C::MAXT) return (int)cudaErrorInvalidConfiguration;
+  // Wx ring depth: as deep as shared memory allows, 2..12 stages
+  int dev = 0, max_smem = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  int ns = 12;
+  while (ns > 2 && fwd_smem_layout<C>(p.U, ns).total > (uint32_t)max_smem) --ns;
+  p.NS = ns;
+  const uint32_t smem = fwd_smem_layout<C>(p.U, ns).total;
+  if (smem > (uint32_t)max_smem) return (int)cudaErrorInvalidConfiguration;
+  const int grid = p.NH * p.nbslices * p.CS;
+  if (info) *info = LaunchInfo{grid, threads, p.CS, C::NB, (int)smem, CELL * 100 + DH / 32};
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return (int)e;
+  if (p.CS > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return (int)e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.CS > 1 ? 1 : 0;
+  if (p.CS > 1) {
+    int ncl = 0;
+    e = cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg);
+    if (e != cudaSuccess) return (int)e;
+    if (ncl < 1) return -1;  // cluster cannot be co-scheduled
+  }
+  if (query_only) return 0;
+  return (int)cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+}  // namespace srnn

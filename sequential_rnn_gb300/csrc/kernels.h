@@ -1,0 +1,87 @@
+// Internal interface between the C ABI (capi.cu) and the kernel translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace srnn {
+
+enum : int { kLSTM = 0, kGRU = 1, kSLSTM = 2 };
+enum : int { kStatusTimeout = 1 };  // bits of the device status word
+
+// Arguments of one forward launch.  Grid: one CTA per (head, batch slice,
+// cluster rank); blockIdx.x = ((head * nbslices) + bslice) * CS + rank.
+struct FwdParams {
+  const void* Wx;
+  const void* R;
+  const float* bias;
+  const float* h0;
+  const float* c0;
+  const float* n0;
+  const float* m0;
+  void* h_seq;
+  float* hT;
+  float* cT;
+  float* nT;
+  float* mT;
+  float* stash_gates;  // LSTM training stash: activations i,f,z,o  [T,B,NH,4Dh]
+  float* stash_c;      // and c_t                                    [T,B,NH,Dh]
+  int* status;
+  int T, B, NH;
+  int CS;        // CTAs per (head, batch slice): thread-block cluster size
+  int U;         // hidden units owned by one CTA (Dh / CS)
+  int NS;        // stages of the Wx ring
+  int nbslices;  // batch slices per head
+  int flags;
+  unsigned long long timeout_ns;
+};
+
+struct LaunchInfo {
+  int grid, threads, cluster, nb, smem, kernel_id;
+};
+
+// Each returns a cudaError_t value (cast to int); `info` is filled when non-null.
+// With `query_only` nothing is launched.
+int launch_fwd_f32(const FwdParams& p, int cell, int Dh, cudaStream_t s, bool query_only,
+                   LaunchInfo* info);
+int launch_fwd_bf16_lstm(const FwdParams& p, int Dh, int NT, cudaStream_t s, bool query_only,
+                         LaunchInfo* info);
+int launch_fwd_bf16_gru(const FwdParams& p, int Dh, int NT, cudaStream_t s, bool query_only,
+                        LaunchInfo* info);
+int launch_fwd_bf16_slstm(const FwdParams& p, int Dh, int NT, cudaStream_t s, bool query_only,
+                          LaunchInfo* info);
+// Units handled by one warp in the bf16 kernels (gate rows of one warp = UG * G).
+inline int bf16_unit_group(int cell) { return cell == kGRU ? 16 : 8; }
+
+// Empty-step kernel with the launch shape of a bf16/fp32 forward.
+int launch_sync_floor(const LaunchInfo& li, int T, int* status, cudaStream_t s);
+
+// Backward (LSTM, bf16).
+struct BwdParams {
+  const void* R;
+  const void* dh_seq;
+  const float* dhT;
+  const float* dcT;
+  const float* stash_gates;
+  const float* stash_c;
+  const float* c0;  // unused (c_{-1} comes from the stash or zero)
+  void* dWx;
+  float* dh0;
+  float* dc0;
+  float* db_part;  // [nbslices, NH, 4Dh] per-slice bias-gradient partials (workspace)
+  int* status;
+  int T, B, NH;
+  int CS, U, nbslices, flags;
+  unsigned long long timeout_ns;
+  const float* c_init;  // c0 fp32 [B,NH,Dh] (NULL = zeros), c_{-1} for the first step
+};
+int launch_bwd_lstm_bf16(const BwdParams& p, int Dh, cudaStream_t s, bool query_only,
+                         LaunchInfo* info);
+
+// dR = sum_t h_{t-1}^T dWx_t (bf16 operands, fp32 result) and db from partials.
+int launch_grad_weights(const void* h_seq, const void* h0_bf16, const void* dWx, float* dR,
+                        int T, int B, int NH, int Dh, int G, cudaStream_t s);
+int launch_h0_to_bf16(const float* h0, void* out, int n, cudaStream_t s);
+int launch_db_reduce(const float* part, float* db, int nslices, int n, cudaStream_t s);
+
+}  // namespace srnn

@@ -1,0 +1,97 @@
+"""C ABI host-side checks that need no GPU.
+
+The library loads, exports every entry point include/rnn.h declares, and its
+argument checks reject bad calls before touching CUDA (fake, never
+dereferenced pointer values are fine here because validation fails first).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sequential_rnn_gb300 import build, _lib
+    build.build()
+    return _lib.load()
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "rnn.h")).read()
+    return sorted(set(re.findall(r"\b(rnn_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    from sequential_rnn_gb300 import _lib
+    declared = _declared_symbols()
+    assert set(declared) == set(_lib.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def _desc(**kw):
+    from sequential_rnn_gb300._lib import rnn_desc_t
+    d = dict(cell=0, dtype=1, T=8, B=4, NH=2, Dh=64, flags=0, cluster=0)
+    d.update(kw)
+    return rnn_desc_t(**d)
+
+
+def _fwd(lib, desc, ws=0x1000, ws_bytes=256, wx=0x2000, r=0x3000, hseq=0x4000, stash=None):
+    P = ctypes.c_void_p
+    return lib.rnn_fwd(ctypes.byref(desc), P(wx), P(r), None, None, None, None, None, P(hseq),
+                       None, None, None, None, P(stash) if stash else None, P(ws), ws_bytes, None)
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert lib.rnn_status_str(s)
+    assert lib.rnn_status_str(99) == b"unknown status"
+
+
+def test_sizes(lib):
+    d = _desc(T=10, B=3, NH=2, Dh=64)
+    assert lib.rnn_workspace_size(ctypes.byref(d), 0) >= 256
+    assert lib.rnn_workspace_size(ctypes.byref(d), 1) >= 256 + 3 * 2 * 64 * 2
+    assert lib.rnn_stash_size(ctypes.byref(d)) == 10 * 3 * 2 * 64 * 5 * 4
+    assert lib.rnn_stash_size(ctypes.byref(_desc(cell=1))) == 0
+    assert lib.rnn_workspace_size(ctypes.byref(_desc(T=-1)), 0) == 0
+    assert lib.rnn_workspace_size(None, 0) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(cell=7), 1), (dict(dtype=5), 1), (dict(T=-1), 1), (dict(B=-2), 1), (dict(Dh=0), 1),
+    (dict(cluster=-1), 1),
+    (dict(Dh=48), 2), (dict(dtype=0, Dh=128), 2), (dict(Dh=512), 2), (dict(cluster=3), 2),
+    (dict(Dh=64, cluster=16), 2), (dict(cell=1, Dh=64, cluster=8), 2), (dict(dtype=0, cluster=2), 2),
+])
+def test_invalid_descriptors(lib, kw, status):
+    assert _fwd(lib, _desc(**kw)) == status
+
+
+def test_null_and_small_workspace(lib):
+    assert lib.rnn_fwd(None, *([None] * 14), 0, None) == 1
+    assert _fwd(lib, _desc(), ws=0) == 1
+    assert _fwd(lib, _desc(), ws_bytes=8) == 1
+    assert _fwd(lib, _desc(), wx=0) == 1
+    assert _fwd(lib, _desc(), hseq=0) == 1
+
+
+def test_misaligned_pointers(lib):
+    assert _fwd(lib, _desc(), wx=0x2008) == 3
+    assert _fwd(lib, _desc(), r=0x3002) == 3
+    assert _fwd(lib, _desc(), ws=0x1004) == 3
+
+
+def test_train_flag_rules(lib):
+    assert _fwd(lib, _desc(flags=1)) == 1                      # no stash
+    assert _fwd(lib, _desc(cell=1, flags=1), stash=0x5000) == 2  # no GRU backward
+    assert _fwd(lib, _desc(dtype=0, flags=1), stash=0x5000) == 2
+
+
+def test_empty_batch_is_noop(lib):
+    assert _fwd(lib, _desc(B=0)) == 0
+    assert _fwd(lib, _desc(NH=0)) == 0

@@ -1,0 +1,147 @@
+"""GPU parity of the forward recurrence against the fp64 oracle (needs a GB300).
+
+Every case calls the CUDA path through the C ABI (ctypes binding) on seeded
+inputs from ``synth`` and compares element by element with the oracle:
+max |dh| <= 1e-4 for fp32, <= 2e-2 for bf16 inputs (fp32 state), over h_seq
+and the final states.  Full-size workloads are compared over every output.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import rnn_oracle as O
+from synth import WORKLOADS, make_inputs, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+@pytest.fixture(scope="module")
+def S():
+    from sequential_rnn_gb300 import build
+    build.build()
+    import sequential_rnn_gb300 as S
+    return S
+
+
+def dev(d):
+    dt = torch.bfloat16 if d["dtype"] == "bf16" else torch.float32
+    g = {k: torch.from_numpy(np.ascontiguousarray(d[k])).to("cuda", dt) for k in ("Wx", "R")}
+    for k in ("b", "h0", "c0", "n0", "m0"):
+        g[k] = torch.from_numpy(np.ascontiguousarray(d[k])).to("cuda", torch.float32)
+    return g
+
+
+def run(S, d, cluster=0, train=False, g=None):
+    g = g or dev(d)
+    cell = d["cell"]
+    out = S.forward(cell, g["Wx"], g["R"], g["b"], g["h0"], g["c0"],
+                    g["n0"] if cell == "slstm" else None, g["m0"] if cell == "slstm" else None,
+                    cluster=cluster, train=train)
+    torch.cuda.synchronize()
+    return out
+
+
+def oracle(d):
+    return O.forward(d["cell"], d["Wx"], d["R"], d["b"], d["h0"], d["c0"], d["n0"], d["m0"])
+
+
+def compare(out, ref, dtype, label=""):
+    tol = TOL[dtype]
+    keys = ["h_seq", "hT"] + [k for k in ("cT", "nT") if k in out]
+    worst = {}
+    for k in keys:
+        got = out[k].float().cpu().numpy().astype(np.float64)
+        assert np.isfinite(got).all(), (label, k)
+        err = np.abs(got - ref[k]).max() if got.size else 0.0
+        worst[k] = err
+        assert err <= tol, f"{label} {k}: max|d|={err:.3g} > {tol}"
+    return worst
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_workload_forward_full(S, name):
+    d = workload_inputs(name)
+    out = run(S, d, train=WORKLOADS[name]["backward"])
+    compare(out, oracle(d), d["dtype"], name)
+
+
+SWEEP = [
+    # cell, dtype, Dh, B, NH, T
+    ("lstm", "f32", 16, 3, 2, 17), ("gru", "f32", 32, 13, 1, 9), ("slstm", "f32", 64, 5, 3, 12),
+    ("lstm", "f32", 64, 1, 1, 1), ("gru", "f32", 64, 9, 2, 2),
+    ("lstm", "bf16", 32, 3, 3, 17), ("lstm", "bf16", 64, 13, 2, 33), ("lstm", "bf16", 128, 9, 1, 20),
+    ("lstm", "bf16", 256, 4, 2, 25), ("lstm", "bf16", 768, 11, 1, 12), ("lstm", "bf16", 64, 1, 1, 1),
+    ("gru", "bf16", 32, 2, 2, 17), ("gru", "bf16", 64, 8, 3, 10), ("gru", "bf16", 128, 17, 1, 19),
+    ("gru", "bf16", 256, 3, 1, 21), ("gru", "bf16", 768, 5, 1, 7), ("gru", "bf16", 128, 1, 2, 2),
+    ("slstm", "bf16", 32, 7, 2, 15), ("slstm", "bf16", 64, 16, 1, 31), ("slstm", "bf16", 128, 3, 2, 9),
+    ("slstm", "bf16", 256, 9, 1, 40), ("slstm", "bf16", 768, 2, 1, 6), ("slstm", "bf16", 256, 1, 1, 1),
+]
+
+
+@pytest.mark.parametrize("cell,dtype,Dh,B,NH,T", SWEEP)
+def test_forward_small_sweep(S, cell, dtype, Dh, B, NH, T):
+    d = make_inputs(cell, dtype, T, B, NH, Dh, seed=Dh + B + T, bias="normal0.1", states="random")
+    compare(run(S, d), oracle(d), dtype, f"{cell}/{dtype}/Dh{Dh}/B{B}/NH{NH}/T{T}")
+
+
+@pytest.mark.parametrize("cell,Dh,clusters", [
+    ("lstm", 64, (1, 2, 4, 8)), ("gru", 128, (1, 2, 4, 8)), ("slstm", 256, (2, 4, 8, 16)),
+    ("lstm", 256, (4, 8, 16)),
+])
+def test_cluster_split_is_bitwise_identical(S, cell, Dh, clusters):
+    """Splitting a head over CTAs changes who computes, not the arithmetic."""
+    d = make_inputs(cell, "bf16", 14, 10, 2, Dh, seed=5, bias="normal0.1", states="random")
+    g = dev(d)
+    outs = [run(S, d, cluster=c, g=g) for c in clusters]
+    for c, o in zip(clusters[1:], outs[1:]):
+        assert torch.equal(o["h_seq"], outs[0]["h_seq"]), f"cluster {c}"
+        assert torch.equal(o["hT"], outs[0]["hT"]), f"cluster {c}"
+    compare(outs[0], oracle(d), "bf16")
+
+
+@pytest.mark.parametrize("cell,dtype,Dh", [("lstm", "bf16", 64), ("gru", "bf16", 128),
+                                           ("slstm", "bf16", 256), ("lstm", "f32", 64)])
+def test_chunking_through_final_state_is_bitwise(S, cell, dtype, Dh):
+    d = make_inputs(cell, dtype, 20, 9, 2, Dh, seed=7, bias="normal0.1", states="random")
+    g = dev(d)
+    full = run(S, d, g=g)
+    a = S.forward(cell, g["Wx"][:8].contiguous(), g["R"], g["b"], g["h0"], g["c0"],
+                  g["n0"] if cell == "slstm" else None, g["m0"] if cell == "slstm" else None)
+    b = S.forward(cell, g["Wx"][8:].contiguous(), g["R"], g["b"], a["hT"], a.get("cT"),
+                  a.get("nT"), a.get("mT"))
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([a["h_seq"], b["h_seq"]]), full["h_seq"])
+    assert torch.equal(b["hT"], full["hT"])
+
+
+def test_head_and_batch_permutation_is_bitwise(S):
+    d = make_inputs("lstm", "bf16", 12, 11, 4, 64, seed=9, bias="normal0.1", states="random")
+    g = dev(d)
+    base = run(S, d, g=g)
+    ph = torch.tensor([2, 0, 3, 1], device="cuda")
+    gp = {"Wx": g["Wx"][:, :, ph].contiguous(), "R": g["R"][ph].contiguous(),
+          "b": g["b"][ph].contiguous()}
+    for k in ("h0", "c0", "n0", "m0"):
+        gp[k] = g[k][:, ph].contiguous()
+    perm = run(S, d, g=gp)
+    assert torch.equal(perm["h_seq"], base["h_seq"][:, :, ph])
+
+
+def test_zero_length_sequence_copies_state(S):
+    d = make_inputs("slstm", "bf16", 0, 3, 2, 64, seed=1, states="random")
+    g = dev(d)
+    out = run(S, d, g=g)
+    for k, s in (("hT", "h0"), ("cT", "c0"), ("nT", "n0"), ("mT", "m0")):
+        assert torch.equal(out[k], g[s])
+
+
+@pytest.mark.parametrize("cell,Dh,cluster", [("lstm", 64, 0), ("slstm", 256, 4)])
+def test_bounded_wait_reports_timeout_and_context_survives(S, cell, Dh, cluster):
+    d = make_inputs(cell, "bf16", 6, 4, 1, Dh, seed=2)
+    g = dev(d)
+    out = S.forward(cell, g["Wx"], g["R"], g["b"], cluster=cluster, test_timeout=True, check=False)
+    assert S.rnn_read_status(out["workspace"]) == 5  # RNN_ERR_TIMEOUT
+    good = run(S, d, cluster=cluster, g=g)
+    compare(good, oracle(d), "bf16")
