@@ -29,7 +29,12 @@
  *
  * Numerics: RNN_F32 computes in fp32 throughout (fp32 FMA contraction,
  * accurate exp/tanh).  RNN_BF16 feeds bf16(h_{t-1}) and bf16 R to the tensor
- * cores with fp32 accumulation; gate math and all states are fp32.
+ * cores with fp32 accumulation; gate math and all states are fp32 (LSTM/GRU
+ * gates on the hardware tanh).  For the sLSTM, whose exponential gating
+ * amplifies per-step rounding of h by ~10^3 over 4096 steps, h_{t-1} enters
+ * the tensor cores as a bf16 pair hi + lo (hi = bf16(h), lo = bf16(h - hi),
+ * two MMAs into fp32) and exp/tanh are the accurate library functions;
+ * RNN_FLAG_H_BF16 turns this off.
  *
  * Ownership: the caller allocates and owns every buffer (device memory),
  * including the workspace and the training stash.  Nothing is allocated by
@@ -55,6 +60,8 @@ typedef enum { RNN_F32 = 0, RNN_BF16 = 1 } rnn_dtype_t;
 /* desc.flags */
 enum {
   RNN_FLAG_TRAIN = 1,              /* forward also writes the stash rnn_bwd needs */
+  RNN_FLAG_H_BF16 = 2,             /* sLSTM: plain bf16 h operand and fast gate math
+                                      (default for sLSTM is the hi+lo split, see Numerics) */
   RNN_FLAG_TEST_TIMEOUT = 1 << 30  /* test only: the kernel waits on a barrier that nothing
                                       completes, gives up after ~50 ms and reports
                                       RNN_ERR_TIMEOUT in the status word */

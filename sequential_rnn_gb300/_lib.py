@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(_PKG, "libsrnn.so")
 RNN_LSTM, RNN_GRU, RNN_SLSTM = 0, 1, 2
 RNN_F32, RNN_BF16 = 0, 1
 RNN_FLAG_TRAIN = 1
+RNN_FLAG_H_BF16 = 2
 RNN_FLAG_TEST_TIMEOUT = 1 << 30
 STATUS = {0: "RNN_OK", 1: "RNN_ERR_INVALID_ARG", 2: "RNN_ERR_UNSUPPORTED",
           3: "RNN_ERR_MISALIGNED", 4: "RNN_ERR_LAUNCH", 5: "RNN_ERR_TIMEOUT",

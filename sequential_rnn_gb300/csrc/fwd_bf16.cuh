@@ -37,7 +37,7 @@
 
 namespace srnn {
 
-template <int CELL, int DH, int UG, int NT, int KREG>
+template <int CELL, int DH, int UG, int NT, int KREG, int HS>
 struct FwdCfg {
   static constexpr int G = CELL == kGRU ? 3 : 4;
   static constexpr int GD = G * DH;
@@ -49,8 +49,10 @@ struct FwdCfg {
   static constexpr int HPB = ((DH * 2 / 16) % 2 == 0) ? DH * 2 + 16 : DH * 2;
   static constexpr int NSLOT = UG == 16 ? 2 : 1;  // units per thread
   static constexpr int NE = NSLOT * NT * 2;       // (unit, batch) cells per thread
+  // HS: h_{t-1} enters the MMA as a bf16 pair hi + lo (hi = bf16(h), lo = bf16(h - hi))
+  static constexpr int HPARTS = HS ? 2 : 1;
   // register estimate per compute thread -> largest CTA the register file holds
-  static constexpr int REG_EST = MT * KREG * 4 + MT * NT * 8 + 88;
+  static constexpr int REG_EST = MT * KREG * 4 + MT * NT * 8 + 88 + HS * NT * 8;
   static constexpr int MAXT_R = (65536 / REG_EST) / 32 * 32;
   static constexpr int MAXT = MAXT_R < 17 * 32 ? MAXT_R : 17 * 32;
   static_assert(UG == 8 || UG == 16, "unit group");
@@ -68,7 +70,7 @@ __host__ __device__ inline FwdSmem fwd_smem_layout(int U, int NS) {
   FwdSmem L;
   const int NW = U / (C::MT * 16 / C::G);
   L.h = 0;
-  uint32_t o = 2u * C::NB * C::HPB;
+  uint32_t o = 2u * C::HPARTS * C::NB * C::HPB;
   o = (o + 127) & ~127u;
   L.wx = o;
   o += (uint32_t)NS * C::NB * C::G * U * 2;
@@ -101,9 +103,10 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   }
 }
 
-template <int CELL, int DH, int UG, int NT, int KREG>
-__global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG>::MAXT, 1) fwd_bf16_kernel(const FwdParams p) {
-  using C = FwdCfg<CELL, DH, UG, NT, KREG>;
+template <int CELL, int DH, int UG, int NT, int KREG, int HS>
+__global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
+    fwd_bf16_kernel(const FwdParams p) {
+  using C = FwdCfg<CELL, DH, UG, NT, KREG, HS>;
   constexpr int G = C::G, GD = C::GD, MT = C::MT, KS = C::KS, KSM = C::KSM, NB = C::NB;
   constexpr int HPB = C::HPB, NE = C::NE, NSLOT = C::NSLOT;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -125,6 +128,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG>::MAXT, 1) fwd_b
   const uint32_t bar_dummy = bar_h + 16;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flag);
   const uint32_t stage_bytes = (uint32_t)NB * G * U * 2;
+  const uint32_t hpart = 2u * NB * HPB;  // byte offset of the lo part of h
+  const uint32_t htx = (uint32_t)C::HPARTS * NB * DH * 2;  // h bytes landing per step
 
   // ------------------------------------------------------------- set-up --
   if (tid == 0) {
@@ -157,13 +162,16 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG>::MAXT, 1) fwd_b
       v1 = src[1];
     }
     *reinterpret_cast<uint32_t*>(smem + L.h + n * HPB + j * 2) = pack_bf16x2(v0, v1);
+    if (HS)
+      *reinterpret_cast<uint32_t*>(smem + L.h + hpart + n * HPB + j * 2) =
+          pack_bf16x2(v0 - bf16_round(v0), v1 - bf16_round(v1));
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
   if (tid == 0 && CS > 1) {
     // h_0 lands in buffer 1, h_1 in buffer 0 (first phase of each)
-    if (T >= 2) mbar_arrive_expect_tx(bar_h + 8, (uint32_t)NB * DH * 2);
-    if (T >= 3) mbar_arrive_expect_tx(bar_h, (uint32_t)NB * DH * 2);
+    if (T >= 2) mbar_arrive_expect_tx(bar_h + 8, htx);
+    if (T >= 3) mbar_arrive_expect_tx(bar_h, htx);
   }
   if (CS > 1) cluster_sync();
   else __syncthreads();
@@ -281,7 +289,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG>::MAXT, 1) fwd_b
         if (!wait_phase<true>(bar_h + 8 * (t & 1), ((t - 1) >> 1) & 1, abort_flag, p.status, tlim))
           dead = true;
         else if (tid == 0 && t + 1 <= T - 2)
-          mbar_arrive_expect_tx(bar_h + 8 * (t & 1), (uint32_t)NB * DH * 2);  // for h_{t+1}
+          mbar_arrive_expect_tx(bar_h + 8 * (t & 1), htx);  // for h_{t+1}
       }
       const int s = t % NS;
       if (!dead && !wait_phase<false>(bar_full + 8 * s, (t / NS) & 1, abort_flag, p.status, tlim))
@@ -319,9 +327,14 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG>::MAXT, 1) fwd_b
         const uint32_t hb = s_h + (uint32_t)(t & 1) * NB * HPB + lm_off;
 #pragma unroll
         for (int kp = 0; kp < KS / 2; ++kp) {
-          uint32_t bfr[NT][4];
+          uint32_t bfr[NT][4], bfl[HS ? NT : 1][4];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) ldmatrix_x4(bfr[nt], hb + nt * 8 * HPB + kp * 64);
+          if (HS) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              ldmatrix_x4(bfl[HS ? nt : 0], hb + hpart + nt * 8 * HPB + kp * 64);
+          }
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             const int ks = 2 * kp + hf;
@@ -336,8 +349,15 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG>::MAXT, 1) fwd_b
               }
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
-                if (hf == 0) mma_bf16_16816(acc[mt][nt], a, bfr[nt][0], bfr[nt][1]);
-                else mma_bf16_16816(acc2[mt][nt], a, bfr[nt][2], bfr[nt][3]);
+                if (HS) {  // hi and lo parts on two independent accumulator chains
+                  mma_bf16_16816(acc[mt][nt], a, bfr[nt][2 * hf], bfr[nt][2 * hf + 1]);
+                  mma_bf16_16816(acc2[mt][nt], a, bfl[HS ? nt : 0][2 * hf],
+                                 bfl[HS ? nt : 0][2 * hf + 1]);
+                } else if (hf == 0) {
+                  mma_bf16_16816(acc[mt][nt], a, bfr[nt][0], bfr[nt][1]);
+                } else {
+                  mma_bf16_16816(acc2[mt][nt], a, bfr[nt][2], bfr[nt][3]);
+                }
               }
             }
           }
@@ -395,14 +415,16 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG>::MAXT, 1) fwd_b
                 const float pi = r[0] + wx[0][ei], pf = r[1] + wx[1][ei];
                 const float pz = r[2] + wx[2][ei], po = r[3] + wx[3][ei];
                 const float mn = fmaxf(pf + st_m[ei], pi);
-                const float ig = __expf(pi - mn);
-                const float fg = __expf(pf + st_m[ei] - mn);
-                const float c = fmaf(fg, st_c[ei], ig * tanh_fast(pz));
+                // HS: accurate exp/tanh (the exponential gating amplifies rounding)
+                const float ig = HS ? expf(pi - mn) : __expf(pi - mn);
+                const float fg = HS ? expf(pf + st_m[ei] - mn) : __expf(pf + st_m[ei] - mn);
+                const float c = fmaf(fg, st_c[ei], ig * (HS ? tanhf(pz) : tanh_fast(pz)));
                 const float nn = fmaf(fg, st_n[ei], ig);
                 st_c[ei] = c;
                 st_n[ei] = nn;
                 st_m[ei] = mn;
-                h = sigmoid_fast(po) * (c / nn);
+                const float og = HS ? 1.f / (1.f + expf(-po)) : sigmoid_fast(po);
+                h = og * (c / nn);
               }
               hv[ei] = h;
               st_h[ei] = h;
@@ -419,16 +441,26 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG>::MAXT, 1) fwd_b
             const int e0 = (us * NT + nt) * 2;
             const float mine = ueven ? hv[e0 + 1] : hv[e0];
             const float other = __shfl_xor_sync(0xffffffffu, mine, 4);
-            const uint32_t pk = ueven ? pack_bf16x2(hv[e0], other) : pack_bf16x2(other, hv[e0 + 1]);
+            // h of units (2k, 2k+1) for one batch row: rounded pair, and its residual pair
+            const float v_ev = ueven ? hv[e0] : other, v_od = ueven ? other : hv[e0 + 1];
+            const uint32_t pk = pack_bf16x2(v_ev, v_od);
+            const uint32_t pkl =
+                HS ? pack_bf16x2(v_ev - bf16_round(v_ev), v_od - bf16_round(v_od)) : 0u;
             const int n = nt * 8 + 2 * (lane & 3) + (ueven ? 0 : 1);
             const int j = u0 + ub + (lane >> 2) + 8 * us - (ueven ? 0 : 1);
             if (send) {
               const uint32_t laddr = nbuf + (uint32_t)n * HPB + (uint32_t)j * 2;
               if (CS == 1) {
                 asm volatile("st.shared.u32 [%0], %1;" ::"r"(laddr), "r"(pk) : "memory");
+                if (HS)
+                  asm volatile("st.shared.u32 [%0], %1;" ::"r"(laddr + hpart), "r"(pkl) : "memory");
               } else {
                 const uint32_t lbar = bar_h + 8 * ((t + 1) & 1);
-                for (int rk = 0; rk < CS; ++rk) st_async_b32(mapa(laddr, rk), pk, mapa(lbar, rk));
+                for (int rk = 0; rk < CS; ++rk) {
+                  const uint32_t rbar = mapa(lbar, rk);
+                  st_async_b32(mapa(laddr, rk), pk, rbar);
+                  if (HS) st_async_b32(mapa(laddr + hpart, rk), pkl, rbar);
+                }
               }
             }
             if (n < nvalid)
@@ -466,12 +498,12 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG>::MAXT, 1) fwd_b
   if (CS > 1) cluster_sync();
 }
 
-template <int CELL, int DH, int UG, int NT, int KREG>
+template <int CELL, int DH, int UG, int NT, int KREG, int HS = 0>
 int launch_fwd_bf16_t(const FwdParams& p_in, cudaStream_t stream, bool query_only,
                       LaunchInfo* info) {
-  using C = FwdCfg<CELL, DH, UG, NT, KREG>;
+  using C = FwdCfg<CELL, DH, UG, NT, KREG, HS>;
   FwdParams p = p_in;
-  auto kern = fwd_bf16_kernel<CELL, DH, UG, NT, KREG>;
+  auto kern = fwd_bf16_kernel<CELL, DH, UG, NT, KREG, HS>;
   const int NW = p.U / UG;
   const int threads = (NW + 1) * 32;
   if (p.U % UG != 0 || NW < 1 || threads > C::MAXT) return (int)cudaErrorInvalidConfiguration;
@@ -485,7 +517,7 @@ int launch_fwd_bf16_t(const FwdParams& p_in, cudaStream_t stream, bool query_onl
   const uint32_t smem = fwd_smem_layout<C>(p.U, ns).total;
   if (smem > (uint32_t)max_smem) return (int)cudaErrorInvalidConfiguration;
   const int grid = p.NH * p.nbslices * p.CS;
-  if (info) *info = LaunchInfo{grid, threads, p.CS, C::NB, (int)smem, CELL * 100 + DH / 32};
+  if (info) *info = LaunchInfo{grid, threads, p.CS, C::NB, (int)smem, CELL * 100 + DH / 32 + 50 * HS};
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return (int)e;
   if (p.CS > 8) {

@@ -3,8 +3,21 @@
 
 namespace srnn {
 
-int launch_fwd_bf16_slstm(const FwdParams& p, int Dh, int NT, cudaStream_t s, bool query_only,
-                          LaunchInfo* info) {
+int launch_fwd_bf16_slstm(const FwdParams& p, int Dh, int NT, int hsplit, cudaStream_t s,
+                          bool query_only, LaunchInfo* info) {
+  if (hsplit) {
+    // h_{t-1} as a bf16 hi + lo pair: the exponentially gated recurrence amplifies
+    // per-step rounding of h by orders of magnitude over thousands of steps.
+    if (NT != 1) return (int)cudaErrorInvalidValue;
+    switch (Dh) {
+      case 32: return launch_fwd_bf16_t<kSLSTM, 32, 8, 1, 2, 1>(p, s, query_only, info);
+      case 64: return launch_fwd_bf16_t<kSLSTM, 64, 8, 1, 4, 1>(p, s, query_only, info);
+      case 128: return launch_fwd_bf16_t<kSLSTM, 128, 8, 1, 8, 1>(p, s, query_only, info);
+      case 256: return launch_fwd_bf16_t<kSLSTM, 256, 8, 1, 12, 1>(p, s, query_only, info);
+      case 768: return launch_fwd_bf16_t<kSLSTM, 768, 8, 1, 14, 1>(p, s, query_only, info);
+      default: return (int)cudaErrorInvalidValue;
+    }
+  }
   // KREG: k16 steps of R^T held in registers per warp; the rest sit in shared memory.
   constexpr int UG = 8;
   if (NT == 2) {
