@@ -2,8 +2,11 @@
 
 Every case calls the CUDA path through the C ABI (ctypes binding) on seeded
 inputs from ``synth`` and compares element by element with the oracle:
-max |dh| <= 1e-4 for fp32, <= 2e-2 for bf16 inputs (fp32 state), over h_seq
-and the final states.  Full-size workloads are compared over every output.
+max |dh| <= 1e-4 for fp32, <= 2e-2 for bf16 inputs (fp32 state), over h_seq,
+hT and the LSTM cell state cT.  The sLSTM accumulators cT and nT carry the
+scale exp(-m) of the stabiliser (|n| reaches ~10 here), so they are compared
+normwise: max |d| / max |ref| within the same bound.  Full-size workloads are
+compared over every output.
 """
 import numpy as np
 import pytest
@@ -50,11 +53,14 @@ def oracle(d):
 def compare(out, ref, dtype, label=""):
     tol = TOL[dtype]
     keys = ["h_seq", "hT"] + [k for k in ("cT", "nT") if k in out]
+    slstm = "nT" in out
     worst = {}
     for k in keys:
         got = out[k].float().cpu().numpy().astype(np.float64)
         assert np.isfinite(got).all(), (label, k)
         err = np.abs(got - ref[k]).max() if got.size else 0.0
+        if slstm and k in ("cT", "nT") and got.size:
+            err /= max(np.abs(ref[k]).max(), 1.0)
         worst[k] = err
         assert err <= tol, f"{label} {k}: max|d|={err:.3g} > {tol}"
     return worst
