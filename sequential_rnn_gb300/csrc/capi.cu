@@ -88,7 +88,9 @@ int launch_forward(const rnn_desc_t* d, const Plan& pl, const FwdParams& p, cuda
     case RNN_LSTM: return launch_fwd_bf16_lstm(p, d->Dh, pl.NT, s, query_only, info);
     case RNN_GRU: return launch_fwd_bf16_gru(p, d->Dh, pl.NT, s, query_only, info);
     default:
-      return launch_fwd_bf16_slstm(p, d->Dh, pl.NT, (d->flags & RNN_FLAG_H_BF16) ? 0 : 1, s,
+      // hi+lo split of h for the sLSTM while it fits on chip (Dh <= 256)
+      return launch_fwd_bf16_slstm(p, d->Dh, pl.NT,
+                                   ((d->flags & RNN_FLAG_H_BF16) || d->Dh > 256) ? 0 : 1, s,
                                    query_only, info);
   }
 }

@@ -14,7 +14,6 @@ int launch_fwd_bf16_slstm(const FwdParams& p, int Dh, int NT, int hsplit, cudaSt
       case 64: return launch_fwd_bf16_t<kSLSTM, 64, 8, 1, 4, 1>(p, s, query_only, info);
       case 128: return launch_fwd_bf16_t<kSLSTM, 128, 8, 1, 8, 1>(p, s, query_only, info);
       case 256: return launch_fwd_bf16_t<kSLSTM, 256, 8, 1, 12, 1>(p, s, query_only, info);
-      case 768: return launch_fwd_bf16_t<kSLSTM, 768, 8, 1, 14, 1>(p, s, query_only, info);
       default: return (int)cudaErrorInvalidValue;
     }
   }
