@@ -93,8 +93,9 @@ def test_forward_small_sweep(S, cell, dtype, Dh, B, NH, T):
 
 
 @pytest.mark.parametrize("cell,Dh,clusters", [
-    ("lstm", 64, (1, 2, 4, 8)), ("gru", 128, (1, 2, 4, 8)), ("slstm", 256, (2, 4, 8, 16)),
-    ("lstm", 256, (4, 8, 16)),
+    # (a split too coarse for the register file is rejected with UNSUPPORTED)
+    ("lstm", 64, (1, 2, 4, 8)), ("gru", 128, (1, 2, 4, 8)), ("slstm", 256, (4, 8, 16)),
+    ("lstm", 256, (8, 16)), ("gru", 256, (4, 8, 16)),
 ])
 def test_cluster_split_is_bitwise_identical(S, cell, Dh, clusters):
     """Splitting a head over CTAs changes who computes, not the arithmetic."""
@@ -133,6 +134,14 @@ def test_head_and_batch_permutation_is_bitwise(S):
         gp[k] = g[k][:, ph].contiguous()
     perm = run(S, d, g=gp)
     assert torch.equal(perm["h_seq"], base["h_seq"][:, :, ph])
+
+
+def test_too_coarse_cluster_split_is_rejected(S):
+    d = make_inputs("lstm", "bf16", 4, 2, 1, 256, seed=1)
+    g = dev(d)
+    with pytest.raises(S.RnnError) as e:
+        run(S, d, cluster=2, g=g)
+    assert e.value.status == 2
 
 
 def test_zero_length_sequence_copies_state(S):
