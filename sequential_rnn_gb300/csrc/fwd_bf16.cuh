@@ -14,8 +14,12 @@
 // very large heads the k-steps >= KREG sit in shared memory in fragment order)
 // and h_{t-1} (bf16) as the B operand read by ldmatrix from a double buffer.
 // A producer warp streams Wx_t with bulk async copies into a ring of NS stages
-// (full/empty mbarriers).  Gate math runs on the accumulator registers; each
-// thread owns whole (unit, batch) cells, so no gate exchange is needed.
+// (full/empty mbarriers); each thread picks up its Wx values with one
+// transposing ldmatrix, which lands them exactly in accumulator layout, and
+// the accumulators start from Wx + bias.  Gate math runs on the accumulator
+// registers; each thread owns whole (unit, batch) cells, so no gate exchange
+// is needed.  Sigmoid gate rows of R, Wx and bias are pre-scaled by 1/2 so a
+// sigmoid is one hardware tanh and one FMA: sigmoid(x) = (1 + tanh(x/2)) / 2.
 //
 // Exchange of h_t: CS == 1 -> shared memory + one named barrier per step.
 // CS > 1 -> every thread st.async's its bf16 pair of h_t into every cluster
@@ -49,8 +53,12 @@ struct FwdCfg {
   static constexpr int HPB = ((DH * 2 / 16) % 2 == 0) ? DH * 2 + 16 : DH * 2;
   static constexpr int NSLOT = UG == 16 ? 2 : 1;  // units per thread
   static constexpr int NE = NSLOT * NT * 2;       // (unit, batch) cells per thread
+  static constexpr int NTILE = G * NSLOT;         // 8x8 Wx tiles per thread and n-tile
+  static constexpr int NQ = (NTILE + 3) / 4;      // ldmatrix instructions for them
   // HS: h_{t-1} enters the MMA as a bf16 pair hi + lo (hi = bf16(h), lo = bf16(h - hi))
   static constexpr int HPARTS = HS ? 2 : 1;
+  // long k chains run as two interleaved accumulator sets
+  static constexpr bool SPLITK = KS >= 8 || HS;
   // register estimate per compute thread -> largest CTA the register file holds
   static constexpr int REG_EST = MT * KREG * 4 + MT * NT * 8 + 88 + HS * NT * 8;
   static constexpr int MAXT_R = (65536 / REG_EST) / 32 * 32;
@@ -59,6 +67,17 @@ struct FwdCfg {
   static_assert(UG * G % 16 == 0, "gate rows per warp must fill m16 tiles");
   static_assert(DH % 32 == 0, "Dh multiple of 32");
   static_assert(KREG >= 0 && KREG <= KS, "KREG");
+  static_assert(NTILE % 2 == 0, "Wx tiles come in pairs");
+  // scale of gate g's preactivation: 1/2 for sigmoid gates on the fast path
+  __host__ __device__ static constexpr float gate_scale(int g) {
+    return HS ? 1.f
+              : (CELL == kLSTM ? (g == 2 ? 1.f : 0.5f)
+                               : (CELL == kGRU ? (g == 2 ? 1.f : 0.5f) : (g == 3 ? 0.5f : 1.f)));
+  }
+  // Wx row pitch in the ring (bytes): odd number of 16-byte chunks
+  __host__ __device__ static constexpr uint32_t wx_pitch(int U) {
+    return ((G * U * 2 / 16) % 2 == 0) ? G * U * 2 + 16 : G * U * 2;
+  }
 };
 
 struct FwdSmem {
@@ -73,7 +92,7 @@ __host__ __device__ inline FwdSmem fwd_smem_layout(int U, int NS) {
   uint32_t o = 2u * C::HPARTS * C::NB * C::HPB;
   o = (o + 127) & ~127u;
   L.wx = o;
-  o += (uint32_t)NS * C::NB * C::G * U * 2;
+  o += (uint32_t)NS * C::NB * C::wx_pitch(U);
   o = (o + 127) & ~127u;
   L.rf = o;
   o += (uint32_t)NW * C::MT * C::KSM * 512;
@@ -108,7 +127,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     fwd_bf16_kernel(const FwdParams p) {
   using C = FwdCfg<CELL, DH, UG, NT, KREG, HS>;
   constexpr int G = C::G, GD = C::GD, MT = C::MT, KS = C::KS, KSM = C::KSM, NB = C::NB;
-  constexpr int HPB = C::HPB, NE = C::NE, NSLOT = C::NSLOT;
+  constexpr int HPB = C::HPB, NE = C::NE, NSLOT = C::NSLOT, NTILE = C::NTILE, NQ = C::NQ;
   extern __shared__ __align__(128) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -127,7 +146,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   const uint32_t bar_h = bar_empty + 8 * NS;  // two: hfull[0], hfull[1]
   const uint32_t bar_dummy = bar_h + 16;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flag);
-  const uint32_t stage_bytes = (uint32_t)NB * G * U * 2;
+  const uint32_t WP = C::wx_pitch(U);
+  const uint32_t stage_bytes = (uint32_t)NB * WP;
   const uint32_t hpart = 2u * NB * HPB;  // byte offset of the lo part of h
   const uint32_t htx = (uint32_t)C::HPARTS * NB * DH * 2;  // h bytes landing per step
 
@@ -145,11 +165,10 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   }
   // batch rows past B: their ring rows stay zero forever (never copied into)
   if (nvalid < NB) {
-    const int row_bytes = G * U * 2;
-    for (int i = tid; i < NS * (NB - nvalid) * row_bytes / 4; i += blockDim.x) {
-      const int per = (NB - nvalid) * row_bytes / 4;
+    const int per = (NB - nvalid) * (int)WP / 4;
+    for (int i = tid; i < NS * per; i += blockDim.x) {
       const int s = i / per, r = i % per;
-      *reinterpret_cast<uint32_t*>(smem + L.wx + s * stage_bytes + nvalid * row_bytes + r * 4) = 0u;
+      *reinterpret_cast<uint32_t*>(smem + L.wx + s * stage_bytes + nvalid * WP + r * 4) = 0u;
     }
   }
   // h_{-1} = bf16(h0) for all Dh units of this batch slice into buffer 0
@@ -182,29 +201,35 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     // ------------------------------------------------ Wx producer warp --
     if (lane == 0) {
       const __nv_bfloat16* Wx = static_cast<const __nv_bfloat16*>(p.Wx);
-      int t = 0;
-      for (; t < T; ++t) {
-        const int s = t % NS, k = t / NS;
-        if (t >= NS && !wait_phase<false>(bar_empty + 8 * s, (k - 1) & 1, abort_flag, p.status, tlim))
+      const size_t tstride = (size_t)B * NH * GD;
+      const __nv_bfloat16* rowt = Wx + ((size_t)b0 * NH + head) * GD + u0;
+      int t = 0, s = 0;
+      uint32_t ph = 0;
+      for (; t < T; ++t, rowt += tstride) {
+        if (t >= NS && !wait_phase<false>(bar_empty + 8 * s, ph ^ 1u, abort_flag, p.status, tlim))
           break;
         if (*abort_flag) break;
         mbar_arrive_expect_tx(bar_full + 8 * s, (uint32_t)nvalid * G * U * 2);
         const uint32_t dst0 = s_wx + s * stage_bytes;
         for (int n = 0; n < nvalid; ++n) {
-          const __nv_bfloat16* row = Wx + (((size_t)t * B + b0 + n) * NH + head) * GD;
+          const __nv_bfloat16* row = rowt + (size_t)n * NH * GD;
           if (U == DH) {
-            bulk_g2s(dst0 + n * GD * 2, row, GD * 2, bar_full + 8 * s);
+            bulk_g2s(dst0 + n * WP, row, GD * 2, bar_full + 8 * s);
           } else {
             for (int g = 0; g < G; ++g)
-              bulk_g2s(dst0 + (n * G + g) * U * 2, row + g * DH + u0, U * 2, bar_full + 8 * s);
+              bulk_g2s(dst0 + n * WP + g * U * 2, row + g * DH, U * 2, bar_full + 8 * s);
           }
+        }
+        if (++s == NS) {
+          s = 0;
+          ph ^= 1u;
         }
       }
       // let every issued copy land before the CTA can exit
       for (int tt = max(0, t - NS); tt < t; ++tt) {
-        const int s = tt % NS;
+        const int ss = tt % NS;
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar_full + 8 * s, (tt / NS) & 1)) {
+        while (!mbar_try_wait(bar_full + 8 * ss, (tt / NS) & 1)) {
           if (globaltimer_ns() - t0 > tlim) break;
         }
       }
@@ -212,28 +237,34 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------- compute warps --
-    const __nv_bfloat16* Rh = static_cast<const __nv_bfloat16*>(p.R) + (size_t)head * DH * GD;
-    const uint16_t* Rb = reinterpret_cast<const uint16_t*>(Rh);
+    const uint16_t* Rb = static_cast<const uint16_t*>(p.R) + (size_t)head * DH * GD;
     const int ub = warp * UG;  // first CTA-local unit of this warp
 
-    // A fragments of R^T: rows = (gate g, unit u) with row = g*UG + u.
+    // A fragments of R^T: rows = (gate g, unit u) with row = g*UG + u; sigmoid
+    // gate rows pre-scaled by 1/2 (exact in bf16).
     uint32_t areg[MT][KREG > 0 ? KREG : 1][4];
     const uint32_t rf_warp = s_rf + (uint32_t)warp * MT * KSM * 512 + lane * 16;
+    auto rval = [&](int k, int col, float sc) -> uint32_t {
+      const uint16_t v = Rb[(size_t)k * GD + col];
+      if (sc == 1.f) return v;
+      const __nv_bfloat16 x = __float2bfloat16_rn(__uint_as_float((uint32_t)v << 16) * sc);
+      return (uint32_t)(*reinterpret_cast<const uint16_t*>(&x));
+    };
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       const int ra = mt * 16 + (lane >> 2), rb = ra + 8;
-      const int ca = (ra / UG) * DH + u0 + ub + (ra % UG);
-      const int cb = (rb / UG) * DH + u0 + ub + (rb % UG);
+      const int ga = ra / UG, gb = rb / UG;
+      const int ca = ga * DH + u0 + ub + (ra % UG);
+      const int cb = gb * DH + u0 + ub + (rb % UG);
+      const float sa = C::gate_scale(ga), sb = C::gate_scale(gb);
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const int k0 = ks * 16 + 2 * (lane & 3);
         uint32_t a[4];
-        a[0] = (uint32_t)Rb[(size_t)k0 * GD + ca] | ((uint32_t)Rb[(size_t)(k0 + 1) * GD + ca] << 16);
-        a[1] = (uint32_t)Rb[(size_t)k0 * GD + cb] | ((uint32_t)Rb[(size_t)(k0 + 1) * GD + cb] << 16);
-        a[2] = (uint32_t)Rb[(size_t)(k0 + 8) * GD + ca] |
-               ((uint32_t)Rb[(size_t)(k0 + 9) * GD + ca] << 16);
-        a[3] = (uint32_t)Rb[(size_t)(k0 + 8) * GD + cb] |
-               ((uint32_t)Rb[(size_t)(k0 + 9) * GD + cb] << 16);
+        a[0] = rval(k0, ca, sa) | (rval(k0 + 1, ca, sa) << 16);
+        a[1] = rval(k0, cb, sb) | (rval(k0 + 1, cb, sb) << 16);
+        a[2] = rval(k0 + 8, ca, sa) | (rval(k0 + 9, ca, sa) << 16);
+        a[3] = rval(k0 + 8, cb, sb) | (rval(k0 + 9, cb, sb) << 16);
         if (ks < KREG) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) areg[mt][ks < KREG ? ks : 0][q] = a[q];
@@ -246,14 +277,15 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
       }
     }
 
-    // per-thread cells: slot us (unit), n-tile nt, column e -> index (us*NT+nt)*2+e
-    float bias_v[G][NSLOT];
+    // per-thread cells: slot us (unit lane/4 + 8us), n-tile nt, column e
+    //   -> cell index (us*NT + nt)*2 + e, batch row nt*8 + 2*(lane&3) + e
+    float sbias[G][NSLOT];  // gate_scale(g) * bias
 #pragma unroll
     for (int us = 0; us < NSLOT; ++us) {
       const int j = u0 + ub + (lane >> 2) + 8 * us;
 #pragma unroll
       for (int g = 0; g < G; ++g)
-        bias_v[g][us] = p.bias ? p.bias[(size_t)head * GD + g * DH + j] : 0.f;
+        sbias[g][us] = C::gate_scale(g) * (p.bias ? p.bias[(size_t)head * GD + g * DH + j] : 0.f);
     }
     float st_c[NE], st_n[NE], st_m[NE], st_h[NE];
 #pragma unroll
@@ -273,9 +305,36 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
           st_h[ei] = (ok && p.h0) ? p.h0[si] : 0.f;
         }
 
-    // ldmatrix: lane supplies row (lane & 7) of 8x8 matrix (lane >> 3)
+    // ldmatrix (h, B operand): lane supplies row (lane & 7) of 8x8 matrix (lane >> 3)
     const uint32_t lm_off = (uint32_t)(lane & 7) * HPB + (uint32_t)(lane >> 3) * 16;
-    __nv_bfloat16* hseq = static_cast<__nv_bfloat16*>(p.h_seq);
+    // ldmatrix.trans (Wx): 8x8 tile k = us*G + g holds rows = batch, cols = the 8
+    // units of slot us for gate g; the transpose hands lane l exactly the pair
+    // (unit l/4, batch 2(l%4) and 2(l%4)+1) of its accumulator cells.
+    uint32_t wx_off[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      int k = 4 * q + (lane >> 3);
+      if (k >= NTILE) k -= 2;  // x2 form: lanes 16..31 supply ignored addresses
+      const int us = k / G, g = k % G;
+      wx_off[q] = (uint32_t)(lane & 7) * WP + (uint32_t)(g * U + ub + 8 * us) * 2;
+    }
+    // where this thread publishes its h pairs (per slot, n-tile)
+    const bool ueven = ((lane >> 2) & 1) == 0;
+    uint32_t h_off[NSLOT][NT];
+    __nv_bfloat16* hseq_p[NSLOT][NT];
+    bool h_ok[NSLOT][NT];
+#pragma unroll
+    for (int us = 0; us < NSLOT; ++us)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int n = nt * 8 + 2 * (lane & 3) + (ueven ? 0 : 1);
+        const int j = u0 + ub + (lane >> 2) + 8 * us - (ueven ? 0 : 1);
+        h_off[us][nt] = (uint32_t)n * HPB + (uint32_t)j * 2;
+        h_ok[us][nt] = n < nvalid;
+        hseq_p[us][nt] = static_cast<__nv_bfloat16*>(p.h_seq) +
+                         ((size_t)(h_ok[us][nt] ? b0 + n : b0) * NH + head) * DH + j;
+      }
+    const size_t hseq_tstride = (size_t)B * NH * DH;
     const bool train = (p.flags & 1) && CELL == kLSTM && p.stash_gates != nullptr;
 
     bool dead = false;
@@ -283,6 +342,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
       if (!wait_phase<false>(bar_dummy, 0, abort_flag, p.status, tlim)) dead = true;
     }
 
+    int s = 0;
+    uint32_t ph = 0;
     for (int t = 0; t < T; ++t) {
       // ---- wait for h_{t-1} (cluster) and Wx_t
       if (!dead && CS > 1 && t > 0) {
@@ -291,39 +352,68 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
         else if (tid == 0 && t + 1 <= T - 2)
           mbar_arrive_expect_tx(bar_h + 8 * (t & 1), htx);  // for h_{t+1}
       }
-      const int s = t % NS;
-      if (!dead && !wait_phase<false>(bar_full + 8 * s, (t / NS) & 1, abort_flag, p.status, tlim))
-        dead = true;
+      if (!dead && !wait_phase<false>(bar_full + 8 * s, ph, abort_flag, p.status, tlim)) dead = true;
 
       if (!dead) {
-        // ---- Wx_t values of this thread's cells
-        float wx[G][NE];
-        const uint8_t* stage = smem + L.wx + s * stage_bytes;
+        // ---- Wx_t in accumulator layout: one transposing ldmatrix per 4 tiles
+        const uint32_t stage = s_wx + s * stage_bytes;
+        uint32_t wxr[NT][NQ * 4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) {
+            const uint32_t addr = stage + nt * 8 * WP + wx_off[q];
+            if (4 * q + 4 <= NTILE) {
+              uint32_t r4[4];
+              ldmatrix_x4_trans(r4, addr);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) wxr[nt][4 * q + i] = r4[i];
+            } else {
+              uint32_t r2[2];
+              ldmatrix_x2_trans(r2, addr);
+              wxr[nt][4 * q] = r2[0];
+              wxr[nt][4 * q + 1] = r2[1];
+            }
+          }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+        if (++s == NS) {
+          s = 0;
+          ph ^= 1u;
+        }
+
+        // ---- accumulators start at scale*(Wx + bias); GRU n-gate keeps Wx_n apart
+        float acc[MT][NT][4], acc2[C::SPLITK ? MT : 1][NT][4];
+        float wxn[NE];
 #pragma unroll
         for (int us = 0; us < NSLOT; ++us)
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int ei = (us * NT + nt) * 2 + e;
-              const int n = nt * 8 + 2 * (lane & 3) + e;
-              const int ul = ub + (lane >> 2) + 8 * us;
+            for (int g = 0; g < G; ++g)
 #pragma unroll
-              for (int g = 0; g < G; ++g)
-                wx[g][ei] = bf16_to_f32(
-                    *reinterpret_cast<const uint16_t*>(stage + ((n * G + g) * U + ul) * 2));
-            }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+              for (int e = 0; e < 2; ++e) {
+                const uint32_t wv = wxr[nt][us * G + g];
+                const float x = e ? bf16_hi(wv) : bf16_lo(wv);
+                const int mt = UG == 16 ? g : g / 2;
+                const int q = UG == 16 ? us * 2 + e : (g % 2) * 2 + e;
+                if (CELL == kGRU && g == 2) {
+                  acc[mt][nt][q] = sbias[g][us];
+                  wxn[(us * NT + nt) * 2 + e] = x;
+                } else {
+                  acc[mt][nt][q] = fmaf(C::gate_scale(g), x, sbias[g][us]);
+                }
+              }
+        if (C::SPLITK) {
+#pragma unroll
+          for (int mt = 0; mt < (C::SPLITK ? MT : 1); ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) acc2[mt][nt][q] = 0.f;
+        }
 
-        // ---- acc = R^T h_{t-1}: two accumulator sets halve the k chain
-        float acc[MT][NT][4], acc2[MT][NT][4];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[mt][nt][q] = acc2[mt][nt][q] = 0.f;
+        // ---- acc += R^T h_{t-1}
         const uint32_t hb = s_h + (uint32_t)(t & 1) * NB * HPB + lm_off;
 #pragma unroll
         for (int kp = 0; kp < KS / 2; ++kp) {
@@ -351,23 +441,25 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
               for (int nt = 0; nt < NT; ++nt) {
                 if (HS) {  // hi and lo parts on two independent accumulator chains
                   mma_bf16_16816(acc[mt][nt], a, bfr[nt][2 * hf], bfr[nt][2 * hf + 1]);
-                  mma_bf16_16816(acc2[mt][nt], a, bfl[HS ? nt : 0][2 * hf],
+                  mma_bf16_16816(acc2[C::SPLITK ? mt : 0][nt], a, bfl[HS ? nt : 0][2 * hf],
                                  bfl[HS ? nt : 0][2 * hf + 1]);
-                } else if (hf == 0) {
-                  mma_bf16_16816(acc[mt][nt], a, bfr[nt][0], bfr[nt][1]);
+                } else if (C::SPLITK && hf == 1) {
+                  mma_bf16_16816(acc2[C::SPLITK ? mt : 0][nt], a, bfr[nt][2], bfr[nt][3]);
                 } else {
-                  mma_bf16_16816(acc2[mt][nt], a, bfr[nt][2], bfr[nt][3]);
+                  mma_bf16_16816(acc[mt][nt], a, bfr[nt][2 * hf], bfr[nt][2 * hf + 1]);
                 }
               }
             }
           }
         }
+        if (C::SPLITK) {
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
+          for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[mt][nt][q] += acc2[mt][nt][q];
+              for (int q = 0; q < 4; ++q) acc[mt][nt][q] += acc2[C::SPLITK ? mt : 0][nt][q];
+        }
 
         // ---- gate math and state update, one (unit, batch) cell at a time
         float hv[NE];
@@ -381,14 +473,13 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
               float r[G];
 #pragma unroll
               for (int g = 0; g < G; ++g)
-                r[g] = (UG == 16 ? acc[g][nt][us * 2 + e] : acc[g / 2][nt][(g % 2) * 2 + e]) +
-                       bias_v[g][us];
+                r[g] = UG == 16 ? acc[g][nt][us * 2 + e] : acc[g / 2][nt][(g % 2) * 2 + e];
               float h;
-              if (CELL == kLSTM) {
-                const float ig = sigmoid_fast(r[0] + wx[0][ei]);
-                const float fg = sigmoid_fast(r[1] + wx[1][ei]);
-                const float zg = tanh_fast(r[2] + wx[2][ei]);
-                const float og = sigmoid_fast(r[3] + wx[3][ei]);
+              if (CELL == kLSTM) {  // r[i,f,o] hold x/2
+                const float ig = fmaf(0.5f, tanh_fast(r[0]), 0.5f);
+                const float fg = fmaf(0.5f, tanh_fast(r[1]), 0.5f);
+                const float zg = tanh_fast(r[2]);
+                const float og = fmaf(0.5f, tanh_fast(r[3]), 0.5f);
                 const float c = fmaf(fg, st_c[ei], ig * zg);
                 st_c[ei] = c;
                 h = og * tanh_fast(c);
@@ -405,15 +496,13 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                     p.stash_c[row * DH + j] = c;
                   }
                 }
-              } else if (CELL == kGRU) {
-                const float rg = sigmoid_fast(wx[0][ei] + r[0]);
-                const float zg = sigmoid_fast(wx[1][ei] + r[1]);
-                const float ng = tanh_fast(fmaf(rg, r[2], wx[2][ei]));
+              } else if (CELL == kGRU) {  // r[r,z] hold x/2; r[n] = R_n h + b_n
+                const float rg = fmaf(0.5f, tanh_fast(r[0]), 0.5f);
+                const float zg = fmaf(0.5f, tanh_fast(r[1]), 0.5f);
+                const float ng = tanh_fast(fmaf(rg, r[2], wxn[ei]));
                 h = fmaf(zg, st_h[ei] - ng, ng);
-                st_h[ei] = h;
               } else {
-                const float pi = r[0] + wx[0][ei], pf = r[1] + wx[1][ei];
-                const float pz = r[2] + wx[2][ei], po = r[3] + wx[3][ei];
+                const float pi = r[0], pf = r[1], pz = r[2], po = r[3];
                 const float mn = fmaxf(pf + st_m[ei], pi);
                 // HS: accurate exp/tanh (the exponential gating amplifies rounding)
                 const float ig = HS ? expf(pi - mn) : __expf(pi - mn);
@@ -423,7 +512,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 st_c[ei] = c;
                 st_n[ei] = nn;
                 st_m[ei] = mn;
-                const float og = HS ? 1.f / (1.f + expf(-po)) : sigmoid_fast(po);
+                // r[o] holds o~ (HS) or o~/2 (fast path)
+                const float og = HS ? 1.f / (1.f + expf(-po)) : fmaf(0.5f, tanh_fast(po), 0.5f);
                 h = og * (c / nn);
               }
               hv[ei] = h;
@@ -431,7 +521,6 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
             }
 
         // ---- publish h_t: bf16 pairs (unit 2k, 2k+1) of one batch row
-        const bool ueven = ((lane >> 2) & 1) == 0;
         const uint32_t nbuf = s_h + (uint32_t)((t + 1) & 1) * NB * HPB;
         const bool send = t + 1 < T;
 #pragma unroll
@@ -444,12 +533,10 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
             // h of units (2k, 2k+1) for one batch row: rounded pair, and its residual pair
             const float v_ev = ueven ? hv[e0] : other, v_od = ueven ? other : hv[e0 + 1];
             const uint32_t pk = pack_bf16x2(v_ev, v_od);
-            const uint32_t pkl =
-                HS ? pack_bf16x2(v_ev - bf16_round(v_ev), v_od - bf16_round(v_od)) : 0u;
-            const int n = nt * 8 + 2 * (lane & 3) + (ueven ? 0 : 1);
-            const int j = u0 + ub + (lane >> 2) + 8 * us - (ueven ? 0 : 1);
             if (send) {
-              const uint32_t laddr = nbuf + (uint32_t)n * HPB + (uint32_t)j * 2;
+              const uint32_t laddr = nbuf + h_off[us][nt];
+              const uint32_t pkl =
+                  HS ? pack_bf16x2(v_ev - bf16_round(v_ev), v_od - bf16_round(v_od)) : 0u;
               if (CS == 1) {
                 asm volatile("st.shared.u32 [%0], %1;" ::"r"(laddr), "r"(pk) : "memory");
                 if (HS)
@@ -463,9 +550,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 }
               }
             }
-            if (n < nvalid)
-              *reinterpret_cast<uint32_t*>(hseq + (((size_t)t * B + b0 + n) * NH + head) * DH + j) =
-                  pk;
+            if (h_ok[us][nt]) *reinterpret_cast<uint32_t*>(hseq_p[us][nt]) = pk;
+            hseq_p[us][nt] += hseq_tstride;
           }
         if (t == T - 1) {
 #pragma unroll
