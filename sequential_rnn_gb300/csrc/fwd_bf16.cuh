@@ -13,13 +13,15 @@
 // with R^T as the mma.sync A operand (fragments resident in registers; for
 // very large heads the k-steps >= KREG sit in shared memory in fragment order)
 // and h_{t-1} (bf16) as the B operand read by ldmatrix from a double buffer.
-// A producer warp streams Wx_t with bulk async copies into a ring of NS stages
+// A producer warp streams Wx_t with 16-byte cp.async (all 32 lanes, each
+// lane's completion counted on the stage's mbarrier) into a ring of NS stages
 // (full/empty mbarriers); each thread picks up its Wx values with one
 // transposing ldmatrix, which lands them exactly in accumulator layout, and
 // the accumulators start from Wx + bias.  Gate math runs on the accumulator
 // registers; each thread owns whole (unit, batch) cells, so no gate exchange
 // is needed.  Sigmoid gate rows of R, Wx and bias are pre-scaled by 1/2 so a
-// sigmoid is one hardware tanh and one FMA: sigmoid(x) = (1 + tanh(x/2)) / 2.
+// sigmoid is one hardware tanh and one FMA: sigmoid(x) = (1 + tanh(x/2)) / 2;
+// LSTM/GRU gate activations of two cells share one packed fp16x2 tanh.
 //
 // Exchange of h_t: CS == 1 -> shared memory + one named barrier per step.
 // CS > 1 -> every thread st.async's its bf16 pair of h_t into every cluster
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   // ------------------------------------------------------------- set-up --
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_full + 8 * s, 32);  // one cp.async-tracked arrival per producer lane
       mbar_init(bar_empty + 8 * s, NW);
     }
     mbar_init(bar_h, 1);
@@ -199,41 +201,44 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 
   if (warp == NW) {
     // ------------------------------------------------ Wx producer warp --
-    if (lane == 0) {
-      const __nv_bfloat16* Wx = static_cast<const __nv_bfloat16*>(p.Wx);
-      const size_t tstride = (size_t)B * NH * GD;
-      const __nv_bfloat16* rowt = Wx + ((size_t)b0 * NH + head) * GD + u0;
-      int t = 0, s = 0;
-      uint32_t ph = 0;
-      for (; t < T; ++t, rowt += tstride) {
+    // The step's Wx slice is nvalid rows x G gates x U units; lane l copies the
+    // 16-byte chunks l, l+32, ... (offsets fixed for all steps, computed once).
+    constexpr int MAXCH = 32;
+    const int cpr = G * U / 8;  // chunks per batch row
+    const int nch = nvalid * cpr;
+    uint32_t dsto[MAXCH], srco[MAXCH];
+#pragma unroll
+    for (int i = 0; i < MAXCH; ++i) {
+      const int c = lane + 32 * i;
+      const int n = c / cpr, rem = c % cpr, g = rem / (U / 8), k = rem % (U / 8);
+      dsto[i] = (uint32_t)n * WP + (uint32_t)(g * U + 8 * k) * 2;
+      srco[i] = (uint32_t)(n * NH * GD + g * DH + 8 * k);
+    }
+    const __nv_bfloat16* Wx = static_cast<const __nv_bfloat16*>(p.Wx);
+    const size_t tstride = (size_t)B * NH * GD;
+    const __nv_bfloat16* rowt = Wx + ((size_t)b0 * NH + head) * GD + u0;
+    int s = 0;
+    uint32_t ph = 0;
+    for (int t = 0; t < T; ++t, rowt += tstride) {
+      bool stop = false;
+      if (lane == 0) {
         if (t >= NS && !wait_phase<false>(bar_empty + 8 * s, ph ^ 1u, abort_flag, p.status, tlim))
-          break;
-        if (*abort_flag) break;
-        mbar_arrive_expect_tx(bar_full + 8 * s, (uint32_t)nvalid * G * U * 2);
-        const uint32_t dst0 = s_wx + s * stage_bytes;
-        for (int n = 0; n < nvalid; ++n) {
-          const __nv_bfloat16* row = rowt + (size_t)n * NH * GD;
-          if (U == DH) {
-            bulk_g2s(dst0 + n * WP, row, GD * 2, bar_full + 8 * s);
-          } else {
-            for (int g = 0; g < G; ++g)
-              bulk_g2s(dst0 + n * WP + g * U * 2, row + g * DH, U * 2, bar_full + 8 * s);
-          }
-        }
-        if (++s == NS) {
-          s = 0;
-          ph ^= 1u;
-        }
+          stop = true;
+        if (*abort_flag) stop = true;
       }
-      // let every issued copy land before the CTA can exit
-      for (int tt = max(0, t - NS); tt < t; ++tt) {
-        const int ss = tt % NS;
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar_full + 8 * ss, (tt / NS) & 1)) {
-          if (globaltimer_ns() - t0 > tlim) break;
-        }
+      if (__shfl_sync(0xffffffffu, stop, 0)) break;
+      const uint32_t dst0 = s_wx + s * stage_bytes;
+#pragma unroll
+      for (int i = 0; i < MAXCH; ++i)
+        if (lane + 32 * i < nch) cp_async16(dst0 + dsto[i], rowt + srco[i]);
+      cp_async_mbar_arrive_noinc(bar_full + 8 * s);
+      if (++s == NS) {
+        s = 0;
+        ph ^= 1u;
       }
     }
+    // let every issued copy land before the CTA can exit
+    cp_async_wait_all();
     __syncwarp();
   } else {
     // ------------------------------------------------- compute warps --
@@ -320,7 +325,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     }
     // where this thread publishes its h pairs (per slot, n-tile)
     const bool ueven = ((lane >> 2) & 1) == 0;
-    uint32_t h_off[NSLOT][NT];
+    uint32_t h_off[NSLOT][NT], h_off1[NSLOT][NT];
     __nv_bfloat16* hseq_p[NSLOT][NT];
     bool h_ok[NSLOT][NT];
 #pragma unroll
@@ -330,6 +335,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
         const int n = nt * 8 + 2 * (lane & 3) + (ueven ? 0 : 1);
         const int j = u0 + ub + (lane >> 2) + 8 * us - (ueven ? 0 : 1);
         h_off[us][nt] = (uint32_t)n * HPB + (uint32_t)j * 2;
+        h_off1[us][nt] = (uint32_t)(nt * 8 + 2 * (lane & 3)) * HPB +
+                         (uint32_t)(u0 + ub + (lane >> 2) + 8 * us) * 2;
         h_ok[us][nt] = n < nvalid;
         hseq_p[us][nt] = static_cast<__nv_bfloat16*>(p.h_seq) +
                          ((size_t)(h_ok[us][nt] ? b0 + n : b0) * NH + head) * DH + j;
@@ -476,10 +483,12 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 r[g] = UG == 16 ? acc[g][nt][us * 2 + e] : acc[g / 2][nt][(g % 2) * 2 + e];
               float h;
               if (CELL == kLSTM) {  // r[i,f,o] hold x/2
-                const float ig = fmaf(0.5f, tanh_fast(r[0]), 0.5f);
-                const float fg = fmaf(0.5f, tanh_fast(r[1]), 0.5f);
-                const float zg = tanh_fast(r[2]);
-                const float og = fmaf(0.5f, tanh_fast(r[3]), 0.5f);
+                const float2 t_if = tanh2_fast(r[0], r[1]);
+                const float2 t_zo = tanh2_fast(r[2], r[3]);
+                const float ig = fmaf(0.5f, t_if.x, 0.5f);
+                const float fg = fmaf(0.5f, t_if.y, 0.5f);
+                const float zg = t_zo.x;
+                const float og = fmaf(0.5f, t_zo.y, 0.5f);
                 const float c = fmaf(fg, st_c[ei], ig * zg);
                 st_c[ei] = c;
                 h = og * tanh_fast(c);
@@ -497,8 +506,9 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                   }
                 }
               } else if (CELL == kGRU) {  // r[r,z] hold x/2; r[n] = R_n h + b_n
-                const float rg = fmaf(0.5f, tanh_fast(r[0]), 0.5f);
-                const float zg = fmaf(0.5f, tanh_fast(r[1]), 0.5f);
+                const float2 t_rz = tanh2_fast(r[0], r[1]);
+                const float rg = fmaf(0.5f, t_rz.x, 0.5f);
+                const float zg = fmaf(0.5f, t_rz.y, 0.5f);
                 const float ng = tanh_fast(fmaf(rg, r[2], wxn[ei]));
                 h = fmaf(zg, st_h[ei] - ng, ng);
               } else {
@@ -523,6 +533,20 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
         // ---- publish h_t: bf16 pairs (unit 2k, 2k+1) of one batch row
         const uint32_t nbuf = s_h + (uint32_t)((t + 1) & 1) * NB * HPB;
         const bool send = t + 1 < T;
+        if (CS == 1 && !HS && send) {
+          // own cells straight into the next buffer: no shuffle on the critical path
+#pragma unroll
+          for (int us = 0; us < NSLOT; ++us)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const __nv_bfloat16 hb16 = __float2bfloat16_rn(hv[(us * NT + nt) * 2 + e]);
+                asm volatile("st.shared.u16 [%0], %1;" ::"r"(nbuf + h_off1[us][nt] + e * HPB),
+                             "h"(*reinterpret_cast<const uint16_t*>(&hb16))
+                             : "memory");
+              }
+        }
 #pragma unroll
         for (int us = 0; us < NSLOT; ++us)
 #pragma unroll
@@ -538,7 +562,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
               const uint32_t pkl =
                   HS ? pack_bf16x2(v_ev - bf16_round(v_ev), v_od - bf16_round(v_od)) : 0u;
               if (CS == 1) {
-                asm volatile("st.shared.u32 [%0], %1;" ::"r"(laddr), "r"(pk) : "memory");
+                if (HS)
+                  asm volatile("st.shared.u32 [%0], %1;" ::"r"(laddr), "r"(pk) : "memory");
                 if (HS)
                   asm volatile("st.shared.u32 [%0], %1;" ::"r"(laddr + hpart), "r"(pkl) : "memory");
               } else {

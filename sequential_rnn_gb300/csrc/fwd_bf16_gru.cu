@@ -18,7 +18,7 @@ int launch_fwd_bf16_gru(const FwdParams& p, int Dh, int NT, cudaStream_t s, bool
   switch (Dh) {
     case 32: return launch_fwd_bf16_t<kGRU, 32, UG, 1, 2>(p, s, query_only, info);
     case 64: return launch_fwd_bf16_t<kGRU, 64, UG, 1, 4>(p, s, query_only, info);
-    case 128: return launch_fwd_bf16_t<kGRU, 128, UG, 1, 7>(p, s, query_only, info);
+    case 128: return launch_fwd_bf16_t<kGRU, 128, UG, 1, 6>(p, s, query_only, info);
     case 256: return launch_fwd_bf16_t<kGRU, 256, UG, 1, (UG == 16 ? 10 : 16)>(p, s, query_only, info);
     case 768: return launch_fwd_bf16_t<kGRU, 768, UG, 1, 10>(p, s, query_only, info);
     default: return (int)cudaErrorInvalidValue;

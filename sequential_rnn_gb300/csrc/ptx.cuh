@@ -3,6 +3,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace srnn {
 
@@ -146,6 +147,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
+// arrive on `bar` once all prior cp.async of this thread have landed (count pre-set)
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -158,6 +164,14 @@ __device__ __forceinline__ float tanh_fast(float x) {
   float y;
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+// Two hardware tanh at once on a packed fp16 pair (PTX tanh.approx.f16x2):
+// returns tanh(a), tanh(b) in fp32.  fp16 keeps 11 significant bits.
+__device__ __forceinline__ float2 tanh2_fast(float a, float b) {
+  __half2 x = __floats2half2_rn(a, b);
+  uint32_t xi = *reinterpret_cast<uint32_t*>(&x), yi;
+  asm("tanh.approx.f16x2 %0, %1;" : "=r"(yi) : "r"(xi));
+  return __half22float2(*reinterpret_cast<__half2*>(&yi));
 }
 // sigmoid(x) = (1 + tanh(x/2)) / 2  (identity), on the hardware tanh.
 __device__ __forceinline__ float sigmoid_fast(float x) { return fmaf(0.5f, tanh_fast(0.5f * x), 0.5f); }
