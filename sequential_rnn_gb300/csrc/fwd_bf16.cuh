@@ -351,75 +351,80 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 
     int s = 0;
     uint32_t ph = 0;
+    // accumulators of the step about to run, primed with scale*(Wx + bias)
+    float acc[MT][NT][4], acc2[C::SPLITK ? MT : 1][NT][4];
+    float wxn[NE];  // GRU: Wx_n stays outside r*(R_n h + b_n)
+    // Wait for the next Wx stage, move it into accumulator layout and release
+    // the stage.  Runs before the step barrier, off the recurrence's critical path.
+    auto prep = [&]() -> bool {
+      if (!wait_phase<false>(bar_full + 8 * s, ph, abort_flag, p.status, tlim)) return false;
+      const uint32_t stage = s_wx + s * stage_bytes;
+      uint32_t wxr[NT][NQ * 4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          const uint32_t addr = stage + nt * 8 * WP + wx_off[q];
+          if (4 * q + 4 <= NTILE) {
+            uint32_t r4[4];
+            ldmatrix_x4_trans(r4, addr);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) wxr[nt][4 * q + i] = r4[i];
+          } else {
+            uint32_t r2[2];
+            ldmatrix_x2_trans(r2, addr);
+            wxr[nt][4 * q] = r2[0];
+            wxr[nt][4 * q + 1] = r2[1];
+          }
+        }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+      if (++s == NS) {
+        s = 0;
+        ph ^= 1u;
+      }
+#pragma unroll
+      for (int us = 0; us < NSLOT; ++us)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const uint32_t wv = wxr[nt][us * G + g];
+              const float x = e ? bf16_hi(wv) : bf16_lo(wv);
+              const int mt = UG == 16 ? g : g / 2;
+              const int q = UG == 16 ? us * 2 + e : (g % 2) * 2 + e;
+              if (CELL == kGRU && g == 2) {
+                acc[mt][nt][q] = sbias[g][us];
+                wxn[(us * NT + nt) * 2 + e] = x;
+              } else {
+                acc[mt][nt][q] = fmaf(C::gate_scale(g), x, sbias[g][us]);
+              }
+            }
+      if (C::SPLITK) {
+#pragma unroll
+        for (int mt = 0; mt < (C::SPLITK ? MT : 1); ++mt)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc2[mt][nt][q] = 0.f;
+      }
+      return true;
+    };
+    if (!dead && T > 0 && !prep()) dead = true;
+
     for (int t = 0; t < T; ++t) {
-      // ---- wait for h_{t-1} (cluster) and Wx_t
+      // ---- wait for h_{t-1} (cluster)
       if (!dead && CS > 1 && t > 0) {
         if (!wait_phase<true>(bar_h + 8 * (t & 1), ((t - 1) >> 1) & 1, abort_flag, p.status, tlim))
           dead = true;
         else if (tid == 0 && t + 1 <= T - 2)
           mbar_arrive_expect_tx(bar_h + 8 * (t & 1), htx);  // for h_{t+1}
       }
-      if (!dead && !wait_phase<false>(bar_full + 8 * s, ph, abort_flag, p.status, tlim)) dead = true;
+      uint32_t pk_out[NSLOT][NT];  // bf16 pairs of h_t for h_seq, stored after the barrier
 
       if (!dead) {
-        // ---- Wx_t in accumulator layout: one transposing ldmatrix per 4 tiles
-        const uint32_t stage = s_wx + s * stage_bytes;
-        uint32_t wxr[NT][NQ * 4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int q = 0; q < NQ; ++q) {
-            const uint32_t addr = stage + nt * 8 * WP + wx_off[q];
-            if (4 * q + 4 <= NTILE) {
-              uint32_t r4[4];
-              ldmatrix_x4_trans(r4, addr);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) wxr[nt][4 * q + i] = r4[i];
-            } else {
-              uint32_t r2[2];
-              ldmatrix_x2_trans(r2, addr);
-              wxr[nt][4 * q] = r2[0];
-              wxr[nt][4 * q + 1] = r2[1];
-            }
-          }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-        if (++s == NS) {
-          s = 0;
-          ph ^= 1u;
-        }
-
-        // ---- accumulators start at scale*(Wx + bias); GRU n-gate keeps Wx_n apart
-        float acc[MT][NT][4], acc2[C::SPLITK ? MT : 1][NT][4];
-        float wxn[NE];
-#pragma unroll
-        for (int us = 0; us < NSLOT; ++us)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int g = 0; g < G; ++g)
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const uint32_t wv = wxr[nt][us * G + g];
-                const float x = e ? bf16_hi(wv) : bf16_lo(wv);
-                const int mt = UG == 16 ? g : g / 2;
-                const int q = UG == 16 ? us * 2 + e : (g % 2) * 2 + e;
-                if (CELL == kGRU && g == 2) {
-                  acc[mt][nt][q] = sbias[g][us];
-                  wxn[(us * NT + nt) * 2 + e] = x;
-                } else {
-                  acc[mt][nt][q] = fmaf(C::gate_scale(g), x, sbias[g][us]);
-                }
-              }
-        if (C::SPLITK) {
-#pragma unroll
-          for (int mt = 0; mt < (C::SPLITK ? MT : 1); ++mt)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int q = 0; q < 4; ++q) acc2[mt][nt][q] = 0.f;
-        }
-
         // ---- acc += R^T h_{t-1}
         const uint32_t hb = s_h + (uint32_t)(t & 1) * NB * HPB + lm_off;
 #pragma unroll
@@ -530,7 +535,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
               st_h[ei] = h;
             }
 
-        // ---- publish h_t: bf16 pairs (unit 2k, 2k+1) of one batch row
+        // ---- publish h_t
         const uint32_t nbuf = s_h + (uint32_t)((t + 1) & 1) * NB * HPB;
         const bool send = t + 1 < T;
         if (CS == 1 && !HS && send) {
@@ -547,6 +552,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                              : "memory");
               }
         }
+        // bf16 pairs (unit 2k, 2k+1) of one batch row: for h_seq and the cluster exchange
 #pragma unroll
         for (int us = 0; us < NSLOT; ++us)
 #pragma unroll
@@ -554,18 +560,17 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
             const int e0 = (us * NT + nt) * 2;
             const float mine = ueven ? hv[e0 + 1] : hv[e0];
             const float other = __shfl_xor_sync(0xffffffffu, mine, 4);
-            // h of units (2k, 2k+1) for one batch row: rounded pair, and its residual pair
             const float v_ev = ueven ? hv[e0] : other, v_od = ueven ? other : hv[e0 + 1];
             const uint32_t pk = pack_bf16x2(v_ev, v_od);
-            if (send) {
+            pk_out[us][nt] = pk;
+            if (send && (CS > 1 || HS)) {
               const uint32_t laddr = nbuf + h_off[us][nt];
+              // residual pair (HS): h - bf16(h), rounded to bf16
               const uint32_t pkl =
                   HS ? pack_bf16x2(v_ev - bf16_round(v_ev), v_od - bf16_round(v_od)) : 0u;
               if (CS == 1) {
-                if (HS)
-                  asm volatile("st.shared.u32 [%0], %1;" ::"r"(laddr), "r"(pk) : "memory");
-                if (HS)
-                  asm volatile("st.shared.u32 [%0], %1;" ::"r"(laddr + hpart), "r"(pkl) : "memory");
+                asm volatile("st.shared.u32 [%0], %1;" ::"r"(laddr), "r"(pk) : "memory");
+                asm volatile("st.shared.u32 [%0], %1;" ::"r"(laddr + hpart), "r"(pkl) : "memory");
               } else {
                 const uint32_t lbar = bar_h + 8 * ((t + 1) & 1);
                 for (int rk = 0; rk < CS; ++rk) {
@@ -575,8 +580,6 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 }
               }
             }
-            if (h_ok[us][nt]) *reinterpret_cast<uint32_t*>(hseq_p[us][nt]) = pk;
-            hseq_p[us][nt] += hseq_tstride;
           }
         if (t == T - 1) {
 #pragma unroll
@@ -596,6 +599,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 if (p.mT && CELL == kSLSTM) p.mT[si] = st_m[ei];
               }
         }
+        // ---- prime the next step's accumulators while other warps finish
+        if (send && !prep()) dead = true;
       }
       if (CS == 1) {
         // h_t visible to every compute warp; a dead warp stops all of them together
@@ -603,6 +608,14 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
       } else if (dead) {
         break;
       }
+      // h_seq stores after the barrier: they overlap the next step's loads
+#pragma unroll
+      for (int us = 0; us < NSLOT; ++us)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          if (h_ok[us][nt]) *reinterpret_cast<uint32_t*>(hseq_p[us][nt]) = pk_out[us][nt];
+          hseq_p[us][nt] += hseq_tstride;
+        }
     }
   }
   // peers may still st.async into this CTA until they pass this point
