@@ -124,7 +124,8 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   }
 }
 
-template <int CELL, int DH, int UG, int NT, int KREG, int HS>
+// CL: the head is split over a thread-block cluster (CS > 1); TR: LSTM training stash.
+template <int CELL, int DH, int UG, int NT, int KREG, int HS, int CL, int TR>
 __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     fwd_bf16_kernel(const FwdParams p) {
   using C = FwdCfg<CELL, DH, UG, NT, KREG, HS>;
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int U = p.U, NW = U / UG, CS = p.CS, NS = p.NS, T = p.T, B = p.B, NH = p.NH;
-  const uint32_t crank = CS > 1 ? cluster_ctarank() : 0u;
+  const uint32_t crank = CL ? cluster_ctarank() : 0u;
   const int cid = blockIdx.x / CS;
   const int head = cid / p.nbslices, bslice = cid % p.nbslices;
   const int u0 = (int)crank * U;
@@ -189,12 +190,12 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
-  if (tid == 0 && CS > 1) {
+  if (tid == 0 && CL) {
     // h_0 lands in buffer 1, h_1 in buffer 0 (first phase of each)
     if (T >= 2) mbar_arrive_expect_tx(bar_h + 8, htx);
     if (T >= 3) mbar_arrive_expect_tx(bar_h, htx);
   }
-  if (CS > 1) cluster_sync();
+  if (CL) cluster_sync();
   else __syncthreads();
 
   const unsigned long long tlim = p.timeout_ns;
@@ -342,7 +343,6 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                          ((size_t)(h_ok[us][nt] ? b0 + n : b0) * NH + head) * DH + j;
       }
     const size_t hseq_tstride = (size_t)B * NH * DH;
-    const bool train = (p.flags & 1) && CELL == kLSTM && p.stash_gates != nullptr;
 
     bool dead = false;
     if (p.flags & (1 << 30)) {  // test hook: a barrier nothing ever completes
@@ -413,10 +413,11 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
       return true;
     };
     if (!dead && T > 0 && !prep()) dead = true;
+    float hv[NE];  // h_t of this thread's cells (fp32)
 
     for (int t = 0; t < T; ++t) {
       // ---- wait for h_{t-1} (cluster)
-      if (!dead && CS > 1 && t > 0) {
+      if (!dead && CL && t > 0) {
         if (!wait_phase<true>(bar_h + 8 * (t & 1), ((t - 1) >> 1) & 1, abort_flag, p.status, tlim))
           dead = true;
         else if (tid == 0 && t + 1 <= T - 2)
@@ -474,7 +475,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
         }
 
         // ---- gate math and state update, one (unit, batch) cell at a time
-        float hv[NE];
+        float act[TR ? 4 : 1][TR ? NE : 1];  // LSTM gate activations for the stash
 #pragma unroll
         for (int us = 0; us < NSLOT; ++us)
 #pragma unroll
@@ -497,18 +498,11 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 const float c = fmaf(fg, st_c[ei], ig * zg);
                 st_c[ei] = c;
                 h = og * tanh_fast(c);
-                if (train) {
-                  const int n = nt * 8 + 2 * (lane & 3) + e;
-                  if (n < nvalid) {
-                    const int j = u0 + ub + (lane >> 2) + 8 * us;
-                    const size_t row = ((size_t)t * B + b0 + n) * NH + head;
-                    float* sg = p.stash_gates + row * GD + j;
-                    sg[0] = ig;
-                    sg[DH] = fg;
-                    sg[2 * DH] = zg;
-                    sg[3 * DH] = og;
-                    p.stash_c[row * DH + j] = c;
-                  }
+                if (TR) {
+                  act[0][ei] = ig;
+                  act[1][ei] = fg;
+                  act[2][ei] = zg;
+                  act[3][ei] = og;
                 }
               } else if (CELL == kGRU) {  // r[r,z] hold x/2; r[n] = R_n h + b_n
                 const float2 t_rz = tanh2_fast(r[0], r[1]);
@@ -535,10 +529,30 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
               st_h[ei] = h;
             }
 
+        if (TR) {  // training stash: gate activations and c_t of this step
+#pragma unroll
+          for (int us = 0; us < NSLOT; ++us)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int ei = (us * NT + nt) * 2 + e;
+                const int n = nt * 8 + 2 * (lane & 3) + e;
+                if (n < nvalid) {
+                  const int j = u0 + ub + (lane >> 2) + 8 * us;
+                  const size_t row = ((size_t)t * B + b0 + n) * NH + head;
+                  float* sg = p.stash_gates + row * GD + j;
+#pragma unroll
+                  for (int g = 0; g < 4; ++g) sg[g * DH] = act[TR ? g : 0][TR ? ei : 0];
+                  p.stash_c[row * DH + j] = st_c[ei];
+                }
+              }
+        }
+
         // ---- publish h_t
         const uint32_t nbuf = s_h + (uint32_t)((t + 1) & 1) * NB * HPB;
         const bool send = t + 1 < T;
-        if (CS == 1 && !HS && send) {
+        if (!CL && !HS && send) {
           // own cells straight into the next buffer: no shuffle on the critical path
 #pragma unroll
           for (int us = 0; us < NSLOT; ++us)
@@ -563,12 +577,12 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
             const float v_ev = ueven ? hv[e0] : other, v_od = ueven ? other : hv[e0 + 1];
             const uint32_t pk = pack_bf16x2(v_ev, v_od);
             pk_out[us][nt] = pk;
-            if (send && (CS > 1 || HS)) {
+            if (send && (CL || HS)) {
               const uint32_t laddr = nbuf + h_off[us][nt];
               // residual pair (HS): h - bf16(h), rounded to bf16
               const uint32_t pkl =
                   HS ? pack_bf16x2(v_ev - bf16_round(v_ev), v_od - bf16_round(v_od)) : 0u;
-              if (CS == 1) {
+              if (!CL) {
                 asm volatile("st.shared.u32 [%0], %1;" ::"r"(laddr), "r"(pk) : "memory");
                 asm volatile("st.shared.u32 [%0], %1;" ::"r"(laddr + hpart), "r"(pkl) : "memory");
               } else {
@@ -581,28 +595,10 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
               }
             }
           }
-        if (t == T - 1) {
-#pragma unroll
-          for (int us = 0; us < NSLOT; ++us)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int ei = (us * NT + nt) * 2 + e;
-                const int n = nt * 8 + 2 * (lane & 3) + e;
-                if (n >= nvalid) continue;
-                const int j = u0 + ub + (lane >> 2) + 8 * us;
-                const size_t si = ((size_t)(b0 + n) * NH + head) * DH + j;
-                if (p.hT) p.hT[si] = hv[ei];
-                if (p.cT && CELL != kGRU) p.cT[si] = st_c[ei];
-                if (p.nT && CELL == kSLSTM) p.nT[si] = st_n[ei];
-                if (p.mT && CELL == kSLSTM) p.mT[si] = st_m[ei];
-              }
-        }
         // ---- prime the next step's accumulators while other warps finish
         if (send && !prep()) dead = true;
       }
-      if (CS == 1) {
+      if (!CL) {
         // h_t visible to every compute warp; a dead warp stops all of them together
         if (bar_red_or(1, NW * 32, dead)) break;
       } else if (dead) {
@@ -617,17 +613,35 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
           hseq_p[us][nt] += hseq_tstride;
         }
     }
+    if (!dead && T > 0) {  // final states (fp32)
+#pragma unroll
+      for (int us = 0; us < NSLOT; ++us)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int ei = (us * NT + nt) * 2 + e;
+            const int n = nt * 8 + 2 * (lane & 3) + e;
+            if (n >= nvalid) continue;
+            const int j = u0 + ub + (lane >> 2) + 8 * us;
+            const size_t si = ((size_t)(b0 + n) * NH + head) * DH + j;
+            if (p.hT) p.hT[si] = hv[ei];
+            if (p.cT && CELL != kGRU) p.cT[si] = st_c[ei];
+            if (p.nT && CELL == kSLSTM) p.nT[si] = st_n[ei];
+            if (p.mT && CELL == kSLSTM) p.mT[si] = st_m[ei];
+          }
+    }
   }
   // peers may still st.async into this CTA until they pass this point
-  if (CS > 1) cluster_sync();
+  if (CL) cluster_sync();
 }
 
-template <int CELL, int DH, int UG, int NT, int KREG, int HS = 0>
-int launch_fwd_bf16_t(const FwdParams& p_in, cudaStream_t stream, bool query_only,
+template <int CELL, int DH, int UG, int NT, int KREG, int HS, int CL, int TR>
+int launch_fwd_bf16_v(const FwdParams& p_in, cudaStream_t stream, bool query_only,
                       LaunchInfo* info) {
   using C = FwdCfg<CELL, DH, UG, NT, KREG, HS>;
   FwdParams p = p_in;
-  auto kern = fwd_bf16_kernel<CELL, DH, UG, NT, KREG, HS>;
+  auto kern = fwd_bf16_kernel<CELL, DH, UG, NT, KREG, HS, CL, TR>;
   const int NW = p.U / UG;
   const int threads = (NW + 1) * 32;
   if (p.U % UG != 0 || NW < 1 || threads > C::MAXT) return (int)cudaErrorInvalidConfiguration;
@@ -668,6 +682,23 @@ int launch_fwd_bf16_t(const FwdParams& p_in, cudaStream_t stream, bool query_onl
   }
   if (query_only) return 0;
   return (int)cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+// Picks the cluster / training-stash variant of one (cell, Dh, unit group, KREG, HS).
+// Heads that cannot fit one SM (Dh >= 256) only exist as cluster variants.
+template <int CELL, int DH, int UG, int NT, int KREG, int HS = 0>
+int launch_fwd_bf16_t(const FwdParams& p, cudaStream_t stream, bool query_only,
+                      LaunchInfo* info) {
+  const bool tr = CELL == kLSTM && (p.flags & 1) && p.stash_gates != nullptr;
+  if (p.CS > 1) {
+    if (tr) return launch_fwd_bf16_v<CELL, DH, UG, NT, KREG, HS, 1, CELL == kLSTM>(p, stream, query_only, info);
+    return launch_fwd_bf16_v<CELL, DH, UG, NT, KREG, HS, 1, 0>(p, stream, query_only, info);
+  }
+  if constexpr (DH <= 128) {
+    if (tr) return launch_fwd_bf16_v<CELL, DH, UG, NT, KREG, HS, 0, CELL == kLSTM>(p, stream, query_only, info);
+    return launch_fwd_bf16_v<CELL, DH, UG, NT, KREG, HS, 0, 0>(p, stream, query_only, info);
+  }
+  return (int)cudaErrorInvalidConfiguration;
 }
 
 }  // namespace srnn

@@ -4,23 +4,15 @@
 namespace srnn {
 
 int launch_fwd_bf16_lstm(const FwdParams& p, int Dh, int NT, cudaStream_t s, bool query_only,
-                          LaunchInfo* info) {
-  // KREG: k16 steps of R^T held in registers per warp; the rest sit in shared memory.
-  constexpr int UG = 8;
-  if (NT == 2) {
-    switch (Dh) {
-      case 32: return launch_fwd_bf16_t<kLSTM, 32, UG, 2, 2>(p, s, query_only, info);
-      case 64: return launch_fwd_bf16_t<kLSTM, 64, UG, 2, 4>(p, s, query_only, info);
-      case 128: return launch_fwd_bf16_t<kLSTM, 128, UG, 2, 8>(p, s, query_only, info);
-      default: return (int)cudaErrorInvalidValue;
-    }
-  }
+                         LaunchInfo* info) {
+  // <cell, Dh, units per warp, n-tiles, KREG = k16 steps of R^T held in registers>
+  if (NT != 1) return (int)cudaErrorInvalidValue;
   switch (Dh) {
-    case 32: return launch_fwd_bf16_t<kLSTM, 32, UG, 1, 2>(p, s, query_only, info);
-    case 64: return launch_fwd_bf16_t<kLSTM, 64, UG, 1, 4>(p, s, query_only, info);
-    case 128: return launch_fwd_bf16_t<kLSTM, 128, UG, 1, 8>(p, s, query_only, info);
-    case 256: return launch_fwd_bf16_t<kLSTM, 256, UG, 1, (UG == 16 ? 10 : 16)>(p, s, query_only, info);
-    case 768: return launch_fwd_bf16_t<kLSTM, 768, UG, 1, (UG == 16 ? 12 : 20)>(p, s, query_only, info);
+    case 32: return launch_fwd_bf16_t<kLSTM, 32, 8, 1, 2>(p, s, query_only, info);
+    case 64: return launch_fwd_bf16_t<kLSTM, 64, 8, 1, 4>(p, s, query_only, info);
+    case 128: return launch_fwd_bf16_t<kLSTM, 128, 8, 1, 8>(p, s, query_only, info);
+    case 256: return launch_fwd_bf16_t<kLSTM, 256, 8, 1, 16>(p, s, query_only, info);
+    case 768: return launch_fwd_bf16_t<kLSTM, 768, 8, 1, 20>(p, s, query_only, info);
     default: return (int)cudaErrorInvalidValue;
   }
 }

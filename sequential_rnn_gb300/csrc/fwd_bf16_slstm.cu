@@ -1,14 +1,15 @@
-// bf16 forward instantiations for the SLSTM cell (see fwd_bf16.cuh).
+// bf16 forward instantiations for the sLSTM cell (see fwd_bf16.cuh).
 #include "fwd_bf16.cuh"
 
 namespace srnn {
 
 int launch_fwd_bf16_slstm(const FwdParams& p, int Dh, int NT, int hsplit, cudaStream_t s,
                           bool query_only, LaunchInfo* info) {
+  // <cell, Dh, units per warp, n-tiles, KREG = k16 steps of R^T held in registers, HS>
+  if (NT != 1) return (int)cudaErrorInvalidValue;
   if (hsplit) {
     // h_{t-1} as a bf16 hi + lo pair: the exponentially gated recurrence amplifies
     // per-step rounding of h by orders of magnitude over thousands of steps.
-    if (NT != 1) return (int)cudaErrorInvalidValue;
     switch (Dh) {
       case 32: return launch_fwd_bf16_t<kSLSTM, 32, 8, 1, 2, 1>(p, s, query_only, info);
       case 64: return launch_fwd_bf16_t<kSLSTM, 64, 8, 1, 4, 1>(p, s, query_only, info);
@@ -17,22 +18,12 @@ int launch_fwd_bf16_slstm(const FwdParams& p, int Dh, int NT, int hsplit, cudaSt
       default: return (int)cudaErrorInvalidValue;
     }
   }
-  // KREG: k16 steps of R^T held in registers per warp; the rest sit in shared memory.
-  constexpr int UG = 8;
-  if (NT == 2) {
-    switch (Dh) {
-      case 32: return launch_fwd_bf16_t<kSLSTM, 32, UG, 2, 2>(p, s, query_only, info);
-      case 64: return launch_fwd_bf16_t<kSLSTM, 64, UG, 2, 4>(p, s, query_only, info);
-      case 128: return launch_fwd_bf16_t<kSLSTM, 128, UG, 2, 8>(p, s, query_only, info);
-      default: return (int)cudaErrorInvalidValue;
-    }
-  }
   switch (Dh) {
-    case 32: return launch_fwd_bf16_t<kSLSTM, 32, UG, 1, 2>(p, s, query_only, info);
-    case 64: return launch_fwd_bf16_t<kSLSTM, 64, UG, 1, 4>(p, s, query_only, info);
-    case 128: return launch_fwd_bf16_t<kSLSTM, 128, UG, 1, 8>(p, s, query_only, info);
-    case 256: return launch_fwd_bf16_t<kSLSTM, 256, UG, 1, (UG == 16 ? 10 : 16)>(p, s, query_only, info);
-    case 768: return launch_fwd_bf16_t<kSLSTM, 768, UG, 1, 18>(p, s, query_only, info);
+    case 32: return launch_fwd_bf16_t<kSLSTM, 32, 8, 1, 2>(p, s, query_only, info);
+    case 64: return launch_fwd_bf16_t<kSLSTM, 64, 8, 1, 4>(p, s, query_only, info);
+    case 128: return launch_fwd_bf16_t<kSLSTM, 128, 8, 1, 8>(p, s, query_only, info);
+    case 256: return launch_fwd_bf16_t<kSLSTM, 256, 8, 1, 16>(p, s, query_only, info);
+    case 768: return launch_fwd_bf16_t<kSLSTM, 768, 8, 1, 18>(p, s, query_only, info);
     default: return (int)cudaErrorInvalidValue;
   }
 }
