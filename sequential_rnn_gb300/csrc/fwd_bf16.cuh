@@ -61,6 +61,7 @@ struct FwdCfg {
   static constexpr int HPARTS = HS ? 2 : 1;
   // long k chains run as two interleaved accumulator sets
   static constexpr bool SPLITK = KS >= 8 || HS;
+  static_assert(KS >= 2, "two k16 steps at least");
   // register estimate per compute thread -> largest CTA the register file holds
   static constexpr int REG_EST = MT * KREG * 4 + MT * NT * 8 + 88 + HS * NT * 8;
   static constexpr int MAXT_R = (65536 / REG_EST) / 32 * 32;
@@ -131,6 +132,10 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   using C = FwdCfg<CELL, DH, UG, NT, KREG, HS>;
   constexpr int G = C::G, GD = C::GD, MT = C::MT, KS = C::KS, KSM = C::KSM, NB = C::NB;
   constexpr int HPB = C::HPB, NE = C::NE, NSLOT = C::NSLOT, NTILE = C::NTILE, NQ = C::NQ;
+  // A cluster step is latency-bound (few warps per SM): two k chains and plain
+  // fp32 tanh.  One CTA per head is throughput-bound: packed fp16x2 tanh.
+  constexpr bool SPLITK = C::SPLITK || CL;
+  constexpr bool PACKED_TANH = !CL;
   extern __shared__ __align__(128) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -352,7 +357,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     int s = 0;
     uint32_t ph = 0;
     // accumulators of the step about to run, primed with scale*(Wx + bias)
-    float acc[MT][NT][4], acc2[C::SPLITK ? MT : 1][NT][4];
+    float acc[MT][NT][4], acc2[SPLITK ? MT : 1][NT][4];
     float wxn[NE];  // GRU: Wx_n stays outside r*(R_n h + b_n)
     // Wait for the next Wx stage, move it into accumulator layout and release
     // the stage.  Runs before the step barrier, off the recurrence's critical path.
@@ -402,9 +407,9 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 acc[mt][nt][q] = fmaf(C::gate_scale(g), x, sbias[g][us]);
               }
             }
-      if (C::SPLITK) {
+      if (SPLITK) {
 #pragma unroll
-        for (int mt = 0; mt < (C::SPLITK ? MT : 1); ++mt)
+        for (int mt = 0; mt < (SPLITK ? MT : 1); ++mt)
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -454,10 +459,10 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
               for (int nt = 0; nt < NT; ++nt) {
                 if (HS) {  // hi and lo parts on two independent accumulator chains
                   mma_bf16_16816(acc[mt][nt], a, bfr[nt][2 * hf], bfr[nt][2 * hf + 1]);
-                  mma_bf16_16816(acc2[C::SPLITK ? mt : 0][nt], a, bfl[HS ? nt : 0][2 * hf],
+                  mma_bf16_16816(acc2[SPLITK ? mt : 0][nt], a, bfl[HS ? nt : 0][2 * hf],
                                  bfl[HS ? nt : 0][2 * hf + 1]);
-                } else if (C::SPLITK && hf == 1) {
-                  mma_bf16_16816(acc2[C::SPLITK ? mt : 0][nt], a, bfr[nt][2], bfr[nt][3]);
+                } else if (SPLITK && hf == 1) {
+                  mma_bf16_16816(acc2[SPLITK ? mt : 0][nt], a, bfr[nt][2], bfr[nt][3]);
                 } else {
                   mma_bf16_16816(acc[mt][nt], a, bfr[nt][2 * hf], bfr[nt][2 * hf + 1]);
                 }
@@ -465,13 +470,13 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
             }
           }
         }
-        if (C::SPLITK) {
+        if (SPLITK) {
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-              for (int q = 0; q < 4; ++q) acc[mt][nt][q] += acc2[C::SPLITK ? mt : 0][nt][q];
+              for (int q = 0; q < 4; ++q) acc[mt][nt][q] += acc2[SPLITK ? mt : 0][nt][q];
         }
 
         // ---- gate math and state update, one (unit, batch) cell at a time
@@ -489,8 +494,10 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 r[g] = UG == 16 ? acc[g][nt][us * 2 + e] : acc[g / 2][nt][(g % 2) * 2 + e];
               float h;
               if (CELL == kLSTM) {  // r[i,f,o] hold x/2
-                const float2 t_if = tanh2_fast(r[0], r[1]);
-                const float2 t_zo = tanh2_fast(r[2], r[3]);
+                const float2 t_if = PACKED_TANH ? tanh2_fast(r[0], r[1])
+                                                : make_float2(tanh_fast(r[0]), tanh_fast(r[1]));
+                const float2 t_zo = PACKED_TANH ? tanh2_fast(r[2], r[3])
+                                                : make_float2(tanh_fast(r[2]), tanh_fast(r[3]));
                 const float ig = fmaf(0.5f, t_if.x, 0.5f);
                 const float fg = fmaf(0.5f, t_if.y, 0.5f);
                 const float zg = t_zo.x;
@@ -505,7 +512,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                   act[3][ei] = og;
                 }
               } else if (CELL == kGRU) {  // r[r,z] hold x/2; r[n] = R_n h + b_n
-                const float2 t_rz = tanh2_fast(r[0], r[1]);
+                const float2 t_rz = PACKED_TANH ? tanh2_fast(r[0], r[1])
+                                                : make_float2(tanh_fast(r[0]), tanh_fast(r[1]));
                 const float rg = fmaf(0.5f, t_rz.x, 0.5f);
                 const float zg = fmaf(0.5f, t_rz.y, 0.5f);
                 const float ng = tanh_fast(fmaf(rg, r[2], wxn[ei]));
