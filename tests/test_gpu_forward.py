@@ -115,6 +115,34 @@ def test_cluster_split_is_bitwise_identical(S, cell, Dh, clusters):
         compare(outs[c], ref, "bf16", f"cluster {c}")
 
 
+@pytest.mark.parametrize("cell,dtype,Dh", [("lstm", "bf16", 64), ("gru", "bf16", 128),
+                                           ("slstm", "bf16", 256), ("lstm", "f32", 64)])
+def test_chunking_through_final_state_is_bitwise(S, cell, dtype, Dh):
+    d = make_inputs(cell, dtype, 20, 9, 2, Dh, seed=7, bias="normal0.1", states="random")
+    g = dev(d)
+    full = run(S, d, g=g)
+    a = S.forward(cell, g["Wx"][:8].contiguous(), g["R"], g["b"], g["h0"], g["c0"],
+                  g["n0"] if cell == "slstm" else None, g["m0"] if cell == "slstm" else None)
+    b = S.forward(cell, g["Wx"][8:].contiguous(), g["R"], g["b"], a["hT"], a.get("cT"),
+                  a.get("nT"), a.get("mT"))
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([a["h_seq"], b["h_seq"]]), full["h_seq"])
+    assert torch.equal(b["hT"], full["hT"])
+
+
+def test_head_and_batch_permutation_is_bitwise(S):
+    d = make_inputs("lstm", "bf16", 12, 11, 4, 64, seed=9, bias="normal0.1", states="random")
+    g = dev(d)
+    base = run(S, d, g=g)
+    ph = torch.tensor([2, 0, 3, 1], device="cuda")
+    gp = {"Wx": g["Wx"][:, :, ph].contiguous(), "R": g["R"][ph].contiguous(),
+          "b": g["b"][ph].contiguous()}
+    for k in ("h0", "c0", "n0", "m0"):
+        gp[k] = g[k][:, ph].contiguous()
+    perm = run(S, d, g=gp)
+    assert torch.equal(perm["h_seq"], base["h_seq"][:, :, ph])
+
+
 def test_too_coarse_cluster_split_is_rejected(S):
     d = make_inputs("lstm", "bf16", 4, 2, 1, 256, seed=1)
     g = dev(d)
