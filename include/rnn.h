@@ -83,7 +83,8 @@ typedef enum {
   RNN_ERR_MISALIGNED = 3,  /* a pointer violates the alignment stated below */
   RNN_ERR_LAUNCH = 4,      /* the CUDA launch itself failed */
   RNN_ERR_TIMEOUT = 5,     /* device status: a bounded wait ran out, outputs invalid */
-  RNN_ERR_NO_CLUSTER = 6   /* the device cannot co-schedule the needed thread-block cluster */
+  RNN_ERR_NO_CLUSTER = 6,  /* the device cannot co-schedule the needed thread-block cluster */
+  RNN_ERR_SCRATCH_LIMIT = 7 /* rnn_fwd_noalloc: the call needs more scratch than its array holds */
 } rnn_status_t;
 
 /* Bytes of device workspace rnn_fwd (pass 0) / rnn_bwd (pass 1) need.
@@ -133,6 +134,24 @@ int rnn_sync_floor(const rnn_desc_t* desc, int iters, void* workspace, size_t wo
 int rnn_fwd_config(const rnn_desc_t* desc, int32_t* out6);
 
 const char* rnn_status_str(int status);
+
+/* rnn_fwd for callers that cannot allocate device memory.  The FlashRNN pages
+ * have no counterpart; this exists for callers such as a serving process that
+ * reserved its whole device-memory budget up front, or a latency-critical loop
+ * that must not risk an allocation's implicit device synchronisation.  Same
+ * arguments and behaviour as rnn_fwd minus the workspace: its scratch (the
+ * device status word) lives in a 4096-byte file-scope __device__ array of the
+ * library, held by every GPU that loads the library until the process exits.
+ * Calls needing more scratch than that return RNN_ERR_SCRATCH_LIMIT.  The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress),
+ * so make that first call before any stream capture.  Every call shares the
+ * array and clears the status word it uses; calls that overlap on the GPU race
+ * on it, and their device-side timeout status is not reported.  Allocates
+ * nothing (no cudaMalloc / cudaFree, no allocating library call). */
+int rnn_fwd_noalloc(const rnn_desc_t* desc, const void* Wx, const void* R, const float* bias,
+                    const float* h0, const float* c0, const float* n0, const float* m0,
+                    void* h_seq, float* hT, float* cT, float* nT, float* mT, void* stash,
+                    void* stream);
 
 #ifdef __cplusplus
 }

@@ -18,7 +18,8 @@ from ._lib import (CELLS, DTYPES, RNN_BF16, RNN_F32, RNN_FLAG_TEST_TIMEOUT, RNN_
                    STATUS, rnn_desc_t)
 
 __all__ = ["RnnError", "make_desc", "rnn_workspace_size", "rnn_stash_size", "rnn_fwd", "rnn_bwd",
-           "rnn_read_status", "rnn_sync_floor", "rnn_fwd_config", "rnn_status_str", "forward",
+           "rnn_read_status", "rnn_sync_floor", "rnn_fwd_config", "rnn_status_str", "rnn_fwd_noalloc",
+           "forward",
            "backward", "GATES"]
 
 GATES = {"lstm": 4, "gru": 3, "slstm": 4}
@@ -83,6 +84,14 @@ def rnn_fwd(desc, Wx, R, bias, h0, c0, n0, m0, h_seq, hT, cT, nT, mT, stash, wor
         ctypes.byref(desc), _ptr(Wx), _ptr(R), _ptr(bias), _ptr(h0), _ptr(c0), _ptr(n0), _ptr(m0),
         _ptr(h_seq), _ptr(hT), _ptr(cT), _ptr(nT), _ptr(mT), _ptr(stash), _ptr(workspace),
         ws_bytes, _stream(stream)))
+
+
+def rnn_fwd_noalloc(desc, Wx, R, bias, h0, c0, n0, m0, h_seq, hT, cT, nT, mT, stash,
+                    stream=None) -> int:
+    """rnn_fwd without a workspace, for callers that must not allocate device memory."""
+    return int(_lib.load().rnn_fwd_noalloc(
+        ctypes.byref(desc), _ptr(Wx), _ptr(R), _ptr(bias), _ptr(h0), _ptr(c0), _ptr(n0), _ptr(m0),
+        _ptr(h_seq), _ptr(hT), _ptr(cT), _ptr(nT), _ptr(mT), _ptr(stash), _stream(stream)))
 
 
 def rnn_bwd(desc, R, h0, h_seq, stash, dh_seq, dhT, dcT, dWx, dR, db, dh0, dc0, workspace,

@@ -19,13 +19,13 @@ RNN_FLAG_H_BF16 = 2
 RNN_FLAG_TEST_TIMEOUT = 1 << 30
 STATUS = {0: "RNN_OK", 1: "RNN_ERR_INVALID_ARG", 2: "RNN_ERR_UNSUPPORTED",
           3: "RNN_ERR_MISALIGNED", 4: "RNN_ERR_LAUNCH", 5: "RNN_ERR_TIMEOUT",
-          6: "RNN_ERR_NO_CLUSTER"}
+          6: "RNN_ERR_NO_CLUSTER", 7: "RNN_ERR_SCRATCH_LIMIT"}
 CELLS = {"lstm": RNN_LSTM, "gru": RNN_GRU, "slstm": RNN_SLSTM}
 DTYPES = {"f32": RNN_F32, "bf16": RNN_BF16}
 
 # Every symbol include/rnn.h declares (checked by the CPU tests).
 EXPORTS = ("rnn_workspace_size", "rnn_stash_size", "rnn_fwd", "rnn_bwd", "rnn_read_status",
-           "rnn_sync_floor", "rnn_fwd_config", "rnn_status_str")
+           "rnn_sync_floor", "rnn_fwd_config", "rnn_status_str", "rnn_fwd_noalloc")
 
 
 class rnn_desc_t(ctypes.Structure):
@@ -48,6 +48,7 @@ _SIGS = {
     "rnn_sync_floor": (_I, [_DESC, _I, _P, _SZ, _P]),
     "rnn_fwd_config": (_I, [_DESC, ctypes.POINTER(ctypes.c_int32)]),
     "rnn_status_str": (ctypes.c_char_p, [_I]),
+    "rnn_fwd_noalloc": (_I, [_DESC] + [_P] * 14),
 }
 
 _lib = None

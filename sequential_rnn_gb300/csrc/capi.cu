@@ -131,6 +131,7 @@ const char* rnn_status_str(int status) {
     case RNN_ERR_LAUNCH: return "CUDA launch failed";
     case RNN_ERR_TIMEOUT: return "device wait timed out";
     case RNN_ERR_NO_CLUSTER: return "thread-block cluster cannot be scheduled";
+    case RNN_ERR_SCRATCH_LIMIT: return "needs more scratch than the no-allocation entry point holds";
     default: return "unknown status";
   }
 }

@@ -47,7 +47,7 @@ def _fwd(lib, desc, ws=0x1000, ws_bytes=256, wx=0x2000, r=0x3000, hseq=0x4000, s
 
 
 def test_status_strings(lib):
-    for s in range(7):
+    for s in range(8):
         assert lib.rnn_status_str(s)
     assert lib.rnn_status_str(99) == b"unknown status"
 
