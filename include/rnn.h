@@ -106,16 +106,20 @@ int rnn_fwd(const rnn_desc_t* desc, const void* Wx, const void* R, const float* 
             float* hT, float* cT, float* nT, float* mT, void* stash, void* workspace,
             size_t workspace_bytes, void* stream);
 
-/* Backward through time of the LSTM (RNN_BF16, the same Dh set), from the
- * stash of a RNN_FLAG_TRAIN forward with the same desc, inputs and h_seq.
- * Gradients of L = sum(h_seq*dh_seq) + sum(hT*dhT) + sum(cT*dcT):
- *   dWx [T,B,NH,4Dh] input dtype, dR [NH,Dh,4Dh] fp32, db [NH,4Dh] fp32,
- *   dh0, dc0 [B,NH,Dh] fp32 (any of dR/db/dh0/dc0 may be NULL).
- * dhT, dcT NULL = zero.  dh_seq: input dtype, 16-byte aligned. */
-int rnn_bwd(const rnn_desc_t* desc, const void* R, const float* h0, const void* h_seq,
-            const void* stash, const void* dh_seq, const float* dhT, const float* dcT, void* dWx,
-            float* dR, float* db, float* dh0, float* dc0, void* workspace, size_t workspace_bytes,
-            void* stream);
+/* Backward through time of the LSTM (RNN_BF16; Dh in {32,64,128,256,768}),
+ * from the stash of a RNN_FLAG_TRAIN forward with the same desc, inputs and
+ * h_seq.  Gradients of L = sum(h_seq*dh_seq) + sum(hT*dhT) + sum(cT*dcT):
+ *   dWx [T,B,NH,4Dh] input dtype (= the preactivation gradient dG_t),
+ *   dR [NH,Dh,4Dh] fp32 = sum_t h_{t-1}^T dG_t (h_{-1} = h0, as bf16),
+ *   db [NH,4Dh] fp32, dh0, dc0 [B,NH,Dh] fp32 (each of dR/db/dh0/dc0 may be NULL).
+ * h0, c0: the forward's initial states (NULL = zeros).  dhT, dcT NULL = zero.
+ * dh_seq: input dtype.  Alignment: R, h_seq, dh_seq, dWx, stash 16 bytes.
+ * The backward runs the recurrence in reverse as one thread-block cluster per
+ * head (as the forward), then the dR contraction and the db reduction. */
+int rnn_bwd(const rnn_desc_t* desc, const void* R, const float* h0, const float* c0,
+            const void* h_seq, const void* stash, const void* dh_seq, const float* dhT,
+            const float* dcT, void* dWx, float* dR, float* db, float* dh0, float* dc0,
+            void* workspace, size_t workspace_bytes, void* stream);
 
 /* Synchronises `stream`, reads the device status word of `workspace` into
  * *device_status (RNN_OK or RNN_ERR_TIMEOUT).  Returns RNN_OK if the read

@@ -1,0 +1,419 @@
+// Backward through time of the head-wise LSTM (bf16 operands, fp32 state).
+//
+// FlashRNN pages: the cells are trained (blog page, paragraph on gradient
+// clipping and checkpointing during training); the recurrence runs in reverse
+// with the same resident recurrent matrix.  For step t = T-1 .. 0 and every
+// cell (b, j), from the stashed activations i, f, z, o and cell states:
+//     dh   = dh_seq[t] + dh_rec[t]                  (dh_rec[T-1] = dhT)
+//     dc   = dc_carry + dh * o * (1 - tanh(c_t)^2)  (dc_carry[T-1] = dcT)
+//     dG   = [dc*z*i(1-i), dc*c_{t-1}*f(1-f), dc*i*(1-z^2), dh*tanh(c_t)*o(1-o)]
+//     dc_carry = dc * f
+//     dh_rec[t-1] = dG_t @ R[h]^T                    (dh0 = dh_rec[-1], dc0 = dc_carry)
+// dWx_t = dG_t is written in the input dtype; db and dR are reduced later.
+//
+// Layout on sm_103a: the CTAs of one thread-block cluster own disjoint hidden
+// units of a head (U = Dh / CS each), exactly as in the forward.  Per step a
+// CTA forms dG for its own units, then computes, on tensor cores, the partial
+// product of its own gate columns with R^T for ALL Dh units:
+//     part[k, n] = sum_{own gate cols c} R[k, c] * dG[n, c]      (swap-AB mma.sync)
+// and reduce-scatters it: the bf16 partial rows of unit k go by st.async into
+// the shared memory of the CTA owning k, which sums the CS partials in fp32.
+// R's slice stays on chip for the whole loop (registers + shared memory).
+// With CS == 1 the partial is already the full sum and stays local.
+//
+// Every wait is bounded; on expiry the kernel records a timeout in the status
+// word and leaves through the same barriers as a normal run.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace srnn {
+namespace {
+
+constexpr int kNB = 8;  // batch rows per CTA (one mma n-tile)
+
+// Per head size: cluster size, warps, m16 tiles of Dh per warp, k-steps in
+// registers, cells per thread.
+template <int DH>
+struct BwdCfg;
+template <> struct BwdCfg<32> { static constexpr int CS = 1, NW = 2, KREG = 8; };
+template <> struct BwdCfg<64> { static constexpr int CS = 1, NW = 4, KREG = 16; };
+template <> struct BwdCfg<128> { static constexpr int CS = 2, NW = 8, KREG = 16; };
+template <> struct BwdCfg<256> { static constexpr int CS = 8, NW = 8, KREG = 8; };
+template <> struct BwdCfg<768> { static constexpr int CS = 16, NW = 12, KREG = 5; };
+
+template <int DH>
+struct BwdK {
+  static constexpr int CS = BwdCfg<DH>::CS, NW = BwdCfg<DH>::NW, KREG = BwdCfg<DH>::KREG;
+  static constexpr int U = DH / CS;            // units per CTA
+  static constexpr int NTH = NW * 32;
+  static constexpr int MTILES = DH / 16;       // m16 tiles over all units
+  static constexpr int MTW = MTILES / NW;      // per warp
+  static constexpr int KSW = 4 * U / 16;       // k16 steps over own gate columns
+  static constexpr int KSM = KSW - KREG;       // k-steps whose fragments sit in smem
+  static constexpr int EPT = U * kNB / NTH;    // cells per thread
+  static constexpr int DGP = ((4 * U * 2 / 16) % 2 == 0) ? 4 * U * 2 + 16 : 4 * U * 2;  // dG row pitch
+  static_assert(MTILES % NW == 0, "m tiles per warp");
+  static_assert((U * kNB) % NTH == 0, "cells per thread");
+  static_assert(KSW % 2 == 0 && KREG <= KSW && KREG >= 0, "k steps");
+  static_assert(U % 16 == 0, "own gate columns in whole k16 steps");
+  // shared memory: [R frags][dG bf16 (B operand)][dh_rec exchange][db scratch][barriers]
+  static constexpr uint32_t RF = 0;
+  static constexpr uint32_t RF_BYTES = (uint32_t)NW * MTW * KSM * 512;
+  static constexpr uint32_t DG = (RF + RF_BYTES + 127) & ~127u;
+  static constexpr uint32_t DG_BYTES = (uint32_t)kNB * DGP;
+  static constexpr uint32_t RX = (DG + DG_BYTES + 127) & ~127u;
+  // CS > 1: bf16 partials [2 buf][CS src][U unit][NB]; CS == 1: fp32 sums [U][NB]
+  static constexpr uint32_t RX_BYTES = CS > 1 ? 2u * CS * U * kNB * 2 : (uint32_t)U * kNB * 4;
+  static constexpr uint32_t DB = (RX + RX_BYTES + 127) & ~127u;
+  static constexpr uint32_t DB_BYTES = (uint32_t)kNB * 4 * U * 4;
+  static constexpr uint32_t BAR = (DB + DB_BYTES + 15) & ~15u;
+  static constexpr uint32_t FLAG = BAR + 16;
+  static constexpr uint32_t TOTAL = FLAG + 16;
+  static constexpr bool SPLIT = MTW <= 2;      // two k chains when registers allow
+};
+
+template <bool CLUSTER_ACQ>
+__device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                      int* status, unsigned long long limit_ns) {
+  if (CLUSTER_ACQ ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (CLUSTER_ACQ ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+template <int DH>
+__global__ void __launch_bounds__(BwdK<DH>::NTH, 1) bwd_lstm_kernel(const BwdParams p) {
+  using K = BwdK<DH>;
+  constexpr int CS = K::CS, U = K::U, MTW = K::MTW, KSW = K::KSW, KREG = K::KREG;
+  constexpr int KSM = K::KSM, EPT = K::EPT, NTH = K::NTH, DGP = K::DGP;
+  constexpr int GD = 4 * DH;
+  constexpr bool CL = CS > 1;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = p.T, B = p.B, NH = p.NH;
+  const uint32_t crank = CL ? cluster_ctarank() : 0u;
+  const int cid = blockIdx.x / CS;
+  const int head = cid / p.nbslices, bslice = cid % p.nbslices;
+  const int u0 = (int)crank * U;
+  const int b0 = bslice * kNB;
+  const int nvalid = min(kNB, B - b0);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t s_rf = sbase + K::RF, s_dg = sbase + K::DG, s_rx = sbase + K::RX;
+  const uint32_t bar_r = sbase + K::BAR;  // two: partial buffers 0 / 1
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + K::FLAG);
+  const unsigned long long tlim = p.timeout_ns;
+  constexpr uint32_t kTx = (uint32_t)CS * U * kNB * 2;  // partial bytes landing per step
+
+  if (tid == 0) {
+    mbar_init(bar_r, 1);
+    mbar_init(bar_r + 8, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // partials of step s (s = T-1-t, s = 0..T-1) land in buffer s&1 with phase s>>1
+  if (CL && tid == 0) {
+    mbar_arrive_expect_tx(bar_r, kTx);
+    if (T >= 2) mbar_arrive_expect_tx(bar_r + 8, kTx);
+  }
+  if (CL) cluster_sync();
+
+  // ---- A fragments: rows = all Dh units k (warp's m tiles), cols = own gate
+  //      columns c = g*U + u  ->  R[k][g*Dh + u0 + u]
+  const uint16_t* Rb = static_cast<const uint16_t*>(p.R) + (size_t)head * DH * GD;
+  uint32_t areg[MTW][KREG > 0 ? KREG : 1][4];
+  const uint32_t rf_warp = s_rf + (uint32_t)warp * MTW * KSM * 512 + lane * 16;
+#pragma unroll
+  for (int mt = 0; mt < MTW; ++mt) {
+    const int ra = (warp * MTW + mt) * 16 + (lane >> 2), rb = ra + 8;
+#pragma unroll
+    for (int ks = 0; ks < KSW; ++ks) {
+      const int c0 = ks * 16 + 2 * (lane & 3);
+      auto col = [&](int c) { return (c / U) * DH + u0 + (c % U); };
+      uint32_t a[4];
+      a[0] = (uint32_t)Rb[(size_t)ra * GD + col(c0)] | ((uint32_t)Rb[(size_t)ra * GD + col(c0 + 1)] << 16);
+      a[1] = (uint32_t)Rb[(size_t)rb * GD + col(c0)] | ((uint32_t)Rb[(size_t)rb * GD + col(c0 + 1)] << 16);
+      a[2] = (uint32_t)Rb[(size_t)ra * GD + col(c0 + 8)] |
+             ((uint32_t)Rb[(size_t)ra * GD + col(c0 + 9)] << 16);
+      a[3] = (uint32_t)Rb[(size_t)rb * GD + col(c0 + 8)] |
+             ((uint32_t)Rb[(size_t)rb * GD + col(c0 + 9)] << 16);
+      if (ks < KREG) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) areg[mt][ks < KREG ? ks : 0][q] = a[q];
+      } else {
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                         rf_warp + (uint32_t)(mt * KSM + (ks - KREG)) * 512),
+                     "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3])
+                     : "memory");
+      }
+    }
+  }
+
+  // ---- cells: ci = tid + e*NTH -> batch row n = ci / U, own unit u = ci % U
+  int cu[EPT], cn[EPT];
+  bool cok[EPT];
+  float dcar[EPT], dbacc[EPT][4], dhv[EPT];
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    const int ci = tid + e * NTH;
+    cu[e] = ci % U;
+    cn[e] = ci / U;
+    cok[e] = cn[e] < nvalid;
+    const size_t si = ((size_t)(b0 + cn[e]) * NH + head) * DH + u0 + cu[e];
+    dcar[e] = (cok[e] && p.dcT) ? p.dcT[si] : 0.f;
+    dhv[e] = (cok[e] && p.dhT) ? p.dhT[si] : 0.f;  // dh_rec of the last step
+#pragma unroll
+    for (int g = 0; g < 4; ++g) dbacc[e][g] = 0.f;
+  }
+  const __nv_bfloat16* dhs = static_cast<const __nv_bfloat16*>(p.dh_seq);
+  __nv_bfloat16* dwx = static_cast<__nv_bfloat16*>(p.dWx);
+  // per-step inputs of one cell: i f z o, c_t, c_{t-1}, upstream dh
+  auto load_step = [&](int t, int e, float (&v)[7]) {
+    if (t < 0 || !cok[e]) {
+#pragma unroll
+      for (int q = 0; q < 7; ++q) v[q] = 0.f;
+      return;
+    }
+    const size_t row = ((size_t)t * B + b0 + cn[e]) * NH + head;
+    const int j = u0 + cu[e];
+    const float* sg = p.stash_gates + row * GD + j;
+    v[0] = sg[0];
+    v[1] = sg[DH];
+    v[2] = sg[2 * DH];
+    v[3] = sg[3 * DH];
+    v[4] = p.stash_c[row * DH + j];
+    if (t > 0) {
+      v[5] = p.stash_c[(row - (size_t)B * NH) * DH + j];
+    } else {
+      v[5] = p.c_init ? p.c_init[((size_t)(b0 + cn[e]) * NH + head) * DH + j] : 0.f;
+    }
+    v[6] = __bfloat162float(dhs[row * DH + j]);
+  };
+  float cur[EPT][7], nxt[EPT][7];
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    load_step(T - 1, e, cur[e]);
+    load_step(T - 2, e, nxt[e]);
+  }
+
+  // B operand (dG) ldmatrix address of this lane; partial destination rows
+  const uint32_t lm_off = (uint32_t)(lane & 7) * DGP + (uint32_t)(lane >> 3) * 16;
+  bool dead = false;
+
+  for (int s = 0; s <= T; ++s) {  // s = T-1-t; the extra pass s = T yields dh0
+    const int t = T - 1 - s;
+    // ---- dh_rec[t] from the partials of step s-1
+    if (s > 0) {
+      if (CL) {
+        const int ps = s - 1;
+        if (!dead && !bwait<true>(bar_r + 8 * (ps & 1), (ps >> 1) & 1, abort_flag, p.status, tlim))
+          dead = true;
+        if (!dead) {
+          if (tid == 0 && ps + 2 <= T - 1) mbar_arrive_expect_tx(bar_r + 8 * (ps & 1), kTx);
+          const uint8_t* rx = smem + K::RX + (ps & 1) * (CS * U * kNB * 2);
+#pragma unroll
+          for (int e = 0; e < EPT; ++e) {
+            float acc = 0.f;
+#pragma unroll
+            for (int src = 0; src < CS; ++src)
+              acc += bf16_to_f32(*reinterpret_cast<const uint16_t*>(
+                  rx + ((src * U + cu[e]) * kNB + cn[e]) * 2));
+            dhv[e] = acc;
+          }
+        }
+      } else {
+        const float* rx = reinterpret_cast<const float*>(smem + K::RX);
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) dhv[e] = rx[cu[e] * kNB + cn[e]];
+      }
+    }
+    if (s == T) break;  // dh_rec[-1] = dh0 is in dhv
+
+    // ---- pointwise LSTM backward of this step's cells -> dG (bf16 to smem and dWx)
+    if (!dead) {
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) {
+        const float ig = cur[e][0], fg = cur[e][1], zg = cur[e][2], og = cur[e][3];
+        const float c = cur[e][4], cp = cur[e][5];
+        const float dh = cur[e][6] + dhv[e];
+        const float tc = tanhf(c);
+        const float dc = fmaf(dh * og, 1.f - tc * tc, dcar[e]);
+        float dg[4];
+        dg[0] = dc * zg * ig * (1.f - ig);
+        dg[1] = dc * cp * fg * (1.f - fg);
+        dg[2] = dc * ig * (1.f - zg * zg);
+        dg[3] = dh * tc * og * (1.f - og);
+        dcar[e] = dc * fg;
+        const size_t row = ((size_t)t * B + b0 + cn[e]) * NH + head;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const __nv_bfloat16 v = __float2bfloat16_rn(dg[g]);
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(s_dg + cn[e] * DGP + (g * U + cu[e]) * 2),
+                       "h"(*reinterpret_cast<const uint16_t*>(&v))
+                       : "memory");
+          if (cok[e]) dwx[row * GD + g * DH + u0 + cu[e]] = v;
+          dbacc[e][g] += cok[e] ? dg[g] : 0.f;
+        }
+      }
+      // next step's inputs arrive while the exchange runs
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) {
+#pragma unroll
+        for (int q = 0; q < 7; ++q) cur[e][q] = nxt[e][q];
+        load_step(t - 2, e, nxt[e]);
+      }
+    }
+    // dG of all cells in shared memory (and the previous dh_rec fully read)
+    if (bar_red_or(1, NTH, dead)) break;
+
+    // ---- partial[k, n] = sum_{own cols} R[k, c] dG[n, c] for this warp's k tiles
+    constexpr bool SPLIT = K::SPLIT;
+    float acc[MTW][4], acc2[SPLIT ? MTW : 1][4];
+#pragma unroll
+    for (int mt = 0; mt < MTW; ++mt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[mt][q] = acc2[SPLIT ? mt : 0][q] = 0.f;
+#pragma unroll
+    for (int kp = 0; kp < KSW / 2; ++kp) {
+      uint32_t bfr[4];
+      ldmatrix_x4(bfr, s_dg + lm_off + kp * 64);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int ks = 2 * kp + hf;
+#pragma unroll
+        for (int mt = 0; mt < MTW; ++mt) {
+          uint32_t a[4];
+          if (ks < KREG) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) a[q] = areg[mt][ks < KREG ? ks : 0][q];
+          } else {
+            lds128(a, rf_warp + (uint32_t)(mt * KSM + (ks - KREG)) * 512);
+          }
+          if (SPLIT && hf) mma_bf16_16816(acc2[SPLIT ? mt : 0], a, bfr[2], bfr[3]);
+          else mma_bf16_16816(acc[mt], a, bfr[2 * hf], bfr[2 * hf + 1]);
+        }
+      }
+    }
+    // ---- reduce-scatter: rows k (unit) go to the CTA owning k
+#pragma unroll
+    for (int mt = 0; mt < MTW; ++mt) {
+      const int n = 2 * (lane & 3);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int k = (warp * MTW + mt) * 16 + (lane >> 2) + 8 * half;
+        const float v0 = acc[mt][2 * half] + (SPLIT ? acc2[SPLIT ? mt : 0][2 * half] : 0.f);
+        const float v1 =
+            acc[mt][2 * half + 1] + (SPLIT ? acc2[SPLIT ? mt : 0][2 * half + 1] : 0.f);
+        if (CL) {
+          const int owner = k / U, ku = k % U;
+          const uint32_t buf = (uint32_t)(s & 1) * (CS * U * kNB * 2);
+          const uint32_t laddr = s_rx + buf + (uint32_t)((crank * U + ku) * kNB + n) * 2;
+          st_async_b32(mapa(laddr, owner), pack_bf16x2(v0, v1), mapa(bar_r + 8 * (s & 1), owner));
+        } else {
+          float2* rx = reinterpret_cast<float2*>(smem + K::RX + (k * kNB + n) * 4);
+          *rx = make_float2(v0, v1);
+        }
+      }
+    }
+    if (!CL) {
+      // partials complete; also orders the next step's dG writes after these reads
+      if (bar_red_or(1, NTH, dead)) break;
+    }
+  }
+
+  // ---- dh0, dc0 and this slice's bias-gradient partial
+  if (!dead) {
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      if (!cok[e]) continue;
+      const size_t si = ((size_t)(b0 + cn[e]) * NH + head) * DH + u0 + cu[e];
+      if (p.dh0) p.dh0[si] = dhv[e];
+      if (p.dc0) p.dc0[si] = dcar[e];
+    }
+  }
+  __syncthreads();
+  float* dbs = reinterpret_cast<float*>(smem + K::DB);  // [n][g][u]
+#pragma unroll
+  for (int e = 0; e < EPT; ++e)
+#pragma unroll
+    for (int g = 0; g < 4; ++g) dbs[(cn[e] * 4 + g) * U + cu[e]] = dbacc[e][g];
+  __syncthreads();
+  if (p.db_part && !dead) {
+    for (int i = tid; i < 4 * U; i += NTH) {
+      const int g = i / U, u = i % U;
+      float sum = 0.f;
+      for (int n = 0; n < kNB; ++n) sum += dbs[(n * 4 + g) * U + u];
+      p.db_part[((size_t)bslice * NH + head) * GD + g * DH + u0 + u] = sum;
+    }
+  }
+  if (CL) cluster_sync();
+}
+
+template <int DH>
+int launch_t(const BwdParams& p_in, cudaStream_t s, bool query_only, LaunchInfo* info) {
+  using K = BwdK<DH>;
+  BwdParams p = p_in;
+  p.CS = K::CS;
+  p.U = K::U;
+  auto kern = bwd_lstm_kernel<DH>;
+  int dev = 0, max_smem = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (K::TOTAL > (uint32_t)max_smem) return (int)cudaErrorInvalidConfiguration;
+  const int grid = p.NH * p.nbslices * K::CS;
+  if (info) *info = LaunchInfo{grid, K::NTH, K::CS, kNB, (int)K::TOTAL, 500 + DH / 32};
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::TOTAL);
+  if (e != cudaSuccess) return (int)e;
+  if (K::CS > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return (int)e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(K::NTH);
+  cfg.dynamicSmemBytes = K::TOTAL;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = K::CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = K::CS > 1 ? 1 : 0;
+  if (K::CS > 1) {
+    int ncl = 0;
+    e = cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg);
+    if (e != cudaSuccess) return (int)e;
+    if (ncl < 1) return -1;
+  }
+  if (query_only) return 0;
+  return (int)cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+}  // namespace
+
+int launch_bwd_lstm_bf16(const BwdParams& p, int Dh, cudaStream_t s, bool query_only,
+                         LaunchInfo* info) {
+  switch (Dh) {
+    case 32: return launch_t<32>(p, s, query_only, info);
+    case 64: return launch_t<64>(p, s, query_only, info);
+    case 128: return launch_t<128>(p, s, query_only, info);
+    case 256: return launch_t<256>(p, s, query_only, info);
+    case 768: return launch_t<768>(p, s, query_only, info);
+    default: return (int)cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace srnn

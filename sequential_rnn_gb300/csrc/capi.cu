@@ -255,15 +255,78 @@ int rnn_sync_floor(const rnn_desc_t* d, int iters, void* workspace, size_t works
   return map_launch_error(launch_sync_floor(li, iters, static_cast<int*>(workspace), s));
 }
 
-int rnn_bwd(const rnn_desc_t* d, const void* R, const float* h0, const void* h_seq,
-            const void* stash, const void* dh_seq, const float* dhT, const float* dcT, void* dWx,
-            float* dR, float* db, float* dh0, float* dc0, void* workspace, size_t workspace_bytes,
-            void* stream) {
-  (void)R; (void)h0; (void)h_seq; (void)stash; (void)dh_seq; (void)dhT; (void)dcT; (void)dWx;
-  (void)dR; (void)db; (void)dh0; (void)dc0; (void)workspace; (void)workspace_bytes; (void)stream;
+int rnn_bwd(const rnn_desc_t* d, const void* R, const float* h0, const float* c0,
+            const void* h_seq, const void* stash, const void* dh_seq, const float* dhT,
+            const float* dcT, void* dWx, float* dR, float* db, float* dh0, float* dc0,
+            void* workspace, size_t workspace_bytes, void* stream) {
   int st = check_desc(d);
   if (st != RNN_OK) return st;
-  return RNN_ERR_UNSUPPORTED;
+  if (d->cell != RNN_LSTM || d->dtype != RNN_BF16) return RNN_ERR_UNSUPPORTED;
+  const int Dh = d->Dh;
+  if (Dh != 32 && Dh != 64 && Dh != 128 && Dh != 256 && Dh != 768) return RNN_ERR_UNSUPPORTED;
+  if (d->B == 0 || d->NH == 0) return RNN_OK;
+  if (workspace == nullptr || workspace_bytes < rnn_workspace_size(d, 1)) return RNN_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return RNN_ERR_MISALIGNED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t nstate = (size_t)d->B * d->NH * Dh;
+  const size_t nw = (size_t)d->NH * 4 * Dh;
+  if (d->T == 0) {  // no steps: gradients pass straight through to the initial states
+    int r;
+    if ((r = copy_state(dh0, dhT, nstate, s)) != RNN_OK) return r;
+    if ((r = copy_state(dc0, dcT, nstate, s)) != RNN_OK) return r;
+    if (dR && cudaMemsetAsync(dR, 0, nw * Dh * sizeof(float), s) != cudaSuccess) return RNN_ERR_LAUNCH;
+    if (db && cudaMemsetAsync(db, 0, nw * sizeof(float), s) != cudaSuccess) return RNN_ERR_LAUNCH;
+    return RNN_OK;
+  }
+  if (R == nullptr || h_seq == nullptr || stash == nullptr || dh_seq == nullptr || dWx == nullptr)
+    return RNN_ERR_INVALID_ARG;
+  if (!aligned(R, 16) || !aligned(h_seq, 16) || !aligned(stash, 16) || !aligned(dh_seq, 16) ||
+      !aligned(dWx, 16))
+    return RNN_ERR_MISALIGNED;
+  const float* fp[] = {h0, c0, dhT, dcT, dR, db, dh0, dc0};
+  for (const float* q : fp)
+    if (!aligned(q, 8)) return RNN_ERR_MISALIGNED;
+
+  const int nbslices = (d->B + 7) / 8;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* h0b = ws + kStatusBytes;
+  float* db_part = reinterpret_cast<float*>(ws + kStatusBytes + align_up(nstate * 2, 256));
+
+  BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.R = R;
+  p.dh_seq = dh_seq;
+  p.dhT = dhT;
+  p.dcT = dcT;
+  p.stash_gates = static_cast<const float*>(stash);
+  p.stash_c = p.stash_gates + (size_t)d->T * nstate * 4;
+  p.dWx = dWx;
+  p.dh0 = dh0;
+  p.dc0 = dc0;
+  p.db_part = db ? db_part : nullptr;
+  p.status = static_cast<int*>(workspace);
+  p.T = d->T;
+  p.B = d->B;
+  p.NH = d->NH;
+  p.nbslices = nbslices;
+  p.flags = d->flags;
+  p.timeout_ns = (d->flags & RNN_FLAG_TEST_TIMEOUT) ? kTestTimeoutNs : kTimeoutNs;
+  p.c_init = c0;
+
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return RNN_ERR_LAUNCH;
+  int e = launch_bwd_lstm_bf16(p, Dh, s, false, nullptr);
+  if (e != 0) return map_launch_error(e);
+  if (dR) {
+    e = launch_h0_to_bf16(h0, h0b, (int)nstate, s);
+    if (e != 0) return map_launch_error(e);
+    e = launch_grad_weights(h_seq, h0b, dWx, dR, d->T, d->B, d->NH, Dh, 4, s);
+    if (e != 0) return map_launch_error(e);
+  }
+  if (db) {
+    e = launch_db_reduce(db_part, db, nbslices, (int)nw, s);
+    if (e != 0) return map_launch_error(e);
+  }
+  return RNN_OK;
 }
 
 }  // extern "C"

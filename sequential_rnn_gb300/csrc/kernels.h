@@ -65,7 +65,6 @@ struct BwdParams {
   const float* dcT;
   const float* stash_gates;
   const float* stash_c;
-  const float* c0;  // unused (c_{-1} comes from the stash or zero)
   void* dWx;
   float* dh0;
   float* dc0;

@@ -1,0 +1,101 @@
+"""GPU parity of the LSTM backward (BPTT) against the fp64 oracle (needs a GB300).
+
+A training forward (stash of gate activations and cell states) followed by
+rnn_bwd through the C ABI; every gradient is compared with the oracle's
+textbook BPTT on the same seeded inputs, normwise:
+    max |d| / max |oracle|  <=  5e-2     for dWx, dR, db, dh0, dc0,
+and h_seq of the training forward as in the forward tests (<= 2e-2).
+Identities between the GPU's own outputs are checked tighter: dR equals
+sum_t h_{t-1}^T dWx_t recomputed from the GPU's h_seq and dWx, db equals the
+batch/time sum of dWx.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import rnn_oracle as O
+from synth import make_inputs, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+GRAD_TOL = 5e-2
+H_TOL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def S():
+    from sequential_rnn_gb300 import build
+    build.build()
+    import sequential_rnn_gb300 as S
+    return S
+
+
+def run_fb(S, d):
+    dt = torch.bfloat16
+    g = {k: torch.from_numpy(np.ascontiguousarray(d[k])).to("cuda", dt) for k in ("Wx", "R", "dh")}
+    for k in ("b", "h0", "c0", "dhT", "dcT"):
+        g[k] = torch.from_numpy(np.ascontiguousarray(d[k])).to("cuda", torch.float32)
+    fw = S.forward("lstm", g["Wx"], g["R"], g["b"], g["h0"], g["c0"], train=True)
+    gr = S.backward(fw, g["R"], g["h0"], g["c0"], g["dh"], g["dhT"], g["dcT"])
+    torch.cuda.synchronize()
+    return g, fw, gr
+
+
+def normwise(got, ref):
+    got = got.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    return np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30)
+
+
+def check(S, d, label):
+    g, fw, gr = run_fb(S, d)
+    ref_f = O.lstm_forward(d["Wx"], d["R"], d["b"], d["h0"], d["c0"])
+    ref = O.lstm_backward(d["Wx"], d["R"], d["b"], d["h0"], d["c0"], dh_seq=d["dh"],
+                          dhT=d["dhT"], dcT=d["dcT"])
+    herr = np.abs(fw["h_seq"].float().cpu().numpy() - ref_f["h_seq"]).max()
+    assert herr <= H_TOL, (label, "h_seq", herr)
+    errs = {k: normwise(gr[k], ref[k]) for k in ("dWx", "dR", "db", "dh0", "dc0")}
+    for k, e in errs.items():
+        assert e <= GRAD_TOL, (label, k, e, errs)
+    return g, fw, gr
+
+
+def test_training_workload_full(S):
+    """LSTM 1 x 768 head, B=16, T=1024: forward with stash, then BPTT."""
+    d = workload_inputs("lstm_bf16_1x768_b16_t1024_train")
+    g, fw, gr = check(S, d, "lstm_bf16_1x768_b16_t1024_train")
+    # identities between the GPU's own outputs
+    T, B, NH, Dh = d["Wx"].shape[0], d["Wx"].shape[1], 1, 768
+    hprev = torch.cat([g["h0"].to(torch.bfloat16)[None], fw["h_seq"][:-1]]).float()
+    dwx = gr["dWx"].float()
+    dR_id = torch.einsum("tbhj,tbhk->hjk", hprev, dwx)
+    assert (gr["dR"] - dR_id).abs().max() <= 1e-3 * dR_id.abs().max()
+    db_id = dwx.sum(dim=(0, 1))
+    assert (gr["db"] - db_id).abs().max() <= 1e-2 * db_id.abs().max()
+
+
+CASES = [
+    # Dh, B, NH, T
+    (32, 3, 2, 17), (64, 13, 2, 9), (64, 1, 1, 1), (128, 9, 1, 12), (256, 5, 2, 10),
+    (256, 8, 1, 2), (768, 3, 1, 6), (768, 16, 1, 1),
+]
+
+
+@pytest.mark.parametrize("Dh,B,NH,T", CASES)
+def test_backward_small_sweep(S, Dh, B, NH, T):
+    d = make_inputs("lstm", "bf16", T, B, NH, Dh, seed=Dh + 7 * T, bias="forget1",
+                    states="random", backward=True)
+    rng = np.random.default_rng(Dh + B)
+    d["dhT"] = rng.standard_normal(d["h0"].shape).astype(np.float32)
+    d["dcT"] = rng.standard_normal(d["h0"].shape).astype(np.float32)
+    check(S, d, f"Dh{Dh}/B{B}/NH{NH}/T{T}")
+
+
+def test_backward_zero_length(S):
+    d = make_inputs("lstm", "bf16", 0, 3, 2, 64, seed=1, states="random", backward=True)
+    rng = np.random.default_rng(3)
+    d["dhT"] = rng.standard_normal(d["h0"].shape).astype(np.float32)
+    d["dcT"] = rng.standard_normal(d["h0"].shape).astype(np.float32)
+    g, fw, gr = run_fb(S, d)
+    assert torch.equal(gr["dh0"], g["dhT"]) and torch.equal(gr["dc0"], g["dcT"])
+    assert float(gr["dR"].abs().max()) == 0.0 and float(gr["db"].abs().max()) == 0.0
