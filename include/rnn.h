@@ -96,7 +96,7 @@ size_t rnn_workspace_size(const rnn_desc_t* desc, int pass);
  * the caller; pass the same buffer to rnn_bwd.  0 for cells without backward. */
 size_t rnn_stash_size(const rnn_desc_t* desc);
 
-/* Forward recurrence.  Alignment: Wx, R 16 bytes; h_seq 4 bytes; fp32
+/* Forward recurrence.  Alignment: Wx, R, h_seq, stash 16 bytes; fp32
  * pointers 4 bytes.  Supported: RNN_F32 with Dh in {16,32,64};
  * RNN_BF16 with Dh in {32,64,128,256,768} (Dh > 128 runs as a thread-block
  * cluster per head).  T == 0 copies the initial states to the final ones;

@@ -199,7 +199,7 @@ int rnn_fwd(const rnn_desc_t* d, const void* Wx, const void* R, const float* bia
     return RNN_OK;
   }
   if (Wx == nullptr || R == nullptr || h_seq == nullptr) return RNN_ERR_INVALID_ARG;
-  if (!aligned(Wx, 16) || !aligned(R, 16) || !aligned(h_seq, 4) || !aligned(stash, 16))
+  if (!aligned(Wx, 16) || !aligned(R, 16) || !aligned(h_seq, 16) || !aligned(stash, 16))
     return RNN_ERR_MISALIGNED;
   const float* fp[] = {bias, h0, c0, n0, m0, hT, cT, nT, mT};
   for (const float* q : fp)

@@ -157,7 +157,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   const uint32_t WP = C::wx_pitch(U);
   const uint32_t stage_bytes = (uint32_t)NB * WP;
   const uint32_t hpart = 2u * NB * HPB;  // byte offset of the lo part of h
-  const uint32_t htx = (uint32_t)C::HPARTS * NB * DH * 2;  // h bytes landing per step
+  // bytes of h the peers deliver per step (this CTA's own slice is stored locally)
+  const uint32_t htx = (uint32_t)C::HPARTS * NB * (DH - U) * 2;
 
   // ------------------------------------------------------------- set-up --
   if (tid == 0) {
@@ -165,8 +166,9 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
       mbar_init(bar_full + 8 * s, 32);  // one cp.async-tracked arrival per producer lane
       mbar_init(bar_empty + 8 * s, NW);
     }
-    mbar_init(bar_h, 1);
-    mbar_init(bar_h + 8, 1);
+    // cluster: one arming arrival (expect_tx for the peers' bytes) + one per local warp
+    mbar_init(bar_h, CL ? 1 + NW : 1);
+    mbar_init(bar_h + 8, CL ? 1 + NW : 1);
     mbar_init(bar_dummy, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -329,26 +331,24 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
       const int us = k / G, g = k % G;
       wx_off[q] = (uint32_t)(lane & 7) * WP + (uint32_t)(g * U + ub + 8 * us) * 2;
     }
-    // where this thread publishes its h pairs (per slot, n-tile)
-    const bool ueven = ((lane >> 2) & 1) == 0;
-    uint32_t h_off[NSLOT][NT], h_off1[NSLOT][NT];
-    __nv_bfloat16* hseq_p[NSLOT][NT];
-    bool h_ok[NSLOT][NT];
+    // where this thread's cells go in the h buffers (batch row, unit)
+    uint32_t h_off1[NSLOT][NT];
 #pragma unroll
     for (int us = 0; us < NSLOT; ++us)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int n = nt * 8 + 2 * (lane & 3) + (ueven ? 0 : 1);
-        const int j = u0 + ub + (lane >> 2) + 8 * us - (ueven ? 0 : 1);
-        h_off[us][nt] = (uint32_t)n * HPB + (uint32_t)j * 2;
+      for (int nt = 0; nt < NT; ++nt)
         h_off1[us][nt] = (uint32_t)(nt * 8 + 2 * (lane & 3)) * HPB +
                          (uint32_t)(u0 + ub + (lane >> 2) + 8 * us) * 2;
-        h_ok[us][nt] = n < nvalid;
-        hseq_p[us][nt] = static_cast<__nv_bfloat16*>(p.h_seq) +
-                         ((size_t)(h_ok[us][nt] ? b0 + n : b0) * NH + head) * DH + j;
-      }
+    // 16-byte rows of this warp's slice (UG units x NB rows): lane -> one row chunk,
+    // used to ship h_t to the cluster peers and to store h_seq
+    constexpr int NCH = NB * UG / 8;
+    const int ch_n = lane / (UG / 8), ch_k = lane % (UG / 8);
+    const bool ch_on = lane < NCH;
+    const uint32_t ch_off = (uint32_t)ch_n * HPB + (uint32_t)(u0 + ub + 8 * ch_k) * 2;
+    const bool ch_store = ch_on && ch_n < nvalid;
+    __nv_bfloat16* hseq_ch = static_cast<__nv_bfloat16*>(p.h_seq) +
+                             ((size_t)(ch_store ? b0 + ch_n : b0) * NH + head) * DH + u0 + ub + 8 * ch_k;
     const size_t hseq_tstride = (size_t)B * NH * DH;
-
     bool dead = false;
     if (p.flags & (1 << 30)) {  // test hook: a barrier nothing ever completes
       if (!wait_phase<false>(bar_dummy, 0, abort_flag, p.status, tlim)) dead = true;
@@ -428,7 +428,6 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
         else if (tid == 0 && t + 1 <= T - 2)
           mbar_arrive_expect_tx(bar_h + 8 * (t & 1), htx);  // for h_{t+1}
       }
-      uint32_t pk_out[NSLOT][NT];  // bf16 pairs of h_t for h_seq, stored after the barrier
 
       if (!dead) {
         // ---- acc += R^T h_{t-1}
@@ -557,52 +556,57 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
               }
         }
 
-        // ---- publish h_t
+        // ---- publish h_t: own cells into this CTA's next buffer (also at the last
+        //      step: h_seq is stored from there)
         const uint32_t nbuf = s_h + (uint32_t)((t + 1) & 1) * NB * HPB;
         const bool send = t + 1 < T;
-        if (!CL && !HS && send) {
-          // own cells straight into the next buffer: no shuffle on the critical path
-#pragma unroll
-          for (int us = 0; us < NSLOT; ++us)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const __nv_bfloat16 hb16 = __float2bfloat16_rn(hv[(us * NT + nt) * 2 + e]);
-                asm volatile("st.shared.u16 [%0], %1;" ::"r"(nbuf + h_off1[us][nt] + e * HPB),
-                             "h"(*reinterpret_cast<const uint16_t*>(&hb16))
-                             : "memory");
-              }
-        }
-        // bf16 pairs (unit 2k, 2k+1) of one batch row: for h_seq and the cluster exchange
 #pragma unroll
         for (int us = 0; us < NSLOT; ++us)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const int e0 = (us * NT + nt) * 2;
-            const float mine = ueven ? hv[e0 + 1] : hv[e0];
-            const float other = __shfl_xor_sync(0xffffffffu, mine, 4);
-            const float v_ev = ueven ? hv[e0] : other, v_od = ueven ? other : hv[e0 + 1];
-            const uint32_t pk = pack_bf16x2(v_ev, v_od);
-            pk_out[us][nt] = pk;
-            if (send && (CL || HS)) {
-              const uint32_t laddr = nbuf + h_off[us][nt];
-              // residual pair (HS): h - bf16(h), rounded to bf16
-              const uint32_t pkl =
-                  HS ? pack_bf16x2(v_ev - bf16_round(v_ev), v_od - bf16_round(v_od)) : 0u;
-              if (!CL) {
-                asm volatile("st.shared.u32 [%0], %1;" ::"r"(laddr), "r"(pk) : "memory");
-                asm volatile("st.shared.u32 [%0], %1;" ::"r"(laddr + hpart), "r"(pkl) : "memory");
-              } else {
-                const uint32_t lbar = bar_h + 8 * ((t + 1) & 1);
-                for (int rk = 0; rk < CS; ++rk) {
-                  const uint32_t rbar = mapa(lbar, rk);
-                  st_async_b32(mapa(laddr, rk), pk, rbar);
-                  if (HS) st_async_b32(mapa(laddr + hpart, rk), pkl, rbar);
-                }
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float hvv = hv[(us * NT + nt) * 2 + e];
+              const __nv_bfloat16 hi = __float2bfloat16_rn(hvv);
+              const uint32_t addr = nbuf + h_off1[us][nt] + e * HPB;
+              asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr),
+                           "h"(*reinterpret_cast<const uint16_t*>(&hi))
+                           : "memory");
+              if (HS) {  // residual part: bf16(h - bf16(h))
+                const __nv_bfloat16 lo = __float2bfloat16_rn(hvv - __bfloat162float(hi));
+                asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr + hpart),
+                             "h"(*reinterpret_cast<const uint16_t*>(&lo))
+                             : "memory");
               }
             }
+        if (CL) {
+          // ship this warp's slice to every peer as 16-byte rows, then count the
+          // local part on this CTA's own barrier
+          __syncwarp();
+          const uint32_t lbar = bar_h + 8 * ((t + 1) & 1);
+          if (send && ch_on) {
+            uint32_t v[4], vl[4];
+            lds128(v, nbuf + ch_off);
+            if (HS) lds128(vl, nbuf + hpart + ch_off);
+            for (int rk = 0; rk < CS; ++rk) {
+              if (rk == (int)crank) continue;
+              const uint32_t rbar = mapa(lbar, rk);
+              st_async_v4(mapa(nbuf + ch_off, rk), v, rbar);
+              if (HS) st_async_v4(mapa(nbuf + hpart + ch_off, rk), vl, rbar);
+            }
           }
+          __syncwarp();
+          if (send && lane == 0) mbar_arrive(lbar);
+          // h_seq from the same rows
+          if (ch_store) {
+            uint32_t v[4];
+            lds128(v, nbuf + ch_off);
+            asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(hseq_ch), "r"(v[0]),
+                         "r"(v[1]), "r"(v[2]), "r"(v[3])
+                         : "memory");
+          }
+          hseq_ch += hseq_tstride;
+        }
         // ---- prime the next step's accumulators while other warps finish
         if (send && !prep()) dead = true;
       }
@@ -612,14 +616,17 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
       } else if (dead) {
         break;
       }
-      // h_seq stores after the barrier: they overlap the next step's loads
-#pragma unroll
-      for (int us = 0; us < NSLOT; ++us)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          if (h_ok[us][nt]) *reinterpret_cast<uint32_t*>(hseq_p[us][nt]) = pk_out[us][nt];
-          hseq_p[us][nt] += hseq_tstride;
+      if (!CL) {
+        // h_seq rows of this warp's slice after the barrier: they overlap the next step
+        if (ch_store) {
+          uint32_t v[4];
+          lds128(v, s_h + (uint32_t)((t + 1) & 1) * NB * HPB + ch_off);
+          asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(hseq_ch), "r"(v[0]), "r"(v[1]),
+                       "r"(v[2]), "r"(v[3])
+                       : "memory");
         }
+        hseq_ch += hseq_tstride;
+      }
     }
     if (!dead && T > 0) {  // final states (fp32)
 #pragma unroll

@@ -91,6 +91,15 @@ __device__ __forceinline__ void st_async_b32(uint32_t raddr, uint32_t v, uint32_
                : "memory");
 }
 
+// 16-byte variant of st_async_b32.
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, const uint32_t (&v)[4], uint32_t rbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(
+          raddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(rbar)
+      : "memory");
+}
+
 // --------------------------------------------------------- named barrier --
 __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
