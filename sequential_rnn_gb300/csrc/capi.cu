@@ -30,10 +30,14 @@ int check_desc(const rnn_desc_t* d) {
   return RNN_OK;
 }
 
-// Default CTAs per head for the bf16 kernels: as few as hold R on chip.
+// Default CTAs per head for the bf16 kernels, from per-step timings on GB300:
+// small heads are latency-bound, so splitting them over a 4-CTA cluster (one
+// DSMEM exchange per step) beats one CTA doing all units; large heads need the
+// split to keep R on chip.
 int default_cluster(int cell, int Dh) {
-  if (Dh <= 64) return 1;
-  if (Dh == 128) return cell == RNN_GRU ? 1 : 2;
+  if (Dh <= 32) return 1;
+  if (Dh == 64) return cell == RNN_SLSTM ? 1 : 4;
+  if (Dh == 128) return cell == RNN_SLSTM ? 2 : 4;
   if (Dh == 256) return 8;
   return 16;
 }

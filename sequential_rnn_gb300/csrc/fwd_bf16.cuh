@@ -157,8 +157,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   const uint32_t WP = C::wx_pitch(U);
   const uint32_t stage_bytes = (uint32_t)NB * WP;
   const uint32_t hpart = 2u * NB * HPB;  // byte offset of the lo part of h
-  // bytes of h the peers deliver per step (this CTA's own slice is stored locally)
-  const uint32_t htx = (uint32_t)C::HPARTS * NB * (DH - U) * 2;
+  const uint32_t htx = (uint32_t)C::HPARTS * NB * DH * 2;  // h bytes landing per step (cluster)
 
   // ------------------------------------------------------------- set-up --
   if (tid == 0) {
@@ -166,9 +165,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
       mbar_init(bar_full + 8 * s, 32);  // one cp.async-tracked arrival per producer lane
       mbar_init(bar_empty + 8 * s, NW);
     }
-    // cluster: one arming arrival (expect_tx for the peers' bytes) + one per local warp
-    mbar_init(bar_h, CL ? 1 + NW : 1);
-    mbar_init(bar_h + 8, CL ? 1 + NW : 1);
+    mbar_init(bar_h, 1);
+    mbar_init(bar_h + 8, 1);
     mbar_init(bar_dummy, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -349,6 +347,22 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     __nv_bfloat16* hseq_ch = static_cast<__nv_bfloat16*>(p.h_seq) +
                              ((size_t)(ch_store ? b0 + ch_n : b0) * NH + head) * DH + u0 + ub + 8 * ch_k;
     const size_t hseq_tstride = (size_t)B * NH * DH;
+    // cluster: bf16 pairs (unit 2k, 2k+1) of one batch row, one per (slot, n-tile)
+    const bool ueven = ((lane >> 2) & 1) == 0;
+    uint32_t h_off[NSLOT][NT];
+    __nv_bfloat16* hseq_p[NSLOT][NT];
+    bool h_ok[NSLOT][NT];
+#pragma unroll
+    for (int us = 0; us < NSLOT; ++us)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int n = nt * 8 + 2 * (lane & 3) + (ueven ? 0 : 1);
+        const int j = u0 + ub + (lane >> 2) + 8 * us - (ueven ? 0 : 1);
+        h_off[us][nt] = (uint32_t)n * HPB + (uint32_t)j * 2;
+        h_ok[us][nt] = n < nvalid;
+        hseq_p[us][nt] = static_cast<__nv_bfloat16*>(p.h_seq) +
+                         ((size_t)(h_ok[us][nt] ? b0 + n : b0) * NH + head) * DH + j;
+      }
     bool dead = false;
     if (p.flags & (1 << 30)) {  // test hook: a barrier nothing ever completes
       if (!wait_phase<false>(bar_dummy, 0, abort_flag, p.status, tlim)) dead = true;
@@ -556,56 +570,58 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
               }
         }
 
-        // ---- publish h_t: own cells into this CTA's next buffer (also at the last
-        //      step: h_seq is stored from there)
+        // ---- publish h_t
         const uint32_t nbuf = s_h + (uint32_t)((t + 1) & 1) * NB * HPB;
         const bool send = t + 1 < T;
-#pragma unroll
-        for (int us = 0; us < NSLOT; ++us)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float hvv = hv[(us * NT + nt) * 2 + e];
-              const __nv_bfloat16 hi = __float2bfloat16_rn(hvv);
-              const uint32_t addr = nbuf + h_off1[us][nt] + e * HPB;
-              asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr),
-                           "h"(*reinterpret_cast<const uint16_t*>(&hi))
-                           : "memory");
-              if (HS) {  // residual part: bf16(h - bf16(h))
-                const __nv_bfloat16 lo = __float2bfloat16_rn(hvv - __bfloat162float(hi));
-                asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr + hpart),
-                             "h"(*reinterpret_cast<const uint16_t*>(&lo))
-                             : "memory");
-              }
-            }
         if (CL) {
-          // ship this warp's slice to every peer as 16-byte rows, then count the
-          // local part on this CTA's own barrier
-          __syncwarp();
+          // bf16 pairs (unit 2k, 2k+1) of one batch row straight from registers into
+          // every cluster CTA's buffer, this one included
           const uint32_t lbar = bar_h + 8 * ((t + 1) & 1);
-          if (send && ch_on) {
-            uint32_t v[4], vl[4];
-            lds128(v, nbuf + ch_off);
-            if (HS) lds128(vl, nbuf + hpart + ch_off);
-            for (int rk = 0; rk < CS; ++rk) {
-              if (rk == (int)crank) continue;
-              const uint32_t rbar = mapa(lbar, rk);
-              st_async_v4(mapa(nbuf + ch_off, rk), v, rbar);
-              if (HS) st_async_v4(mapa(nbuf + hpart + ch_off, rk), vl, rbar);
+#pragma unroll
+          for (int us = 0; us < NSLOT; ++us)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const int e0 = (us * NT + nt) * 2;
+              const float mine = ueven ? hv[e0 + 1] : hv[e0];
+              const float other = __shfl_xor_sync(0xffffffffu, mine, 4);
+              const float v_ev = ueven ? hv[e0] : other, v_od = ueven ? other : hv[e0 + 1];
+              const uint32_t pk = pack_bf16x2(v_ev, v_od);
+              if (send) {
+                const uint32_t laddr = nbuf + h_off[us][nt];
+                // residual pair (HS): h - bf16(h), rounded to bf16
+                const uint32_t pkl =
+                    HS ? pack_bf16x2(v_ev - bf16_round(v_ev), v_od - bf16_round(v_od)) : 0u;
+                for (int rk = 0; rk < CS; ++rk) {
+                  const uint32_t rbar = mapa(lbar, rk);
+                  st_async_b32(mapa(laddr, rk), pk, rbar);
+                  if (HS) st_async_b32(mapa(laddr + hpart, rk), pkl, rbar);
+                }
+              }
+              if (h_ok[us][nt]) *reinterpret_cast<uint32_t*>(hseq_p[us][nt]) = pk;
+              hseq_p[us][nt] += hseq_tstride;
             }
-          }
-          __syncwarp();
-          if (send && lane == 0) mbar_arrive(lbar);
-          // h_seq from the same rows
-          if (ch_store) {
-            uint32_t v[4];
-            lds128(v, nbuf + ch_off);
-            asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(hseq_ch), "r"(v[0]),
-                         "r"(v[1]), "r"(v[2]), "r"(v[3])
-                         : "memory");
-          }
-          hseq_ch += hseq_tstride;
+        } else {
+          // own cells into the next buffer (also at the last step: h_seq is stored
+          // from there after the barrier)
+#pragma unroll
+          for (int us = 0; us < NSLOT; ++us)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float hvv = hv[(us * NT + nt) * 2 + e];
+                const __nv_bfloat16 hi = __float2bfloat16_rn(hvv);
+                const uint32_t addr = nbuf + h_off1[us][nt] + e * HPB;
+                asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr),
+                             "h"(*reinterpret_cast<const uint16_t*>(&hi))
+                             : "memory");
+                if (HS) {  // residual part: bf16(h - bf16(h))
+                  const __nv_bfloat16 lo = __float2bfloat16_rn(hvv - __bfloat162float(hi));
+                  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr + hpart),
+                               "h"(*reinterpret_cast<const uint16_t*>(&lo))
+                               : "memory");
+                }
+              }
         }
         // ---- prime the next step's accumulators while other warps finish
         if (send && !prep()) dead = true;
