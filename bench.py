@@ -290,12 +290,9 @@ def run_ours(args, w, rank, world, local_rank):
         wall = time.perf_counter() - wall0
     per = [a.elapsed_time(b) for a, b in ev]  # ms
     t_step = sum(per) / len(per) / 1e3
-    # max over ranks
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([t_step], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_step = float(tt.item())
+    # the job takes as long as its slowest rank
+    from sequential_rnn_gb300.dist import max_over_ranks
+    t_step = max_over_ranks(t_step, device=dev)
     if S.rnn_read_status(ws):
         raise S.RnnError(S.rnn_read_status(ws), "timed region (device)")
 
