@@ -44,7 +44,7 @@ template <> struct BwdCfg<32> { static constexpr int CS = 1, NW = 2, KREG = 8; }
 template <> struct BwdCfg<64> { static constexpr int CS = 1, NW = 4, KREG = 16; };
 template <> struct BwdCfg<128> { static constexpr int CS = 2, NW = 8, KREG = 16; };
 template <> struct BwdCfg<256> { static constexpr int CS = 8, NW = 8, KREG = 8; };
-template <> struct BwdCfg<768> { static constexpr int CS = 16, NW = 12, KREG = 5; };
+template <> struct BwdCfg<768> { static constexpr int CS = 16, NW = 12, KREG = 4; };
 
 template <int DH>
 struct BwdK {
@@ -67,11 +67,14 @@ struct BwdK {
   static constexpr uint32_t DG = (RF + RF_BYTES + 127) & ~127u;
   static constexpr uint32_t DG_BYTES = (uint32_t)kNB * DGP;
   static constexpr uint32_t RX = (DG + DG_BYTES + 127) & ~127u;
-  // CS > 1: bf16 partials [2 buf][CS src][U unit][NB]; CS == 1: fp32 sums [U][NB]
+  // CS > 1: bf16 partials [2 buf][CS src][NB][U unit]; CS == 1: fp32 sums [NB][U]
   static constexpr uint32_t RX_BYTES = CS > 1 ? 2u * CS * U * kNB * 2 : (uint32_t)U * kNB * 4;
-  static constexpr uint32_t DB = (RX + RX_BYTES + 127) & ~127u;
+  // db scratch is used only after the last exchange: it aliases the dG and partial
+  // buffers when they are large enough, else it gets its own region
   static constexpr uint32_t DB_BYTES = (uint32_t)kNB * 4 * U * 4;
-  static constexpr uint32_t BAR = (DB + DB_BYTES + 15) & ~15u;
+  static constexpr bool DB_ALIAS = DB_BYTES <= RX + RX_BYTES - DG;
+  static constexpr uint32_t DB = DB_ALIAS ? DG : ((RX + RX_BYTES + 127) & ~127u);
+  static constexpr uint32_t BAR = ((DB_ALIAS ? RX + RX_BYTES : DB + DB_BYTES) + 15) & ~15u;
   static constexpr uint32_t FLAG = BAR + 16;
   static constexpr uint32_t TOTAL = FLAG + 16;
   static constexpr bool SPLIT = MTW <= 2;      // two k chains when registers allow
@@ -201,18 +204,21 @@ __global__ void __launch_bounds__(BwdK<DH>::NTH, 1) bwd_lstm_kernel(const BwdPar
     }
     v[6] = __bfloat162float(dhs[row * DH + j]);
   };
-  float cur[EPT][7], nxt[EPT][7];
+  float bufA[EPT][7], bufB[EPT][7];  // inputs of steps t (A) and t-1 (B)
 #pragma unroll
   for (int e = 0; e < EPT; ++e) {
-    load_step(T - 1, e, cur[e]);
-    load_step(T - 2, e, nxt[e]);
+    load_step(T - 1, e, bufA[e]);
+    load_step(T - 2, e, bufB[e]);
   }
 
   // B operand (dG) ldmatrix address of this lane; partial destination rows
   const uint32_t lm_off = (uint32_t)(lane & 7) * DGP + (uint32_t)(lane >> 3) * 16;
   bool dead = false;
 
-  for (int s = 0; s <= T; ++s) {  // s = T-1-t; the extra pass s = T yields dh0
+  // one reverse step s (t = T-1-s) on the inputs in `cur`; refills `cur` with the
+  // inputs of step t-2 (two buffers alternate: the loads get two steps to land).
+  // Returns true when the loop ends (s == T yields dh0, or every thread gave up).
+  auto rstep = [&](int s, float (&cur)[EPT][7]) -> bool {
     const int t = T - 1 - s;
     // ---- dh_rec[t] from the partials of step s-1
     if (s > 0) {
@@ -229,17 +235,17 @@ __global__ void __launch_bounds__(BwdK<DH>::NTH, 1) bwd_lstm_kernel(const BwdPar
 #pragma unroll
             for (int src = 0; src < CS; ++src)
               acc += bf16_to_f32(*reinterpret_cast<const uint16_t*>(
-                  rx + ((src * U + cu[e]) * kNB + cn[e]) * 2));
+                  rx + ((src * kNB + cn[e]) * U + cu[e]) * 2));
             dhv[e] = acc;
           }
         }
       } else {
         const float* rx = reinterpret_cast<const float*>(smem + K::RX);
 #pragma unroll
-        for (int e = 0; e < EPT; ++e) dhv[e] = rx[cu[e] * kNB + cn[e]];
+        for (int e = 0; e < EPT; ++e) dhv[e] = rx[cn[e] * U + cu[e]];
       }
     }
-    if (s == T) break;  // dh_rec[-1] = dh0 is in dhv
+    if (s == T) return true;  // dh_rec[-1] = dh0 is in dhv
 
     // ---- pointwise LSTM backward of this step's cells -> dG (bf16 to smem and dWx)
     if (!dead) {
@@ -267,16 +273,12 @@ __global__ void __launch_bounds__(BwdK<DH>::NTH, 1) bwd_lstm_kernel(const BwdPar
           dbacc[e][g] += cok[e] ? dg[g] : 0.f;
         }
       }
-      // next step's inputs arrive while the exchange runs
+      // inputs of step t-2 arrive while the exchange runs
 #pragma unroll
-      for (int e = 0; e < EPT; ++e) {
-#pragma unroll
-        for (int q = 0; q < 7; ++q) cur[e][q] = nxt[e][q];
-        load_step(t - 2, e, nxt[e]);
-      }
+      for (int e = 0; e < EPT; ++e) load_step(t - 2, e, cur[e]);
     }
     // dG of all cells in shared memory (and the previous dh_rec fully read)
-    if (bar_red_or(1, NTH, dead)) break;
+    if (bar_red_or(1, NTH, dead)) return true;
 
     // ---- partial[k, n] = sum_{own cols} R[k, c] dG[n, c] for this warp's k tiles
     constexpr bool SPLIT = K::SPLIT;
@@ -316,24 +318,35 @@ __global__ void __launch_bounds__(BwdK<DH>::NTH, 1) bwd_lstm_kernel(const BwdPar
         const float v0 = acc[mt][2 * half] + (SPLIT ? acc2[SPLIT ? mt : 0][2 * half] : 0.f);
         const float v1 =
             acc[mt][2 * half + 1] + (SPLIT ? acc2[SPLIT ? mt : 0][2 * half + 1] : 0.f);
+        // pair units (k, k+1) of one batch row with the neighbour lane (k^1): the
+        // even lane keeps batch n, the odd one batch n+1; rows stay unit-contiguous
+        const bool kev = ((lane >> 2) & 1) == 0;
+        const float other = __shfl_xor_sync(0xffffffffu, kev ? v1 : v0, 4);
+        const float p0 = kev ? v0 : other, p1 = kev ? other : v1;
+        const int nn = n + (kev ? 0 : 1), ke = k & ~1;
         if (CL) {
-          const int owner = k / U, ku = k % U;
+          const int owner = ke / U, ku = ke % U;
           const uint32_t buf = (uint32_t)(s & 1) * (CS * U * kNB * 2);
-          const uint32_t laddr = s_rx + buf + (uint32_t)((crank * U + ku) * kNB + n) * 2;
-          st_async_b32(mapa(laddr, owner), pack_bf16x2(v0, v1), mapa(bar_r + 8 * (s & 1), owner));
+          const uint32_t laddr = s_rx + buf + (uint32_t)((crank * kNB + nn) * U + ku) * 2;
+          st_async_b32(mapa(laddr, owner), pack_bf16x2(p0, p1), mapa(bar_r + 8 * (s & 1), owner));
         } else {
-          float2* rx = reinterpret_cast<float2*>(smem + K::RX + (k * kNB + n) * 4);
-          *rx = make_float2(v0, v1);
+          *reinterpret_cast<float2*>(smem + K::RX + (nn * U + ke) * 4) = make_float2(p0, p1);
         }
       }
     }
     if (!CL) {
       // partials complete; also orders the next step's dG writes after these reads
-      if (bar_red_or(1, NTH, dead)) break;
+      if (bar_red_or(1, NTH, dead)) return true;
     }
+    return false;
+  };
+  for (int s = 0;; s += 2) {
+    if (rstep(s, bufA)) break;
+    if (rstep(s + 1, bufB)) break;
   }
 
-  // ---- dh0, dc0 and this slice's bias-gradient partial
+  // ---- dh0, dc0 and this slice's bias-gradient partial (every exchange is done:
+  //      the last pass consumed the final partials, so the buffers can be reused)
   if (!dead) {
 #pragma unroll
     for (int e = 0; e < EPT; ++e) {
