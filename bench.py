@@ -250,8 +250,9 @@ def run_ours(args, w, rank, world, local_rank):
         if st:
             raise S.RnnError(st, "rnn_fwd")
         if w["backward"]:
-            st = S.rnn_bwd(desc, g["R"] if R is None else R, g["h0"], g["c0"], h_seq, stash, g["dh"], None,
-                           None, gr["dWx"], gr["dR"], gr["db"], gr["dh0"], gr["dc0"], wsb, stream)
+            st = S.rnn_bwd(desc, g["R"] if R is None else R, g["h0"], g["c0"], None, h_seq, stash,
+                           g["dh"], None, None, None, gr["dWx"], gr["dR"], gr["db"], gr["dh0"],
+                           gr["dc0"], None, wsb, stream)
             if st:
                 raise S.RnnError(st, "rnn_bwd")
 

@@ -91,9 +91,10 @@ typedef enum {
  * Always >= 256 (the status word lives at offset 0).  0 on invalid desc. */
 size_t rnn_workspace_size(const rnn_desc_t* desc, int pass);
 
-/* Bytes of the training stash rnn_fwd writes with RNN_FLAG_TRAIN (LSTM:
- * gate activations fp32 [T,B,NH,4*Dh] then c_t fp32 [T,B,NH,Dh]).  Opaque to
- * the caller; pass the same buffer to rnn_bwd.  0 for cells without backward. */
+/* Bytes of the training stash rnn_fwd writes with RNN_FLAG_TRAIN (bf16 only):
+ * four gate values fp32 [T,B,NH,4*Dh], then one state fp32 [T,B,NH,Dh] (LSTM c_t,
+ * GRU h_t), then for the sLSTM n_t [T,B,NH,Dh].  Opaque to the caller; pass the
+ * same buffer to rnn_bwd. */
 size_t rnn_stash_size(const rnn_desc_t* desc);
 
 /* Forward recurrence.  Alignment: Wx, R, h_seq, stash 16 bytes; fp32
@@ -106,20 +107,25 @@ int rnn_fwd(const rnn_desc_t* desc, const void* Wx, const void* R, const float* 
             float* hT, float* cT, float* nT, float* mT, void* stash, void* workspace,
             size_t workspace_bytes, void* stream);
 
-/* Backward through time of the LSTM (RNN_BF16; Dh in {32,64,128,256,768}),
+/* Backward through time (RNN_BF16; LSTM, GRU or sLSTM; Dh in {32,64,128,256,768}),
  * from the stash of a RNN_FLAG_TRAIN forward with the same desc, inputs and
- * h_seq.  Gradients of L = sum(h_seq*dh_seq) + sum(hT*dhT) + sum(cT*dcT):
- *   dWx [T,B,NH,4Dh] input dtype (= the preactivation gradient dG_t),
- *   dR [NH,Dh,4Dh] fp32 = sum_t h_{t-1}^T dG_t (h_{-1} = h0, as bf16),
- *   db [NH,4Dh] fp32, dh0, dc0 [B,NH,Dh] fp32 (each of dR/db/dh0/dc0 may be NULL).
- * h0, c0: the forward's initial states (NULL = zeros).  dhT, dcT NULL = zero.
- * dh_seq: input dtype.  Alignment: R, h_seq, dh_seq, dWx, stash 16 bytes.
- * The backward runs the recurrence in reverse as one thread-block cluster per
- * head (as the forward), then the dR contraction and the db reduction. */
+ * h_seq.  Gradients of L = sum(h_seq*dh_seq) + sum(hT*dhT) + sum(cT*dcT) + sum(nT*dnT):
+ *   dWx [T,B,NH,G*Dh] input dtype,
+ *   dR [NH,Dh,G*Dh] fp32 = sum_t h_{t-1}^T dG_t (h_{-1} = h0 as bf16; dG the
+ *      gradient of the recurrent preactivation h@R+b, = dWx except the GRU n block),
+ *   db [NH,G*Dh] fp32 = sum_t dG_t, dh0, dc0, dn0 [B,NH,Dh] fp32
+ *   (dc0: LSTM/sLSTM, dn0: sLSTM; each of dR/db/dh0/dc0/dn0 may be NULL).
+ * h0, c0, n0: the forward's initial states (NULL = zeros).  dhT, dcT, dnT: upstream
+ * gradients of the final states (NULL = zero).  The sLSTM stabiliser carries no
+ * gradient (the output does not depend on it).  dh_seq: input dtype.  Alignment:
+ * R, h_seq, dh_seq, dWx, stash 16 bytes; fp32 pointers 8 bytes; workspace 256.
+ * The reverse recurrence runs as one thread-block cluster per head slice (as the
+ * forward), then the dR contraction and the db reduction. */
 int rnn_bwd(const rnn_desc_t* desc, const void* R, const float* h0, const float* c0,
-            const void* h_seq, const void* stash, const void* dh_seq, const float* dhT,
-            const float* dcT, void* dWx, float* dR, float* db, float* dh0, float* dc0,
-            void* workspace, size_t workspace_bytes, void* stream);
+            const float* n0, const void* h_seq, const void* stash, const void* dh_seq,
+            const float* dhT, const float* dcT, const float* dnT, void* dWx, float* dR, float* db,
+            float* dh0, float* dc0, float* dn0, void* workspace, size_t workspace_bytes,
+            void* stream);
 
 /* Synchronises `stream`, reads the device status word of `workspace` into
  * *device_status (RNN_OK or RNN_ERR_TIMEOUT).  Returns RNN_OK if the read

@@ -94,14 +94,13 @@ def rnn_fwd_noalloc(desc, Wx, R, bias, h0, c0, n0, m0, h_seq, hT, cT, nT, mT, st
         _ptr(h_seq), _ptr(hT), _ptr(cT), _ptr(nT), _ptr(mT), _ptr(stash), _stream(stream)))
 
 
-def rnn_bwd(desc, R, h0, c0, h_seq, stash, dh_seq, dhT, dcT, dWx, dR, db, dh0, dc0, workspace,
-            stream=None) -> int:
+def rnn_bwd(desc, R, h0, c0, n0, h_seq, stash, dh_seq, dhT, dcT, dnT, dWx, dR, db, dh0, dc0, dn0,
+            workspace, stream=None) -> int:
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     return int(_lib.load().rnn_bwd(
-        ctypes.byref(desc), _ptr(R), _ptr(h0), _ptr(c0), _ptr(h_seq), _ptr(stash), _ptr(dh_seq),
-        _ptr(dhT),
-        _ptr(dcT), _ptr(dWx), _ptr(dR), _ptr(db), _ptr(dh0), _ptr(dc0), _ptr(workspace), ws_bytes,
-        _stream(stream)))
+        ctypes.byref(desc), _ptr(R), _ptr(h0), _ptr(c0), _ptr(n0), _ptr(h_seq), _ptr(stash),
+        _ptr(dh_seq), _ptr(dhT), _ptr(dcT), _ptr(dnT), _ptr(dWx), _ptr(dR), _ptr(db), _ptr(dh0),
+        _ptr(dc0), _ptr(dn0), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def rnn_read_status(workspace, stream=None) -> int:
@@ -157,19 +156,25 @@ def forward(cell: str, Wx, R, bias=None, h0=None, c0=None, n0=None, m0=None, *, 
     return out
 
 
-def backward(fwd: dict, R, h0, c0, dh_seq, dhT=None, dcT=None, *, stream=None, check=True):
+def backward(fwd: dict, R, h0, c0, dh_seq, dhT=None, dcT=None, *, n0=None, dnT=None, stream=None,
+             check=True):
     """Run rnn_bwd after ``forward(..., train=True)``; returns the gradients."""
     desc = fwd["desc"]
     T, B, NH, Dh = desc.T, desc.B, desc.NH, desc.Dh
-    G = 4
+    cell = {v: k for k, v in CELLS.items()}[desc.cell]
+    G = GATES[cell]
     dev = R.device
     f32 = dict(dtype=torch.float32, device=dev)
     g = {"dWx": torch.empty((T, B, NH, G * Dh), dtype=R.dtype, device=dev),
          "dR": torch.empty((NH, Dh, G * Dh), **f32), "db": torch.empty((NH, G * Dh), **f32),
-         "dh0": torch.empty((B, NH, Dh), **f32), "dc0": torch.empty((B, NH, Dh), **f32)}
+         "dh0": torch.empty((B, NH, Dh), **f32)}
+    if cell != "gru":
+        g["dc0"] = torch.empty((B, NH, Dh), **f32)
+    if cell == "slstm":
+        g["dn0"] = torch.empty((B, NH, Dh), **f32)
     ws = torch.zeros(rnn_workspace_size(desc, 1), dtype=torch.uint8, device=dev)
-    st = rnn_bwd(desc, R, h0, c0, fwd["h_seq"], fwd["stash"], dh_seq, dhT, dcT, g["dWx"], g["dR"],
-                 g["db"], g["dh0"], g["dc0"], ws, stream)
+    st = rnn_bwd(desc, R, h0, c0, n0, fwd["h_seq"], fwd["stash"], dh_seq, dhT, dcT, dnT, g["dWx"],
+                 g["dR"], g["db"], g["dh0"], g.get("dc0"), g.get("dn0"), ws, stream)
     if st:
         raise RnnError(st, "rnn_bwd")
     if check:

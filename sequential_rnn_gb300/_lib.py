@@ -43,7 +43,7 @@ _SIGS = {
     "rnn_workspace_size": (_SZ, [_DESC, _I]),
     "rnn_stash_size": (_SZ, [_DESC]),
     "rnn_fwd": (_I, [_DESC] + [_P] * 14 + [_SZ, _P]),
-    "rnn_bwd": (_I, [_DESC] + [_P] * 14 + [_SZ, _P]),
+    "rnn_bwd": (_I, [_DESC] + [_P] * 17 + [_SZ, _P]),
     "rnn_read_status": (_I, [_P, _P, ctypes.POINTER(_I)]),
     "rnn_sync_floor": (_I, [_DESC, _I, _P, _SZ, _P]),
     "rnn_fwd_config": (_I, [_DESC, ctypes.POINTER(ctypes.c_int32)]),

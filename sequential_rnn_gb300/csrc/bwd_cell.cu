@@ -1,23 +1,28 @@
-// Backward through time of the head-wise LSTM (bf16 operands, fp32 state).
+// Backward through time of the head-wise LSTM / GRU / sLSTM (bf16 operands,
+// fp32 state).
 //
 // FlashRNN pages: the cells are trained (blog page, paragraph on gradient
 // clipping and checkpointing during training); the recurrence runs in reverse
 // with the same resident recurrent matrix.  For step t = T-1 .. 0 and every
-// cell (b, j), from the stashed activations i, f, z, o and cell states:
-//     dh   = dh_seq[t] + dh_rec[t]                  (dh_rec[T-1] = dhT)
-//     dc   = dc_carry + dh * o * (1 - tanh(c_t)^2)  (dc_carry[T-1] = dcT)
-//     dG   = [dc*z*i(1-i), dc*c_{t-1}*f(1-f), dc*i*(1-z^2), dh*tanh(c_t)*o(1-o)]
-//     dc_carry = dc * f
-//     dh_rec[t-1] = dG_t @ R[h]^T                    (dh0 = dh_rec[-1], dc0 = dc_carry)
-// dWx_t = dG_t is written in the input dtype; db and dR are reduced later.
+// cell (b, j), from the values the training forward stashed:
+//   LSTM  dh = dh_seq + dh_rec;  dc = dc' + dh*o*(1 - tanh(c)^2)
+//         dG = [dc*z*i(1-i), dc*c_{t-1}*f(1-f), dc*i*(1-z^2), dh*tanh(c)*o(1-o)];  dc' <- dc*f
+//   GRU   dh = dh_seq + dh_rec + dh'*z';  dn~ = dh(1-z)(1-n^2);  dz~ = dh(h_{t-1}-n)z(1-z)
+//         dr~ = dn~*(R_n h + b_n)*r(1-r);  dWx = [dr~, dz~, dn~];  dG = [dr~, dz~, r*dn~]
+//   sLSTM dh = dh_seq + dh_rec;  do = dh*c/n;  dc = dc' + dh*o/n;  dn = dn' - dh*o*c/n^2
+//         dG = [(dc*z + dn)*i, (dc*c_{t-1} + dn*n_{t-1})*f, dc*i*(1-z^2), do*o(1-o)]
+//         dc' <- dc*f, dn' <- dn*f   (the stabiliser m carries no gradient)
+//   all   dh_rec[t-1] = dG_t @ R[h]^T;  dh0 = dh_rec[-1] (+ GRU direct term)
+// dWx_t is written in the input dtype; db sums dG; dR = sum_t h_{t-1}^T dG_t is
+// a GEMM afterwards (grad_weights.cu).
 //
 // Layout on sm_103a: the CTAs of one thread-block cluster own disjoint hidden
-// units of a head (U = Dh / CS each), exactly as in the forward.  Per step a
-// CTA forms dG for its own units, then computes, on tensor cores, the partial
-// product of its own gate columns with R^T for ALL Dh units:
+// units of a head (U = Dh / CS each), as in the forward.  Per step a CTA forms
+// dG for its own units, then computes on tensor cores the partial product of
+// its own gate columns with R^T for ALL Dh units:
 //     part[k, n] = sum_{own gate cols c} R[k, c] * dG[n, c]      (swap-AB mma.sync)
-// and reduce-scatters it: the bf16 partial rows of unit k go by st.async into
-// the shared memory of the CTA owning k, which sums the CS partials in fp32.
+// and reduce-scatters it: bf16 partial rows of unit k go by st.async into the
+// shared memory of the CTA owning k, which sums the CS partials in fp32.
 // R's slice stays on chip for the whole loop (registers + shared memory).
 // With CS == 1 the partial is already the full sum and stays local.
 //
@@ -36,8 +41,7 @@ namespace {
 
 constexpr int kNB = 8;  // batch rows per CTA (one mma n-tile)
 
-// Per head size: cluster size, warps, m16 tiles of Dh per warp, k-steps in
-// registers, cells per thread.
+// Per head size: cluster size, warps, k-steps of the R slice held in registers.
 template <int DH>
 struct BwdCfg;
 template <> struct BwdCfg<32> { static constexpr int CS = 1, NW = 2, KREG = 8; };
@@ -46,22 +50,25 @@ template <> struct BwdCfg<128> { static constexpr int CS = 2, NW = 8, KREG = 16;
 template <> struct BwdCfg<256> { static constexpr int CS = 8, NW = 8, KREG = 8; };
 template <> struct BwdCfg<768> { static constexpr int CS = 16, NW = 12, KREG = 4; };
 
-template <int DH>
+template <int CELL, int DH>
 struct BwdK {
-  static constexpr int CS = BwdCfg<DH>::CS, NW = BwdCfg<DH>::NW, KREG = BwdCfg<DH>::KREG;
+  static constexpr int G = CELL == kGRU ? 3 : 4;
+  static constexpr int CS = BwdCfg<DH>::CS, NW = BwdCfg<DH>::NW;
   static constexpr int U = DH / CS;            // units per CTA
   static constexpr int NTH = NW * 32;
   static constexpr int MTILES = DH / 16;       // m16 tiles over all units
   static constexpr int MTW = MTILES / NW;      // per warp
-  static constexpr int KSW = 4 * U / 16;       // k16 steps over own gate columns
+  static constexpr int KSW = G * U / 16;       // k16 steps over own gate columns
+  static constexpr int KREG = BwdCfg<DH>::KREG < KSW ? BwdCfg<DH>::KREG : KSW;
   static constexpr int KSM = KSW - KREG;       // k-steps whose fragments sit in smem
   static constexpr int EPT = U * kNB / NTH;    // cells per thread
-  static constexpr int DGP = ((4 * U * 2 / 16) % 2 == 0) ? 4 * U * 2 + 16 : 4 * U * 2;  // dG row pitch
+  // per-cell inputs of a step (stash values, previous states, upstream dh)
+  static constexpr int NV = CELL == kLSTM ? 7 : (CELL == kGRU ? 6 : 9);
+  static constexpr int DGP = ((G * U * 2 / 16) % 2 == 0) ? G * U * 2 + 16 : G * U * 2;  // dG row pitch
   static_assert(MTILES % NW == 0, "m tiles per warp");
   static_assert((U * kNB) % NTH == 0, "cells per thread");
-  static_assert(KSW % 2 == 0 && KREG <= KSW && KREG >= 0, "k steps");
   static_assert(U % 16 == 0, "own gate columns in whole k16 steps");
-  // shared memory: [R frags][dG bf16 (B operand)][dh_rec exchange][db scratch][barriers]
+  // shared memory: [R frags][dG bf16 (B operand)][dh_rec exchange][barriers]
   static constexpr uint32_t RF = 0;
   static constexpr uint32_t RF_BYTES = (uint32_t)NW * MTW * KSM * 512;
   static constexpr uint32_t DG = (RF + RF_BYTES + 127) & ~127u;
@@ -71,7 +78,7 @@ struct BwdK {
   static constexpr uint32_t RX_BYTES = CS > 1 ? 2u * CS * U * kNB * 2 : (uint32_t)U * kNB * 4;
   // db scratch is used only after the last exchange: it aliases the dG and partial
   // buffers when they are large enough, else it gets its own region
-  static constexpr uint32_t DB_BYTES = (uint32_t)kNB * 4 * U * 4;
+  static constexpr uint32_t DB_BYTES = (uint32_t)kNB * G * U * 4;
   static constexpr bool DB_ALIAS = DB_BYTES <= RX + RX_BYTES - DG;
   static constexpr uint32_t DB = DB_ALIAS ? DG : ((RX + RX_BYTES + 127) & ~127u);
   static constexpr uint32_t BAR = ((DB_ALIAS ? RX + RX_BYTES : DB + DB_BYTES) + 15) & ~15u;
@@ -96,12 +103,12 @@ __device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile in
   }
 }
 
-template <int DH>
-__global__ void __launch_bounds__(BwdK<DH>::NTH, 1) bwd_lstm_kernel(const BwdParams p) {
-  using K = BwdK<DH>;
-  constexpr int CS = K::CS, U = K::U, MTW = K::MTW, KSW = K::KSW, KREG = K::KREG;
-  constexpr int KSM = K::KSM, EPT = K::EPT, NTH = K::NTH, DGP = K::DGP;
-  constexpr int GD = 4 * DH;
+template <int CELL, int DH>
+__global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const BwdParams p) {
+  using K = BwdK<CELL, DH>;
+  constexpr int G = K::G, CS = K::CS, U = K::U, MTW = K::MTW, KSW = K::KSW, KREG = K::KREG;
+  constexpr int KSM = K::KSM, EPT = K::EPT, NTH = K::NTH, DGP = K::DGP, NV = K::NV;
+  constexpr int GD = G * DH;
   constexpr bool CL = CS > 1;
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -167,7 +174,8 @@ __global__ void __launch_bounds__(BwdK<DH>::NTH, 1) bwd_lstm_kernel(const BwdPar
   // ---- cells: ci = tid + e*NTH -> batch row n = ci / U, own unit u = ci % U
   int cu[EPT], cn[EPT];
   bool cok[EPT];
-  float dcar[EPT], dbacc[EPT][4], dhv[EPT];
+  // carries: LSTM dc; GRU dh*z (direct path to h_{t-1}); sLSTM dc and dn
+  float dcar[EPT], dncar[EPT], dbacc[EPT][G], dhv[EPT];
 #pragma unroll
   for (int e = 0; e < EPT; ++e) {
     const int ci = tid + e * NTH;
@@ -175,50 +183,58 @@ __global__ void __launch_bounds__(BwdK<DH>::NTH, 1) bwd_lstm_kernel(const BwdPar
     cn[e] = ci / U;
     cok[e] = cn[e] < nvalid;
     const size_t si = ((size_t)(b0 + cn[e]) * NH + head) * DH + u0 + cu[e];
-    dcar[e] = (cok[e] && p.dcT) ? p.dcT[si] : 0.f;
+    dcar[e] = (CELL != kGRU && cok[e] && p.dcT) ? p.dcT[si] : 0.f;
+    dncar[e] = (CELL == kSLSTM && cok[e] && p.dnT) ? p.dnT[si] : 0.f;
     dhv[e] = (cok[e] && p.dhT) ? p.dhT[si] : 0.f;  // dh_rec of the last step
 #pragma unroll
-    for (int g = 0; g < 4; ++g) dbacc[e][g] = 0.f;
+    for (int g = 0; g < G; ++g) dbacc[e][g] = 0.f;
   }
   const __nv_bfloat16* dhs = static_cast<const __nv_bfloat16*>(p.dh_seq);
   __nv_bfloat16* dwx = static_cast<__nv_bfloat16*>(p.dWx);
-  // per-step inputs of one cell: i f z o, c_t, c_{t-1}, upstream dh
-  auto load_step = [&](int t, int e, float (&v)[7]) {
+  __nv_bfloat16* drec = static_cast<__nv_bfloat16*>(p.drec);
+  const size_t tstep = (size_t)B * NH;  // rows per time step
+  // per-step inputs of one cell (see NV): the stash row of step t, the state of
+  // step t-1 (or the initial state), and the upstream dh
+  auto load_step = [&](int t, int e, float (&v)[NV]) {
     if (t < 0 || !cok[e]) {
 #pragma unroll
-      for (int q = 0; q < 7; ++q) v[q] = 0.f;
+      for (int q = 0; q < NV; ++q) v[q] = 0.f;
       return;
     }
     const size_t row = ((size_t)t * B + b0 + cn[e]) * NH + head;
     const int j = u0 + cu[e];
-    const float* sg = p.stash_gates + row * GD + j;
-    v[0] = sg[0];
-    v[1] = sg[DH];
-    v[2] = sg[2 * DH];
-    v[3] = sg[3 * DH];
-    v[4] = p.stash_c[row * DH + j];
-    if (t > 0) {
-      v[5] = p.stash_c[(row - (size_t)B * NH) * DH + j];
+    const size_t si0 = ((size_t)(b0 + cn[e]) * NH + head) * DH + j;  // initial-state index
+    const float* sg = p.stash_gates + row * 4 * DH + j;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) v[g] = sg[g * DH];
+    if (CELL == kLSTM) {
+      v[4] = p.stash_c[row * DH + j];
+      v[5] = t > 0 ? p.stash_c[(row - tstep) * DH + j] : (p.c_init ? p.c_init[si0] : 0.f);
+    } else if (CELL == kGRU) {
+      v[4] = t > 0 ? p.stash_c[(row - tstep) * DH + j] : (p.h_init ? p.h_init[si0] : 0.f);
     } else {
-      v[5] = p.c_init ? p.c_init[((size_t)(b0 + cn[e]) * NH + head) * DH + j] : 0.f;
+      v[4] = p.stash_c[row * DH + j];
+      v[5] = p.stash_n[row * DH + j];
+      v[6] = t > 0 ? p.stash_c[(row - tstep) * DH + j] : (p.c_init ? p.c_init[si0] : 0.f);
+      v[7] = t > 0 ? p.stash_n[(row - tstep) * DH + j] : (p.n_init ? p.n_init[si0] : 0.f);
     }
-    v[6] = __bfloat162float(dhs[row * DH + j]);
+    v[NV - 1] = __bfloat162float(dhs[row * DH + j]);
   };
-  float bufA[EPT][7], bufB[EPT][7];  // inputs of steps t (A) and t-1 (B)
+  float bufA[EPT][NV], bufB[EPT][NV];  // inputs of steps t (A) and t-1 (B)
 #pragma unroll
   for (int e = 0; e < EPT; ++e) {
     load_step(T - 1, e, bufA[e]);
     load_step(T - 2, e, bufB[e]);
   }
 
-  // B operand (dG) ldmatrix address of this lane; partial destination rows
+  // B operand (dG) ldmatrix address of this lane
   const uint32_t lm_off = (uint32_t)(lane & 7) * DGP + (uint32_t)(lane >> 3) * 16;
   bool dead = false;
 
   // one reverse step s (t = T-1-s) on the inputs in `cur`; refills `cur` with the
   // inputs of step t-2 (two buffers alternate: the loads get two steps to land).
   // Returns true when the loop ends (s == T yields dh0, or every thread gave up).
-  auto rstep = [&](int s, float (&cur)[EPT][7]) -> bool {
+  auto rstep = [&](int s, float (&cur)[EPT][NV]) -> bool {
     const int t = T - 1 - s;
     // ---- dh_rec[t] from the partials of step s-1
     if (s > 0) {
@@ -245,31 +261,64 @@ __global__ void __launch_bounds__(BwdK<DH>::NTH, 1) bwd_lstm_kernel(const BwdPar
         for (int e = 0; e < EPT; ++e) dhv[e] = rx[cn[e] * U + cu[e]];
       }
     }
-    if (s == T) return true;  // dh_rec[-1] = dh0 is in dhv
+    if (s == T) return true;  // dh_rec[-1] is in dhv
 
-    // ---- pointwise LSTM backward of this step's cells -> dG (bf16 to smem and dWx)
+    // ---- pointwise backward of this step's cells -> dG (bf16 to smem), dWx
     if (!dead) {
 #pragma unroll
       for (int e = 0; e < EPT; ++e) {
-        const float ig = cur[e][0], fg = cur[e][1], zg = cur[e][2], og = cur[e][3];
-        const float c = cur[e][4], cp = cur[e][5];
-        const float dh = cur[e][6] + dhv[e];
-        const float tc = tanhf(c);
-        const float dc = fmaf(dh * og, 1.f - tc * tc, dcar[e]);
-        float dg[4];
-        dg[0] = dc * zg * ig * (1.f - ig);
-        dg[1] = dc * cp * fg * (1.f - fg);
-        dg[2] = dc * ig * (1.f - zg * zg);
-        dg[3] = dh * tc * og * (1.f - og);
-        dcar[e] = dc * fg;
+        const float* v = cur[e];
+        float dg[G], dx[G];  // recurrent-preactivation gradient, input-projection gradient
+        if (CELL == kLSTM) {
+          const float ig = v[0], fg = v[1], zg = v[2], og = v[3], c = v[4], cp = v[5];
+          const float dh = v[6] + dhv[e];
+          const float tc = tanhf(c);
+          const float dc = fmaf(dh * og, 1.f - tc * tc, dcar[e]);
+          dg[0] = dc * zg * ig * (1.f - ig);
+          dg[1] = dc * cp * fg * (1.f - fg);
+          dg[2] = dc * ig * (1.f - zg * zg);
+          dg[3] = dh * tc * og * (1.f - og);
+          dcar[e] = dc * fg;
+#pragma unroll
+          for (int g = 0; g < G; ++g) dx[g] = dg[g];
+        } else if (CELL == kGRU) {
+          const float rg = v[0], zg = v[1], ng = v[2], rn = v[3], hp = v[4];
+          const float dh = v[5] + dhv[e] + dcar[e];
+          const float dnp = dh * (1.f - zg) * (1.f - ng * ng);
+          const float dzp = dh * (hp - ng) * zg * (1.f - zg);
+          const float drp = dnp * rn * rg * (1.f - rg);
+          dx[0] = dg[0] = drp;
+          dx[1] = dg[1] = dzp;
+          dx[2] = dnp;
+          dg[2] = dnp * rg;
+          dcar[e] = dh * zg;
+        } else {
+          const float ig = v[0], fg = v[1], zg = v[2], og = v[3];
+          const float c = v[4], nn = v[5], cp = v[6], np = v[7];
+          const float dh = v[8] + dhv[e];
+          const float rn = 1.f / nn;
+          const float dc = fmaf(dh * og, rn, dcar[e]);
+          const float dn = dncar[e] - dh * og * c * rn * rn;
+          dg[0] = fmaf(dc, zg, dn) * ig;
+          dg[1] = fmaf(dc, cp, dn * np) * fg;
+          dg[2] = dc * ig * (1.f - zg * zg);
+          dg[3] = dh * c * rn * og * (1.f - og);
+          dcar[e] = dc * fg;
+          dncar[e] = dn * fg;
+#pragma unroll
+          for (int g = 0; g < G; ++g) dx[g] = dg[g];
+        }
         const size_t row = ((size_t)t * B + b0 + cn[e]) * NH + head;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const __nv_bfloat16 v = __float2bfloat16_rn(dg[g]);
+        for (int g = 0; g < G; ++g) {
+          const __nv_bfloat16 vg = __float2bfloat16_rn(dg[g]);
           asm volatile("st.shared.u16 [%0], %1;" ::"r"(s_dg + cn[e] * DGP + (g * U + cu[e]) * 2),
-                       "h"(*reinterpret_cast<const uint16_t*>(&v))
+                       "h"(*reinterpret_cast<const uint16_t*>(&vg))
                        : "memory");
-          if (cok[e]) dwx[row * GD + g * DH + u0 + cu[e]] = v;
+          if (cok[e]) {
+            dwx[row * GD + g * DH + u0 + cu[e]] = __float2bfloat16_rn(dx[g]);
+            if (CELL == kGRU && drec) drec[row * GD + g * DH + u0 + cu[e]] = vg;
+          }
           dbacc[e][g] += cok[e] ? dg[g] : 0.f;
         }
       }
@@ -288,12 +337,23 @@ __global__ void __launch_bounds__(BwdK<DH>::NTH, 1) bwd_lstm_kernel(const BwdPar
 #pragma unroll
       for (int q = 0; q < 4; ++q) acc[mt][q] = acc2[SPLIT ? mt : 0][q] = 0.f;
 #pragma unroll
-    for (int kp = 0; kp < KSW / 2; ++kp) {
+    for (int kp = 0; kp < (KSW + 1) / 2; ++kp) {
       uint32_t bfr[4];
-      ldmatrix_x4(bfr, s_dg + lm_off + kp * 64);
+      if (2 * kp + 1 < KSW) {
+        ldmatrix_x4(bfr, s_dg + lm_off + kp * 64);
+      } else {  // odd tail: one k16 step (lanes 16..31 supply unused addresses)
+        uint32_t b2[2];
+        asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+                     : "=r"(b2[0]), "=r"(b2[1])
+                     : "r"(s_dg + (uint32_t)(lane & 7) * DGP + (uint32_t)((lane >> 3) & 1) * 16 + kp * 64));
+        bfr[0] = b2[0];
+        bfr[1] = b2[1];
+        bfr[2] = bfr[3] = 0u;
+      }
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int ks = 2 * kp + hf;
+        if (ks >= KSW) continue;
 #pragma unroll
         for (int mt = 0; mt < MTW; ++mt) {
           uint32_t a[4];
@@ -345,15 +405,17 @@ __global__ void __launch_bounds__(BwdK<DH>::NTH, 1) bwd_lstm_kernel(const BwdPar
     if (rstep(s + 1, bufB)) break;
   }
 
-  // ---- dh0, dc0 and this slice's bias-gradient partial (every exchange is done:
-  //      the last pass consumed the final partials, so the buffers can be reused)
+  // ---- initial-state gradients and this slice's bias-gradient partial (every
+  //      exchange is done: the last pass consumed the final partials, so the
+  //      buffers can be reused)
   if (!dead) {
 #pragma unroll
     for (int e = 0; e < EPT; ++e) {
       if (!cok[e]) continue;
       const size_t si = ((size_t)(b0 + cn[e]) * NH + head) * DH + u0 + cu[e];
-      if (p.dh0) p.dh0[si] = dhv[e];
-      if (p.dc0) p.dc0[si] = dcar[e];
+      if (p.dh0) p.dh0[si] = dhv[e] + (CELL == kGRU ? dcar[e] : 0.f);
+      if (p.dc0 && CELL != kGRU) p.dc0[si] = dcar[e];
+      if (p.dn0 && CELL == kSLSTM) p.dn0[si] = dncar[e];
     }
   }
   __syncthreads();
@@ -361,32 +423,32 @@ __global__ void __launch_bounds__(BwdK<DH>::NTH, 1) bwd_lstm_kernel(const BwdPar
 #pragma unroll
   for (int e = 0; e < EPT; ++e)
 #pragma unroll
-    for (int g = 0; g < 4; ++g) dbs[(cn[e] * 4 + g) * U + cu[e]] = dbacc[e][g];
+    for (int g = 0; g < G; ++g) dbs[(cn[e] * G + g) * U + cu[e]] = dbacc[e][g];
   __syncthreads();
   if (p.db_part && !dead) {
-    for (int i = tid; i < 4 * U; i += NTH) {
+    for (int i = tid; i < G * U; i += NTH) {
       const int g = i / U, u = i % U;
       float sum = 0.f;
-      for (int n = 0; n < kNB; ++n) sum += dbs[(n * 4 + g) * U + u];
+      for (int n = 0; n < kNB; ++n) sum += dbs[(n * G + g) * U + u];
       p.db_part[((size_t)bslice * NH + head) * GD + g * DH + u0 + u] = sum;
     }
   }
   if (CL) cluster_sync();
 }
 
-template <int DH>
+template <int CELL, int DH>
 int launch_t(const BwdParams& p_in, cudaStream_t s, bool query_only, LaunchInfo* info) {
-  using K = BwdK<DH>;
+  using K = BwdK<CELL, DH>;
   BwdParams p = p_in;
   p.CS = K::CS;
   p.U = K::U;
-  auto kern = bwd_lstm_kernel<DH>;
+  auto kern = bwd_cell_kernel<CELL, DH>;
   int dev = 0, max_smem = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (K::TOTAL > (uint32_t)max_smem) return (int)cudaErrorInvalidConfiguration;
   const int grid = p.NH * p.nbslices * K::CS;
-  if (info) *info = LaunchInfo{grid, K::NTH, K::CS, kNB, (int)K::TOTAL, 500 + DH / 32};
+  if (info) *info = LaunchInfo{grid, K::NTH, K::CS, kNB, (int)K::TOTAL, 500 + CELL * 100 + DH / 32};
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::TOTAL);
   if (e != cudaSuccess) return (int)e;
   if (K::CS > 8) {
@@ -415,18 +477,25 @@ int launch_t(const BwdParams& p_in, cudaStream_t s, bool query_only, LaunchInfo*
   return (int)cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-}  // namespace
-
-int launch_bwd_lstm_bf16(const BwdParams& p, int Dh, cudaStream_t s, bool query_only,
-                         LaunchInfo* info) {
+template <int CELL>
+int launch_cell(const BwdParams& p, int Dh, cudaStream_t s, bool q, LaunchInfo* info) {
   switch (Dh) {
-    case 32: return launch_t<32>(p, s, query_only, info);
-    case 64: return launch_t<64>(p, s, query_only, info);
-    case 128: return launch_t<128>(p, s, query_only, info);
-    case 256: return launch_t<256>(p, s, query_only, info);
-    case 768: return launch_t<768>(p, s, query_only, info);
+    case 32: return launch_t<CELL, 32>(p, s, q, info);
+    case 64: return launch_t<CELL, 64>(p, s, q, info);
+    case 128: return launch_t<CELL, 128>(p, s, q, info);
+    case 256: return launch_t<CELL, 256>(p, s, q, info);
+    case 768: return launch_t<CELL, 768>(p, s, q, info);
     default: return (int)cudaErrorInvalidValue;
   }
+}
+
+}  // namespace
+
+int launch_bwd_bf16(const BwdParams& p, int cell, int Dh, cudaStream_t s, bool query_only,
+                    LaunchInfo* info) {
+  if (cell == kLSTM) return launch_cell<kLSTM>(p, Dh, s, query_only, info);
+  if (cell == kGRU) return launch_cell<kGRU>(p, Dh, s, query_only, info);
+  return launch_cell<kSLSTM>(p, Dh, s, query_only, info);
 }
 
 }  // namespace srnn

@@ -141,19 +141,23 @@ const char* rnn_status_str(int status) {
 }
 
 size_t rnn_stash_size(const rnn_desc_t* d) {
-  if (check_desc(d) != RNN_OK || d->cell != RNN_LSTM) return 0;
+  if (check_desc(d) != RNN_OK) return 0;
   const size_t cells = (size_t)d->T * d->B * d->NH * d->Dh;
-  return cells * 5 * sizeof(float);  // activations (4 gates) + c_t
+  // four gate values + one state (+ the sLSTM normaliser)
+  return cells * (d->cell == RNN_SLSTM ? 6 : 5) * sizeof(float);
 }
 
 size_t rnn_workspace_size(const rnn_desc_t* d, int pass) {
   if (check_desc(d) != RNN_OK) return 0;
   if (pass == 0) return kStatusBytes;
-  // backward: status | bf16(h0) [B,NH,Dh] | bias-gradient partials [slices,NH,4Dh] fp32
+  // backward: status | bf16(h0) [B,NH,Dh] | bias-gradient partials [slices,NH,G*Dh]
+  // fp32 | GRU: recurrent-preactivation gradient bf16 [T,B,NH,3Dh]
+  const size_t G = gates_of(d->cell);
   const size_t nb = (size_t)((d->B + 7) / 8);
   size_t o = kStatusBytes;
   o += align_up((size_t)d->B * d->NH * d->Dh * 2, 256);
-  o += align_up(nb * d->NH * 4 * d->Dh * sizeof(float), 256);
+  o += align_up(nb * d->NH * G * d->Dh * sizeof(float), 256);
+  if (d->cell == RNN_GRU) o += align_up((size_t)d->T * d->B * d->NH * G * d->Dh * 2, 256);
   return o;
 }
 
@@ -188,7 +192,7 @@ int rnn_fwd(const rnn_desc_t* d, const void* Wx, const void* R, const float* bia
   if ((st = make_plan(d, &pl)) != RNN_OK) return st;
   if (workspace == nullptr || workspace_bytes < rnn_workspace_size(d, 0)) return RNN_ERR_INVALID_ARG;
   const bool train = (d->flags & RNN_FLAG_TRAIN) != 0;
-  if (train && (d->cell != RNN_LSTM || d->dtype != RNN_BF16)) return RNN_ERR_UNSUPPORTED;
+  if (train && d->dtype != RNN_BF16) return RNN_ERR_UNSUPPORTED;
   if (train && stash == nullptr) return RNN_ERR_INVALID_ARG;
   if (!aligned(workspace, 16)) return RNN_ERR_MISALIGNED;
   const size_t nstate = (size_t)d->B * d->NH * d->Dh;
@@ -225,6 +229,7 @@ int rnn_fwd(const rnn_desc_t* d, const void* Wx, const void* R, const float* bia
   if (train) {
     p.stash_gates = static_cast<float*>(stash);
     p.stash_c = p.stash_gates + (size_t)d->T * nstate * 4;
+    p.stash_n = p.stash_c + (size_t)d->T * nstate;
   }
   p.status = static_cast<int*>(workspace);
   if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return RNN_ERR_LAUNCH;
@@ -260,24 +265,28 @@ int rnn_sync_floor(const rnn_desc_t* d, int iters, void* workspace, size_t works
 }
 
 int rnn_bwd(const rnn_desc_t* d, const void* R, const float* h0, const float* c0,
-            const void* h_seq, const void* stash, const void* dh_seq, const float* dhT,
-            const float* dcT, void* dWx, float* dR, float* db, float* dh0, float* dc0,
-            void* workspace, size_t workspace_bytes, void* stream) {
+            const float* n0, const void* h_seq, const void* stash, const void* dh_seq,
+            const float* dhT, const float* dcT, const float* dnT, void* dWx, float* dR, float* db,
+            float* dh0, float* dc0, float* dn0, void* workspace, size_t workspace_bytes,
+            void* stream) {
   int st = check_desc(d);
   if (st != RNN_OK) return st;
-  if (d->cell != RNN_LSTM || d->dtype != RNN_BF16) return RNN_ERR_UNSUPPORTED;
+  if (d->dtype != RNN_BF16) return RNN_ERR_UNSUPPORTED;
   const int Dh = d->Dh;
   if (Dh != 32 && Dh != 64 && Dh != 128 && Dh != 256 && Dh != 768) return RNN_ERR_UNSUPPORTED;
   if (d->B == 0 || d->NH == 0) return RNN_OK;
   if (workspace == nullptr || workspace_bytes < rnn_workspace_size(d, 1)) return RNN_ERR_INVALID_ARG;
   if (!aligned(workspace, 256)) return RNN_ERR_MISALIGNED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int G = gates_of(d->cell);
   const size_t nstate = (size_t)d->B * d->NH * Dh;
-  const size_t nw = (size_t)d->NH * 4 * Dh;
+  const size_t nw = (size_t)d->NH * G * Dh;
+  const bool has_c = d->cell != RNN_GRU, has_n = d->cell == RNN_SLSTM;
   if (d->T == 0) {  // no steps: gradients pass straight through to the initial states
     int r;
     if ((r = copy_state(dh0, dhT, nstate, s)) != RNN_OK) return r;
-    if ((r = copy_state(dc0, dcT, nstate, s)) != RNN_OK) return r;
+    if (has_c && (r = copy_state(dc0, dcT, nstate, s)) != RNN_OK) return r;
+    if (has_n && (r = copy_state(dn0, dnT, nstate, s)) != RNN_OK) return r;
     if (dR && cudaMemsetAsync(dR, 0, nw * Dh * sizeof(float), s) != cudaSuccess) return RNN_ERR_LAUNCH;
     if (db && cudaMemsetAsync(db, 0, nw * sizeof(float), s) != cudaSuccess) return RNN_ERR_LAUNCH;
     return RNN_OK;
@@ -287,26 +296,37 @@ int rnn_bwd(const rnn_desc_t* d, const void* R, const float* h0, const float* c0
   if (!aligned(R, 16) || !aligned(h_seq, 16) || !aligned(stash, 16) || !aligned(dh_seq, 16) ||
       !aligned(dWx, 16))
     return RNN_ERR_MISALIGNED;
-  const float* fp[] = {h0, c0, dhT, dcT, dR, db, dh0, dc0};
+  const float* fp[] = {h0, c0, n0, dhT, dcT, dnT, dR, db, dh0, dc0, dn0};
   for (const float* q : fp)
     if (!aligned(q, 8)) return RNN_ERR_MISALIGNED;
 
   const int nbslices = (d->B + 7) / 8;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  void* h0b = ws + kStatusBytes;
-  float* db_part = reinterpret_cast<float*>(ws + kStatusBytes + align_up(nstate * 2, 256));
+  size_t o = kStatusBytes;
+  void* h0b = ws + o;
+  o += align_up(nstate * 2, 256);
+  float* db_part = reinterpret_cast<float*>(ws + o);
+  o += align_up((size_t)nbslices * nw * sizeof(float), 256);
+  void* drec = d->cell == RNN_GRU ? ws + o : nullptr;
 
   BwdParams p;
   std::memset(&p, 0, sizeof(p));
   p.R = R;
   p.dh_seq = dh_seq;
   p.dhT = dhT;
-  p.dcT = dcT;
+  p.dcT = has_c ? dcT : nullptr;
+  p.dnT = has_n ? dnT : nullptr;
   p.stash_gates = static_cast<const float*>(stash);
   p.stash_c = p.stash_gates + (size_t)d->T * nstate * 4;
+  p.stash_n = p.stash_c + (size_t)d->T * nstate;
+  p.h_init = h0;
+  p.c_init = has_c ? c0 : nullptr;
+  p.n_init = has_n ? n0 : nullptr;
   p.dWx = dWx;
+  p.drec = drec;
   p.dh0 = dh0;
-  p.dc0 = dc0;
+  p.dc0 = has_c ? dc0 : nullptr;
+  p.dn0 = has_n ? dn0 : nullptr;
   p.db_part = db ? db_part : nullptr;
   p.status = static_cast<int*>(workspace);
   p.T = d->T;
@@ -315,15 +335,14 @@ int rnn_bwd(const rnn_desc_t* d, const void* R, const float* h0, const float* c0
   p.nbslices = nbslices;
   p.flags = d->flags;
   p.timeout_ns = (d->flags & RNN_FLAG_TEST_TIMEOUT) ? kTestTimeoutNs : kTimeoutNs;
-  p.c_init = c0;
 
   if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return RNN_ERR_LAUNCH;
-  int e = launch_bwd_lstm_bf16(p, Dh, s, false, nullptr);
+  int e = launch_bwd_bf16(p, d->cell, Dh, s, false, nullptr);
   if (e != 0) return map_launch_error(e);
   if (dR) {
     e = launch_h0_to_bf16(h0, h0b, (int)nstate, s);
     if (e != 0) return map_launch_error(e);
-    e = launch_grad_weights(h_seq, h0b, dWx, dR, d->T, d->B, d->NH, Dh, 4, s);
+    e = launch_grad_weights(h_seq, h0b, drec ? drec : dWx, dR, d->T, d->B, d->NH, Dh, G, s);
     if (e != 0) return map_launch_error(e);
   }
   if (db) {

@@ -125,7 +125,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   }
 }
 
-// CL: the head is split over a thread-block cluster (CS > 1); TR: LSTM training stash.
+// CL: the head is split over a thread-block cluster (CS > 1); TR: training stash.
 template <int CELL, int DH, int UG, int NT, int KREG, int HS, int CL, int TR>
 __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     fwd_bf16_kernel(const FwdParams p) {
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
         }
 
         // ---- gate math and state update, one (unit, batch) cell at a time
-        float act[TR ? 4 : 1][TR ? NE : 1];  // LSTM gate activations for the stash
+        float act[TR ? 4 : 1][TR ? NE : 1];  // per-cell values the backward needs
 #pragma unroll
         for (int us = 0; us < NSLOT; ++us)
 #pragma unroll
@@ -531,13 +531,20 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 const float zg = fmaf(0.5f, t_rz.y, 0.5f);
                 const float ng = tanh_fast(fmaf(rg, r[2], wxn[ei]));
                 h = fmaf(zg, st_h[ei] - ng, ng);
+                if (TR) {
+                  act[0][TR ? ei : 0] = rg;
+                  act[1][TR ? ei : 0] = zg;
+                  act[2][TR ? ei : 0] = ng;
+                  act[3][TR ? ei : 0] = r[2];  // R_n h + b_n
+                }
               } else {
                 const float pi = r[0], pf = r[1], pz = r[2], po = r[3];
                 const float mn = fmaxf(pf + st_m[ei], pi);
                 // HS: accurate exp/tanh (the exponential gating amplifies rounding)
                 const float ig = HS ? expf(pi - mn) : __expf(pi - mn);
                 const float fg = HS ? expf(pf + st_m[ei] - mn) : __expf(pf + st_m[ei] - mn);
-                const float c = fmaf(fg, st_c[ei], ig * (HS ? tanhf(pz) : tanh_fast(pz)));
+                const float zt = HS ? tanhf(pz) : tanh_fast(pz);
+                const float c = fmaf(fg, st_c[ei], ig * zt);
                 const float nn = fmaf(fg, st_n[ei], ig);
                 st_c[ei] = c;
                 st_n[ei] = nn;
@@ -545,12 +552,21 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 // r[o] holds o~ (HS) or o~/2 (fast path)
                 const float og = HS ? 1.f / (1.f + expf(-po)) : fmaf(0.5f, tanh_fast(po), 0.5f);
                 h = og * (c / nn);
+                if (TR) {
+                  act[0][TR ? ei : 0] = ig;
+                  act[1][TR ? ei : 0] = fg;
+                  act[2][TR ? ei : 0] = zt;
+                  act[3][TR ? ei : 0] = og;
+                }
               }
               hv[ei] = h;
               st_h[ei] = h;
             }
 
-        if (TR) {  // training stash: gate activations and c_t of this step
+        // training stash of this step, per cell: four gate values [T,B,NH,4Dh] and
+        // the state the backward needs [T,B,NH,Dh] (LSTM c_t, GRU h_t, sLSTM c_t
+        // plus n_t in a third array).  GRU slots: r, z, n, R_n h + b_n.
+        if (TR) {
 #pragma unroll
           for (int us = 0; us < NSLOT; ++us)
 #pragma unroll
@@ -562,10 +578,11 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 if (n < nvalid) {
                   const int j = u0 + ub + (lane >> 2) + 8 * us;
                   const size_t row = ((size_t)t * B + b0 + n) * NH + head;
-                  float* sg = p.stash_gates + row * GD + j;
+                  float* sg = p.stash_gates + row * 4 * DH + j;
 #pragma unroll
                   for (int g = 0; g < 4; ++g) sg[g * DH] = act[TR ? g : 0][TR ? ei : 0];
-                  p.stash_c[row * DH + j] = st_c[ei];
+                  p.stash_c[row * DH + j] = CELL == kGRU ? st_h[ei] : st_c[ei];
+                  if (CELL == kSLSTM) p.stash_n[row * DH + j] = st_n[ei];
                 }
               }
         }
@@ -720,13 +737,13 @@ int launch_fwd_bf16_v(const FwdParams& p_in, cudaStream_t stream, bool query_onl
 template <int CELL, int DH, int UG, int NT, int KREG, int HS = 0>
 int launch_fwd_bf16_t(const FwdParams& p, cudaStream_t stream, bool query_only,
                       LaunchInfo* info) {
-  const bool tr = CELL == kLSTM && (p.flags & 1) && p.stash_gates != nullptr;
+  const bool tr = (p.flags & 1) && p.stash_gates != nullptr;
   if (p.CS > 1) {
-    if (tr) return launch_fwd_bf16_v<CELL, DH, UG, NT, KREG, HS, 1, CELL == kLSTM>(p, stream, query_only, info);
+    if (tr) return launch_fwd_bf16_v<CELL, DH, UG, NT, KREG, HS, 1, 1>(p, stream, query_only, info);
     return launch_fwd_bf16_v<CELL, DH, UG, NT, KREG, HS, 1, 0>(p, stream, query_only, info);
   }
   if constexpr (DH <= 128) {
-    if (tr) return launch_fwd_bf16_v<CELL, DH, UG, NT, KREG, HS, 0, CELL == kLSTM>(p, stream, query_only, info);
+    if (tr) return launch_fwd_bf16_v<CELL, DH, UG, NT, KREG, HS, 0, 1>(p, stream, query_only, info);
     return launch_fwd_bf16_v<CELL, DH, UG, NT, KREG, HS, 0, 0>(p, stream, query_only, info);
   }
   return (int)cudaErrorInvalidConfiguration;

@@ -1,12 +1,14 @@
-// Weight gradients of the head-wise LSTM after the reverse recurrence.
+// Weight gradients of the head-wise cells after the reverse recurrence.
 //
 //   dR[h] = sum_{t,b} h_{t-1}[b,h,:]^T dG_t[b,h,:]      (h_{-1} = h0)
 //   db[h] = sum_{t,b} dG_t[b,h,:]
+// with dG the gradient of the recurrent preactivation (h @ R + b): dWx for the
+// LSTM and sLSTM; for the GRU it differs from dWx on the n block (r * dn~).
 //
 // dR is one dense contraction per head over K = T*B rows: the only true GEMM
 // of the path.  Tensor cores (mma.sync bf16 -> fp32) on 128x128 output tiles,
 // K streamed in 32-row chunks through a 3-stage cp.async ring; both operands
-// are read in their natural row-major layouts (h rows of Dh, dWx rows of 4Dh)
+// are read in their natural row-major layouts (h rows of Dh, dG rows of G*Dh)
 // and transposed on the fly by ldmatrix.trans.  db is summed from the
 // per-batch-slice partials the reverse kernel leaves in the workspace.
 #include <cuda_bf16.h>
@@ -31,15 +33,15 @@ __device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, 
                : "memory");
 }
 
-// grid: (ceil(4Dh/BN), ceil(Dh/BM), NH); 256 threads = 8 warps as 2 (M) x 4 (N),
+// grid: (ceil(G*Dh/BN), ceil(Dh/BM), NH); 256 threads = 8 warps as 2 (M) x 4 (N),
 // each warp a 64 x 32 tile = 4 x 4 mma m16n8.
 __global__ void __launch_bounds__(256) dR_gemm_kernel(const __nv_bfloat16* __restrict__ h_seq,
                                                       const __nv_bfloat16* __restrict__ h0b,
                                                       const __nv_bfloat16* __restrict__ dWx,
                                                       float* __restrict__ dR, int T, int B, int NH,
-                                                      int Dh) {
+                                                      int Dh, int G) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int GD = 4 * Dh;
+  const int GD = G * Dh;
   const int head = blockIdx.z;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -155,13 +157,13 @@ __global__ void db_reduce_kernel(const float* __restrict__ part, float* __restri
 
 int launch_grad_weights(const void* h_seq, const void* h0_bf16, const void* dWx, float* dR, int T,
                         int B, int NH, int Dh, int G, cudaStream_t s) {
-  if (G != 4) return (int)cudaErrorInvalidValue;
+  if (G != 3 && G != 4) return (int)cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(dR_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return (int)e;
-  dim3 grid((4 * Dh + BN - 1) / BN, (Dh + BM - 1) / BM, NH);
+  dim3 grid((G * Dh + BN - 1) / BN, (Dh + BM - 1) / BM, NH);
   dR_gemm_kernel<<<grid, 256, SMEM, s>>>(static_cast<const __nv_bfloat16*>(h_seq),
                                          static_cast<const __nv_bfloat16*>(h0_bf16),
-                                         static_cast<const __nv_bfloat16*>(dWx), dR, T, B, NH, Dh);
+                                         static_cast<const __nv_bfloat16*>(dWx), dR, T, B, NH, Dh, G);
   return (int)cudaGetLastError();
 }
 

@@ -24,8 +24,9 @@ struct FwdParams {
   float* cT;
   float* nT;
   float* mT;
-  float* stash_gates;  // LSTM training stash: activations i,f,z,o  [T,B,NH,4Dh]
-  float* stash_c;      // and c_t                                    [T,B,NH,Dh]
+  float* stash_gates;  // training stash: four gate values per cell   [T,B,NH,4Dh]
+  float* stash_c;      // LSTM / sLSTM c_t, GRU h_t                     [T,B,NH,Dh]
+  float* stash_n;      // sLSTM n_t                                     [T,B,NH,Dh]
   int* status;
   int T, B, NH;
   int CS;        // CTAs per (head, batch slice): thread-block cluster size
@@ -57,29 +58,36 @@ inline int bf16_unit_group(int cell) { return cell == kGRU ? 16 : 8; }
 // Empty-step kernel with the launch shape of a bf16/fp32 forward.
 int launch_sync_floor(const LaunchInfo& li, int T, int* status, cudaStream_t s);
 
-// Backward (LSTM, bf16).
+// Backward through time (bf16; LSTM, GRU, sLSTM).
 struct BwdParams {
   const void* R;
   const void* dh_seq;
   const float* dhT;
-  const float* dcT;
+  const float* dcT;    // LSTM / sLSTM
+  const float* dnT;    // sLSTM
   const float* stash_gates;
   const float* stash_c;
+  const float* stash_n;
+  const float* h_init;  // h0 fp32 [B,NH,Dh] (GRU: h_{-1}); NULL = zeros
+  const float* c_init;  // c0 fp32 (NULL = zeros), c_{-1} for the first step
+  const float* n_init;  // sLSTM n0 (NULL = zeros)
   void* dWx;
+  void* drec;           // GRU: recurrent-preactivation gradient, bf16 [T,B,NH,3Dh] (workspace)
   float* dh0;
   float* dc0;
-  float* db_part;  // [nbslices, NH, 4Dh] per-slice bias-gradient partials (workspace)
+  float* dn0;
+  float* db_part;  // [nbslices, NH, G*Dh] per-slice bias-gradient partials (workspace)
   int* status;
   int T, B, NH;
   int CS, U, nbslices, flags;
   unsigned long long timeout_ns;
-  const float* c_init;  // c0 fp32 [B,NH,Dh] (NULL = zeros), c_{-1} for the first step
 };
-int launch_bwd_lstm_bf16(const BwdParams& p, int Dh, cudaStream_t s, bool query_only,
-                         LaunchInfo* info);
+int launch_bwd_bf16(const BwdParams& p, int cell, int Dh, cudaStream_t s, bool query_only,
+                    LaunchInfo* info);
 
-// dR = sum_t h_{t-1}^T dWx_t (bf16 operands, fp32 result) and db from partials.
-int launch_grad_weights(const void* h_seq, const void* h0_bf16, const void* dWx, float* dR,
+// dR = sum_t h_{t-1}^T dG_t (bf16 operands, fp32 result) and db from partials.
+// dG: [T,B,NH,G*Dh] bf16 (dWx for LSTM / sLSTM, the recurrent gradient for GRU).
+int launch_grad_weights(const void* h_seq, const void* h0_bf16, const void* dG, float* dR,
                         int T, int B, int NH, int Dh, int G, cudaStream_t s);
 int launch_h0_to_bf16(const float* h0, void* out, int n, cudaStream_t s);
 int launch_db_reduce(const float* part, float* db, int nslices, int n, cudaStream_t s);

@@ -57,7 +57,10 @@ def test_sizes(lib):
     assert lib.rnn_workspace_size(ctypes.byref(d), 0) >= 256
     assert lib.rnn_workspace_size(ctypes.byref(d), 1) >= 256 + 3 * 2 * 64 * 2
     assert lib.rnn_stash_size(ctypes.byref(d)) == 10 * 3 * 2 * 64 * 5 * 4
-    assert lib.rnn_stash_size(ctypes.byref(_desc(cell=1))) == 0
+    assert lib.rnn_stash_size(ctypes.byref(_desc(cell=1, T=10, B=3, NH=2))) == 10 * 3 * 2 * 64 * 5 * 4
+    assert lib.rnn_stash_size(ctypes.byref(_desc(cell=2, T=10, B=3, NH=2))) == 10 * 3 * 2 * 64 * 6 * 4
+    gru = _desc(cell=1, T=10, B=3, NH=2, Dh=64)
+    assert lib.rnn_workspace_size(ctypes.byref(gru), 1) >= 10 * 3 * 2 * 192 * 2
     assert lib.rnn_workspace_size(ctypes.byref(_desc(T=-1)), 0) == 0
     assert lib.rnn_workspace_size(None, 0) == 0
 
@@ -88,8 +91,29 @@ def test_misaligned_pointers(lib):
 
 def test_train_flag_rules(lib):
     assert _fwd(lib, _desc(flags=1)) == 1                      # no stash
-    assert _fwd(lib, _desc(cell=1, flags=1), stash=0x5000) == 2  # no GRU backward
-    assert _fwd(lib, _desc(dtype=0, flags=1), stash=0x5000) == 2
+    assert _fwd(lib, _desc(cell=1, flags=1)) == 1
+    assert _fwd(lib, _desc(dtype=0, flags=1), stash=0x5000) == 2  # training is bf16 only
+
+
+def _bwd(lib, desc, ws=0x1000, ws_bytes=1 << 30, **ptr):
+    P = ctypes.c_void_p
+    names = ["R", "h0", "c0", "n0", "h_seq", "stash", "dh_seq", "dhT", "dcT", "dnT", "dWx", "dR",
+             "db", "dh0", "dc0", "dn0"]
+    base = dict(R=0x3000, h_seq=0x4000, stash=0x5000, dh_seq=0x6000, dWx=0x7000)
+    base.update(ptr)
+    args = [P(base[n]) if base.get(n) else None for n in names]
+    return lib.rnn_bwd(ctypes.byref(desc), *args, P(ws) if ws else None, ws_bytes, None)
+
+
+def test_backward_argument_checks(lib):
+    assert _bwd(lib, _desc(dtype=0)) == 2                  # bf16 only
+    assert _bwd(lib, _desc(Dh=48)) == 2
+    assert _bwd(lib, _desc(), ws=0) == 1
+    assert _bwd(lib, _desc(), ws_bytes=16) == 1
+    assert _bwd(lib, _desc(), ws=0x1010) == 3               # workspace 256-aligned
+    assert _bwd(lib, _desc(), stash=0) == 1
+    assert _bwd(lib, _desc(cell=2), dWx=0x7008) == 3
+    assert _bwd(lib, _desc(B=0)) == 0
 
 
 def test_empty_batch_is_noop(lib):

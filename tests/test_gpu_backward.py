@@ -1,9 +1,9 @@
-"""GPU parity of the LSTM backward (BPTT) against the fp64 oracle (needs a GB300).
+"""GPU parity of the backward (BPTT) against the fp64 oracle (needs a GB300).
 
-A training forward (stash of gate activations and cell states) followed by
-rnn_bwd through the C ABI; every gradient is compared with the oracle's
-textbook BPTT on the same seeded inputs, normwise:
-    max |d| / max |oracle|  <=  5e-2     for dWx, dR, db, dh0, dc0,
+A training forward (stash of gate values and states) followed by rnn_bwd
+through the C ABI, for the LSTM, GRU and sLSTM; every gradient is compared with
+the oracle's textbook BPTT on the same seeded inputs, normwise:
+    max |d| / max |oracle|  <=  5e-2     for dWx, dR, db, dh0 (dc0, dn0),
 and h_seq of the training forward as in the forward tests (<= 2e-2).
 Identities between the GPU's own outputs are checked tighter: dR equals
 sum_t h_{t-1}^T dWx_t recomputed from the GPU's h_seq and dWx, db equals the
@@ -30,13 +30,16 @@ def S():
     return S
 
 
-def run_fb(S, d):
+def run_fb(S, d, cell="lstm"):
     dt = torch.bfloat16
     g = {k: torch.from_numpy(np.ascontiguousarray(d[k])).to("cuda", dt) for k in ("Wx", "R", "dh")}
-    for k in ("b", "h0", "c0", "dhT", "dcT"):
+    for k in ("b", "h0", "c0", "n0", "m0", "dhT", "dcT"):
         g[k] = torch.from_numpy(np.ascontiguousarray(d[k])).to("cuda", torch.float32)
-    fw = S.forward("lstm", g["Wx"], g["R"], g["b"], g["h0"], g["c0"], train=True)
-    gr = S.backward(fw, g["R"], g["h0"], g["c0"], g["dh"], g["dhT"], g["dcT"])
+    sl = cell == "slstm"
+    fw = S.forward(cell, g["Wx"], g["R"], g["b"], g["h0"], g["c0"], g["n0"] if sl else None,
+                   g["m0"] if sl else None, train=True)
+    gr = S.backward(fw, g["R"], g["h0"], g["c0"], g["dh"], g["dhT"], g["dcT"],
+                    n0=g["n0"] if sl else None)
     torch.cuda.synchronize()
     return g, fw, gr
 
@@ -47,14 +50,19 @@ def normwise(got, ref):
     return np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30)
 
 
-def check(S, d, label):
-    g, fw, gr = run_fb(S, d)
-    ref_f = O.lstm_forward(d["Wx"], d["R"], d["b"], d["h0"], d["c0"])
-    ref = O.lstm_backward(d["Wx"], d["R"], d["b"], d["h0"], d["c0"], dh_seq=d["dh"],
-                          dhT=d["dhT"], dcT=d["dcT"])
+def check(S, d, label, cell="lstm"):
+    g, fw, gr = run_fb(S, d, cell)
+    ref_f = O.forward(cell, d["Wx"], d["R"], d["b"], d["h0"], d["c0"], d["n0"], d["m0"])
+    if cell == "slstm":
+        ref = O.slstm_backward(d["Wx"], d["R"], d["b"], d["h0"], d["c0"], d["n0"], d["m0"],
+                               dh_seq=d["dh"], dhT=d["dhT"], dcT=d["dcT"])
+    else:
+        ref = O.backward(cell, d["Wx"], d["R"], d["b"], d["h0"], d["c0"], dh_seq=d["dh"],
+                         dhT=d["dhT"], dcT=d["dcT"])
     herr = np.abs(fw["h_seq"].float().cpu().numpy() - ref_f["h_seq"]).max()
     assert herr <= H_TOL, (label, "h_seq", herr)
-    errs = {k: normwise(gr[k], ref[k]) for k in ("dWx", "dR", "db", "dh0", "dc0")}
+    keys = ["dWx", "dR", "db", "dh0"] + [k for k in ("dc0", "dn0") if k in gr]
+    errs = {k: normwise(gr[k], ref[k]) for k in keys}
     for k, e in errs.items():
         assert e <= GRAD_TOL, (label, k, e, errs)
     return g, fw, gr
@@ -89,6 +97,39 @@ def test_backward_small_sweep(S, Dh, B, NH, T):
     d["dhT"] = rng.standard_normal(d["h0"].shape).astype(np.float32)
     d["dcT"] = rng.standard_normal(d["h0"].shape).astype(np.float32)
     check(S, d, f"Dh{Dh}/B{B}/NH{NH}/T{T}")
+
+
+CELL_CASES = [
+    # cell, Dh, B, NH, T
+    ("gru", 32, 3, 2, 17), ("gru", 64, 13, 2, 9), ("gru", 128, 9, 1, 12), ("gru", 256, 5, 2, 10),
+    ("gru", 768, 4, 1, 6), ("gru", 64, 1, 1, 1),
+    ("slstm", 32, 3, 2, 17), ("slstm", 64, 13, 2, 9), ("slstm", 128, 9, 1, 12),
+    ("slstm", 256, 5, 2, 10), ("slstm", 768, 4, 1, 5), ("slstm", 64, 1, 1, 1),
+]
+
+
+@pytest.mark.parametrize("cell,Dh,B,NH,T", CELL_CASES)
+def test_backward_gru_slstm(S, cell, Dh, B, NH, T):
+    d = make_inputs(cell, "bf16", T, B, NH, Dh, seed=Dh + 3 * T, bias="normal0.1",
+                    states="random", backward=True)
+    rng = np.random.default_rng(Dh + B + 1)
+    d["dhT"] = rng.standard_normal(d["h0"].shape).astype(np.float32)
+    d["dcT"] = (rng.standard_normal(d["h0"].shape).astype(np.float32) if cell == "slstm"
+                else np.zeros(d["h0"].shape, np.float32))
+    check(S, d, f"{cell}/Dh{Dh}/B{B}/NH{NH}/T{T}", cell)
+
+
+def test_backward_gru_recurrent_gradient_identity(S):
+    """GRU: dR uses r*dn~ on the n block, not dWx; db equals the sum of that gradient."""
+    d = make_inputs("gru", "bf16", 7, 5, 2, 64, seed=4, bias="normal0.1", states="random",
+                    backward=True)
+    g, fw, gr = run_fb(S, d, "gru")
+    ref = O.gru_backward(d["Wx"], d["R"], d["b"], d["h0"], dh_seq=d["dh"])
+    # the n block of dWx and of db differ by the factor r: db is not sum(dWx) there
+    dwx_sum = gr["dWx"].float().sum(dim=(0, 1)).cpu().numpy()
+    n_blk = slice(128, 192)
+    assert np.abs(dwx_sum[:, n_blk] - ref["db"][:, n_blk]).max() > 1e-3
+    assert normwise(gr["db"], ref["db"]) <= GRAD_TOL
 
 
 def test_backward_zero_length(S):
