@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
     if (s > 0) {
       if (CL) {
         const int ps = s - 1;
-        if (!dead && !bwait<true>(bar_r + 8 * (ps & 1), (ps >> 1) & 1, abort_flag, p.status, tlim))
+        if (!dead && !bwait<false>(bar_r + 8 * (ps & 1), (ps >> 1) & 1, abort_flag, p.status, tlim))
           dead = true;
         if (!dead) {
           if (tid == 0 && ps + 2 <= T - 1) mbar_arrive_expect_tx(bar_r + 8 * (ps & 1), kTx);

@@ -52,7 +52,7 @@ __global__ void floor_cluster_kernel(int T, int CS, int NW, unsigned long long t
         const uint32_t par = ((t - 1) >> 1) & 1;
         const uint64_t t0 = globaltimer_ns();
         bool ok = true;
-        while (!mbar_try_wait_cluster(bar, par)) {
+        while (!mbar_try_wait(bar, par)) {
           if (globaltimer_ns() - t0 > tlim) {
             atomicOr(status, kStatusTimeout);
             ok = false;

@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     for (int t = 0; t < T; ++t) {
       // ---- wait for h_{t-1} (cluster)
       if (!dead && CL && t > 0) {
-        if (!wait_phase<true>(bar_h + 8 * (t & 1), ((t - 1) >> 1) & 1, abort_flag, p.status, tlim))
+        if (!wait_phase<false>(bar_h + 8 * (t & 1), ((t - 1) >> 1) & 1, abort_flag, p.status, tlim))
           dead = true;
         else if (tid == 0 && t + 1 <= T - 2)
           mbar_arrive_expect_tx(bar_h + 8 * (t & 1), htx);  // for h_{t+1}
