@@ -14,7 +14,8 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (CELLS, DTYPES, RNN_BF16, RNN_F32, RNN_FLAG_TEST_TIMEOUT, RNN_FLAG_TRAIN,
+from ._lib import (CELLS, DTYPES, RNN_BF16, RNN_F32, RNN_FLAG_H_BF16, RNN_FLAG_TEST_TIMEOUT,
+                   RNN_FLAG_TRAIN,
                    STATUS, rnn_desc_t)
 
 __all__ = ["RnnError", "make_desc", "rnn_workspace_size", "rnn_stash_size", "rnn_fwd", "rnn_bwd",
@@ -127,11 +128,16 @@ def _dtype_name(t: torch.Tensor) -> str:
 
 
 def forward(cell: str, Wx, R, bias=None, h0=None, c0=None, n0=None, m0=None, *, train=False,
-            cluster=0, test_timeout=False, stream=None, check=True):
-    """Allocate outputs and run rnn_fwd.  Wx [T,B,NH,G*Dh], R [NH,Dh,G*Dh]."""
+            cluster=0, h_bf16=False, test_timeout=False, stream=None, check=True):
+    """Allocate outputs and run rnn_fwd.  Wx [T,B,NH,G*Dh], R [NH,Dh,G*Dh].
+
+    ``h_bf16`` sets RNN_FLAG_H_BF16 (sLSTM: h_{t-1} enters the contraction as
+    one bf16 value instead of a hi + lo pair).
+    """
     T, B, NH, _ = Wx.shape
     Dh = R.shape[1]
-    flags = (RNN_FLAG_TRAIN if train else 0) | (RNN_FLAG_TEST_TIMEOUT if test_timeout else 0)
+    flags = ((RNN_FLAG_TRAIN if train else 0) | (RNN_FLAG_TEST_TIMEOUT if test_timeout else 0)
+             | (RNN_FLAG_H_BF16 if h_bf16 else 0))
     desc = make_desc(cell, _dtype_name(Wx), T, B, NH, Dh, flags, cluster)
     dev = Wx.device
     f32 = dict(dtype=torch.float32, device=dev)

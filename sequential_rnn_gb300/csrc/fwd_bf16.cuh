@@ -24,9 +24,10 @@
 // LSTM/GRU gate activations of two cells share one packed fp16x2 tanh.
 //
 // Exchange of h_t: CS == 1 -> shared memory + one named barrier per step.
-// CS > 1 -> every thread st.async's its bf16 pair of h_t into every cluster
-// CTA's buffer, completing bytes on that CTA's mbarrier; a CTA proceeds to step
-// t+1 when all Dh*NB*2 bytes have landed.  Receiving all of h_t from a peer also
+// CS > 1 -> each warp stages its bf16 slice of h_t in shared memory, then its
+// lanes send the slice's 16-byte chunks with st.async into every cluster CTA's
+// buffer (lane -> one chunk, several ranks), completing bytes on that CTA's
+// mbarrier; a CTA proceeds to step t+1 when all Dh*NB*2 bytes have landed.  Receiving all of h_t from a peer also
 // proves the peer finished reading the buffer being overwritten next, so one
 // double buffer suffices without a cluster barrier in the loop.
 //
@@ -62,6 +63,10 @@ struct FwdCfg {
   // long k chains run as two interleaved accumulator sets
   static constexpr bool SPLITK = KS >= 8 || HS;
   static_assert(KS >= 2, "two k16 steps at least");
+  // cluster exchange: one warp's h_t slice (all parts) as 16-byte chunks
+  static constexpr int STG_CH = HPARTS * NB * UG / 8;
+  static constexpr int STG_BYTES = STG_CH * 16;
+  static_assert(32 % STG_CH == 0, "staging chunks must tile a warp");
   // register estimate per compute thread -> largest CTA the register file holds
   static constexpr int REG_EST = MT * KREG * 4 + MT * NT * 8 + 88 + HS * NT * 8;
   static constexpr int MAXT_R = (65536 / REG_EST) / 32 * 32;
@@ -84,7 +89,7 @@ struct FwdCfg {
 };
 
 struct FwdSmem {
-  uint32_t h, wx, rf, bar, flag, total;
+  uint32_t h, wx, rf, stg, bar, flag, total;
 };
 
 template <class C>
@@ -100,6 +105,8 @@ __host__ __device__ inline FwdSmem fwd_smem_layout(int U, int NS) {
   L.rf = o;
   o += (uint32_t)NW * C::MT * C::KSM * 512;
   o = (o + 15) & ~15u;
+  L.stg = o;  // per warp: h_t staging for the cluster exchange, two parities
+  o += (uint32_t)NW * C::STG_BYTES * 2;
   L.bar = o;
   o += (uint32_t)(2 * NS + 3) * 8;
   L.flag = o;
@@ -347,22 +354,24 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     __nv_bfloat16* hseq_ch = static_cast<__nv_bfloat16*>(p.h_seq) +
                              ((size_t)(ch_store ? b0 + ch_n : b0) * NH + head) * DH + u0 + ub + 8 * ch_k;
     const size_t hseq_tstride = (size_t)B * NH * DH;
-    // cluster: bf16 pairs (unit 2k, 2k+1) of one batch row, one per (slot, n-tile)
-    const bool ueven = ((lane >> 2) & 1) == 0;
-    uint32_t h_off[NSLOT][NT];
-    __nv_bfloat16* hseq_p[NSLOT][NT];
-    bool h_ok[NSLOT][NT];
+    // cluster exchange: this warp's staging area [parity][part][row n][UG units];
+    // lane -> chunk x_c = lane % STG_CH (part x_p, row x_n, 8 units at x_k), sent
+    // to ranks lane / STG_CH, + 32 / STG_CH, ...
+    constexpr int STG_CH = C::STG_CH, RSTEP = 32 / STG_CH;
+    const uint32_t stg_warp = sbase + L.stg + (uint32_t)warp * C::STG_BYTES * 2;
+    uint32_t stg_cell[NSLOT][NT];  // this thread's cells (e = 0) in the staging area
 #pragma unroll
     for (int us = 0; us < NSLOT; ++us)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int n = nt * 8 + 2 * (lane & 3) + (ueven ? 0 : 1);
-        const int j = u0 + ub + (lane >> 2) + 8 * us - (ueven ? 0 : 1);
-        h_off[us][nt] = (uint32_t)n * HPB + (uint32_t)j * 2;
-        h_ok[us][nt] = n < nvalid;
-        hseq_p[us][nt] = static_cast<__nv_bfloat16*>(p.h_seq) +
-                         ((size_t)(h_ok[us][nt] ? b0 + n : b0) * NH + head) * DH + j;
-      }
+      for (int nt = 0; nt < NT; ++nt)
+        stg_cell[us][nt] = (uint32_t)(nt * 8 + 2 * (lane & 3)) * (UG * 2) +
+                           (uint32_t)((lane >> 2) + 8 * us) * 2;
+    const int x_c = lane % STG_CH, x_r0 = lane / STG_CH;
+    const int x_p = x_c / (NB * UG / 8), x_n = (x_c / (UG / 8)) % NB, x_k = x_c % (UG / 8);
+    const uint32_t x_dst = (uint32_t)x_p * hpart + (uint32_t)x_n * HPB + (uint32_t)(u0 + ub + 8 * x_k) * 2;
+    const bool x_store = x_r0 == 0 && x_p == 0 && x_n < nvalid;  // h_seq chunk owner
+    __nv_bfloat16* hseq_x = static_cast<__nv_bfloat16*>(p.h_seq) +
+                            ((size_t)(x_store ? b0 + x_n : b0) * NH + head) * DH + u0 + ub + 8 * x_k;
     bool dead = false;
     if (p.flags & (1 << 30)) {  // test hook: a barrier nothing ever completes
       if (!wait_phase<false>(bar_dummy, 0, abort_flag, p.status, tlim)) dead = true;
@@ -591,32 +600,41 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
         const uint32_t nbuf = s_h + (uint32_t)((t + 1) & 1) * NB * HPB;
         const bool send = t + 1 < T;
         if (CL) {
-          // bf16 pairs (unit 2k, 2k+1) of one batch row straight from registers into
-          // every cluster CTA's buffer, this one included
-          const uint32_t lbar = bar_h + 8 * ((t + 1) & 1);
+          // stage this warp's cells, then ship 16-byte chunks to every cluster CTA
+          // (this one included) and store the h_seq chunk
+          const uint32_t stg = stg_warp + (uint32_t)(t & 1) * C::STG_BYTES;
 #pragma unroll
           for (int us = 0; us < NSLOT; ++us)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              const int e0 = (us * NT + nt) * 2;
-              const float mine = ueven ? hv[e0 + 1] : hv[e0];
-              const float other = __shfl_xor_sync(0xffffffffu, mine, 4);
-              const float v_ev = ueven ? hv[e0] : other, v_od = ueven ? other : hv[e0 + 1];
-              const uint32_t pk = pack_bf16x2(v_ev, v_od);
-              if (send) {
-                const uint32_t laddr = nbuf + h_off[us][nt];
-                // residual pair (HS): h - bf16(h), rounded to bf16
-                const uint32_t pkl =
-                    HS ? pack_bf16x2(v_ev - bf16_round(v_ev), v_od - bf16_round(v_od)) : 0u;
-                for (int rk = 0; rk < CS; ++rk) {
-                  const uint32_t rbar = mapa(lbar, rk);
-                  st_async_b32(mapa(laddr, rk), pk, rbar);
-                  if (HS) st_async_b32(mapa(laddr + hpart, rk), pkl, rbar);
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float hvv = hv[(us * NT + nt) * 2 + e];
+                const __nv_bfloat16 hi = __float2bfloat16_rn(hvv);
+                const uint32_t addr = stg + stg_cell[us][nt] + e * (UG * 2);
+                asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr),
+                             "h"(*reinterpret_cast<const uint16_t*>(&hi))
+                             : "memory");
+                if (HS) {  // residual part: bf16(h - bf16(h))
+                  const __nv_bfloat16 lo = __float2bfloat16_rn(hvv - __bfloat162float(hi));
+                  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr + NB * UG * 2),
+                               "h"(*reinterpret_cast<const uint16_t*>(&lo))
+                               : "memory");
                 }
               }
-              if (h_ok[us][nt]) *reinterpret_cast<uint32_t*>(hseq_p[us][nt]) = pk;
-              hseq_p[us][nt] += hseq_tstride;
-            }
+          __syncwarp();
+          uint32_t v[4];
+          lds128(v, stg + (uint32_t)x_c * 16);
+          if (send) {
+            const uint32_t lbar = bar_h + 8 * ((t + 1) & 1);
+            const uint32_t ldst = nbuf + x_dst;
+            for (int rk = x_r0; rk < CS; rk += RSTEP) st_async_v4(mapa(ldst, rk), v, mapa(lbar, rk));
+          }
+          if (x_store)
+            asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(hseq_x), "r"(v[0]), "r"(v[1]),
+                         "r"(v[2]), "r"(v[3])
+                         : "memory");
+          hseq_x += hseq_tstride;
         } else {
           // own cells into the next buffer (also at the last step: h_seq is stored
           // from there after the barrier)
