@@ -120,12 +120,28 @@ int rnn_fwd(const rnn_desc_t* desc, const void* Wx, const void* R, const float* 
  * gradient (the output does not depend on it).  dh_seq: input dtype.  Alignment:
  * R, h_seq, dh_seq, dWx, stash 16 bytes; fp32 pointers 8 bytes; workspace 256.
  * The reverse recurrence runs as one thread-block cluster per head slice (as the
- * forward), then the dR contraction and the db reduction. */
+ * forward), then the dR contraction (tcgen05 tensor cores) and the db reduction. */
 int rnn_bwd(const rnn_desc_t* desc, const void* R, const float* h0, const float* c0,
             const float* n0, const void* h_seq, const void* stash, const void* dh_seq,
             const float* dhT, const float* dcT, const float* dnT, void* dWx, float* dR, float* db,
             float* dh0, float* dc0, float* dn0, void* workspace, size_t workspace_bytes,
             void* stream);
+
+/* Input projection, the dense step in front of the recurrence (FlashRNN blog
+ * page, register-caching paragraph: only the recurrent weight R has to stay on
+ * chip through the sequential time loop; the input weight is applied to all
+ * steps at once):
+ *   Wx[m, n] = sum_k x[m, k] * W[n, k] + bias[n]
+ * x [M, K] bf16 (M = T*B rows of the input sequence), W [N, K] bf16 (rows are
+ * output features, as in a linear layer's weight), bias [N] fp32 (NULL = none),
+ * Wx [M, N] bf16 (fp32 sum rounded to nearest even once).  With N = NH*G*Dh,
+ * Wx is rnn_fwd's input.  fp32 accumulation on the tensor cores (tcgen05, TMA).
+ * Requires K % 8 == 0, N % 16 == 0, M <= 8388480.  Alignment: x, W, Wx 16 bytes,
+ * bias 4 bytes, workspace 256 bytes and >= 256 bytes (status word at offset 0).
+ * M == 0 is a no-op.  Returns rnn_status_t. */
+int rnn_input_proj(int32_t M, int32_t N, int32_t K, const void* x, const void* W,
+                   const float* bias, void* Wx, void* workspace, size_t workspace_bytes,
+                   void* stream);
 
 /* Synchronises `stream`, reads the device status word of `workspace` into
  * *device_status (RNN_OK or RNN_ERR_TIMEOUT).  Returns RNN_OK if the read

@@ -35,6 +35,12 @@ Backward passes are textbook backpropagation through time of exactly these
 forward graphs (the sLSTM stabiliser m is a reparametrisation the output does
 not depend on, so it carries no gradient).
 
+The input projection that produces Wx from an input sequence x (the dense
+step in front of the recurrence; the blog page's register-caching paragraph
+separates the recurrent weight, kept on chip through the time loop, from the
+input weight applied to all steps at once) is the plain definition
+``Wx = x @ W^T + b``.
+
 Everything is fp64 numpy; a library batched matmul is the only "primitive".
 Optionally ``emulate_bf16_h`` rounds h_{t-1} to bf16 before the contraction,
 mirroring a bf16 MMA operand; it is a diagnosis aid, parity is judged against
@@ -45,7 +51,8 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = ["GATES", "forward", "backward", "lstm_forward", "gru_forward",
-           "slstm_forward", "lstm_backward", "gru_backward", "slstm_backward"]
+           "slstm_forward", "lstm_backward", "gru_backward", "slstm_backward",
+           "input_projection"]
 
 GATES = {"lstm": 4, "gru": 3, "slstm": 4}
 
@@ -301,3 +308,19 @@ def backward(cell, Wx, R, b=None, h0=None, c0=None, n0=None, m0=None, dh_seq=Non
     if cell == "slstm":
         return slstm_backward(Wx, R, b, h0, c0, n0, m0, dh_seq, dhT, dcT)
     raise ValueError(cell)
+
+
+# --------------------------------------------------------- input projection --
+def input_projection(x, W, b=None):
+    """Wx[m, n] = sum_k x[m, k] W[n, k] + b[n] in fp64.
+
+    x [M, K], W [N, K] (rows are output features, a linear layer's weight),
+    b [N] or None.  With N = NH*G*Dh and M = T*B the result, reshaped to
+    [T, B, NH, G*Dh], is the recurrence's Wx.
+    """
+    x = np.asarray(x, np.float64)
+    W = np.asarray(W, np.float64)
+    out = x @ W.T
+    if b is not None:
+        out = out + np.asarray(b, np.float64)[None, :]
+    return out

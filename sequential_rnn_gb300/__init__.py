@@ -20,8 +20,7 @@ from ._lib import (CELLS, DTYPES, RNN_BF16, RNN_F32, RNN_FLAG_H_BF16, RNN_FLAG_T
 
 __all__ = ["RnnError", "make_desc", "rnn_workspace_size", "rnn_stash_size", "rnn_fwd", "rnn_bwd",
            "rnn_read_status", "rnn_sync_floor", "rnn_fwd_config", "rnn_status_str", "rnn_fwd_noalloc",
-           "forward",
-           "backward", "GATES"]
+           "rnn_input_proj", "forward", "backward", "input_proj", "GATES"]
 
 GATES = {"lstm": 4, "gru": 3, "slstm": 4}
 
@@ -102,6 +101,12 @@ def rnn_bwd(desc, R, h0, c0, n0, h_seq, stash, dh_seq, dhT, dcT, dnT, dWx, dR, d
         ctypes.byref(desc), _ptr(R), _ptr(h0), _ptr(c0), _ptr(n0), _ptr(h_seq), _ptr(stash),
         _ptr(dh_seq), _ptr(dhT), _ptr(dcT), _ptr(dnT), _ptr(dWx), _ptr(dR), _ptr(db), _ptr(dh0),
         _ptr(dc0), _ptr(dn0), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def rnn_input_proj(M: int, N: int, K: int, x, W, bias, Wx, workspace, stream=None) -> int:
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return int(_lib.load().rnn_input_proj(int(M), int(N), int(K), _ptr(x), _ptr(W), _ptr(bias),
+                                          _ptr(Wx), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def rnn_read_status(workspace, stream=None) -> int:
@@ -189,3 +194,25 @@ def backward(fwd: dict, R, h0, c0, dh_seq, dhT=None, dcT=None, *, n0=None, dnT=N
             raise RnnError(dst, "rnn_bwd (device)")
     g["workspace"] = ws
     return g
+
+
+def input_proj(x, W, bias=None, *, stream=None, check=True):
+    """Wx = x W^T + bias through rnn_input_proj.
+
+    x [..., K] bf16, W [N, K] bf16, bias [N] fp32 or None -> [..., N] bf16.
+    With x [T, B, d] and W [NH*G*Dh, d] the result, viewed as [T, B, NH, G*Dh],
+    is forward()'s Wx.
+    """
+    K = x.shape[-1]
+    N = W.shape[0]
+    M = x.numel() // K if K else 0
+    out = torch.empty(tuple(x.shape[:-1]) + (N,), dtype=torch.bfloat16, device=x.device)
+    ws = torch.zeros(256, dtype=torch.uint8, device=x.device)
+    st = rnn_input_proj(M, N, K, x, W, bias, out, ws, stream)
+    if st:
+        raise RnnError(st, "rnn_input_proj")
+    if check:
+        dst = rnn_read_status(ws, stream)
+        if dst:
+            raise RnnError(dst, "rnn_input_proj (device)")
+    return out

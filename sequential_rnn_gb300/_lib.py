@@ -25,7 +25,8 @@ DTYPES = {"f32": RNN_F32, "bf16": RNN_BF16}
 
 # Every symbol include/rnn.h declares (checked by the CPU tests).
 EXPORTS = ("rnn_workspace_size", "rnn_stash_size", "rnn_fwd", "rnn_bwd", "rnn_read_status",
-           "rnn_sync_floor", "rnn_fwd_config", "rnn_status_str", "rnn_fwd_noalloc")
+           "rnn_sync_floor", "rnn_fwd_config", "rnn_status_str", "rnn_fwd_noalloc",
+           "rnn_input_proj")
 
 
 class rnn_desc_t(ctypes.Structure):
@@ -49,6 +50,7 @@ _SIGS = {
     "rnn_fwd_config": (_I, [_DESC, ctypes.POINTER(ctypes.c_int32)]),
     "rnn_status_str": (ctypes.c_char_p, [_I]),
     "rnn_fwd_noalloc": (_I, [_DESC] + [_P] * 14),
+    "rnn_input_proj": (_I, [ctypes.c_int32] * 3 + [_P] * 5 + [_SZ, _P]),
 }
 
 _lib = None

@@ -14,7 +14,7 @@
 //         dc' <- dc*f, dn' <- dn*f   (the stabiliser m carries no gradient)
 //   all   dh_rec[t-1] = dG_t @ R[h]^T;  dh0 = dh_rec[-1] (+ GRU direct term)
 // dWx_t is written in the input dtype; db sums dG; dR = sum_t h_{t-1}^T dG_t is
-// a GEMM afterwards (grad_weights.cu).
+// a GEMM afterwards (tc_gemm.cu).
 //
 // Layout on sm_103a: the CTAs of one thread-block cluster own disjoint hidden
 // units of a head (U = Dh / CS each), as in the forward.  Per step a CTA forms

@@ -236,6 +236,23 @@ int rnn_fwd(const rnn_desc_t* d, const void* Wx, const void* R, const float* bia
   return map_launch_error(launch_forward(d, pl, p, s, false, nullptr));
 }
 
+int rnn_input_proj(int32_t M, int32_t N, int32_t K, const void* x, const void* W,
+                   const float* bias, void* Wx, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  if (M < 0 || N <= 0 || K <= 0) return RNN_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < kStatusBytes) return RNN_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return RNN_ERR_MISALIGNED;
+  if (K % 8 != 0 || N % 16 != 0 || M > 65535 * 128) return RNN_ERR_UNSUPPORTED;
+  if (M == 0) return RNN_OK;
+  if (x == nullptr || W == nullptr || Wx == nullptr) return RNN_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(W, 16) || !aligned(Wx, 16) || !aligned(bias, 4))
+    return RNN_ERR_MISALIGNED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return RNN_ERR_LAUNCH;
+  return map_launch_error(launch_input_proj_tc(x, W, bias, Wx, M, N, K,
+                                               static_cast<int*>(workspace), kTimeoutNs, s));
+}
+
 int rnn_read_status(const void* workspace, void* stream, int* device_status) {
   if (workspace == nullptr || device_status == nullptr) return RNN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -342,7 +359,8 @@ int rnn_bwd(const rnn_desc_t* d, const void* R, const float* h0, const float* c0
   if (dR) {
     e = launch_h0_to_bf16(h0, h0b, (int)nstate, s);
     if (e != 0) return map_launch_error(e);
-    e = launch_grad_weights(h_seq, h0b, drec ? drec : dWx, dR, d->T, d->B, d->NH, Dh, G, s);
+    e = launch_dR_tc(h_seq, h0b, drec ? drec : dWx, dR, d->T, d->B, d->NH, Dh, G, p.status,
+                     p.timeout_ns, s);
     if (e != 0) return map_launch_error(e);
   }
   if (db) {

@@ -143,6 +143,10 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   // fp32 tanh.  One CTA per head is throughput-bound: packed fp16x2 tanh.
   constexpr bool SPLITK = C::SPLITK || CL;
   constexpr bool PACKED_TANH = !CL;
+  // One CTA per head (all warps meet at a barrier every step): the next step's
+  // Wx is primed while this step's MMAs are in flight, in a second accumulator
+  // set.  A cluster step primes it while h_t travels to the peers instead.
+  constexpr bool EARLY_PREP = !CL && DH <= 128;
   extern __shared__ __align__(128) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -382,8 +386,12 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     // accumulators of the step about to run, primed with scale*(Wx + bias)
     float acc[MT][NT][4], acc2[SPLITK ? MT : 1][NT][4];
     float wxn[NE];  // GRU: Wx_n stays outside r*(R_n h + b_n)
+    float accp[MT][NT][4], wxnp[NE];  // EARLY_PREP: primed for the next step
+    float(*A)[NT][4] = EARLY_PREP ? accp : acc;
+    float* WXN = EARLY_PREP ? wxnp : wxn;
     // Wait for the next Wx stage, move it into accumulator layout and release
-    // the stage.  Runs before the step barrier, off the recurrence's critical path.
+    // the stage.  Runs while the step's MMAs are in flight (EARLY_PREP) or
+    // after h_t is published, off the recurrence's critical path.
     auto prep = [&]() -> bool {
       if (!wait_phase<false>(bar_full + 8 * s, ph, abort_flag, p.status, tlim)) return false;
       const uint32_t stage = s_wx + s * stage_bytes;
@@ -424,20 +432,12 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
               const int mt = UG == 16 ? g : g / 2;
               const int q = UG == 16 ? us * 2 + e : (g % 2) * 2 + e;
               if (CELL == kGRU && g == 2) {
-                acc[mt][nt][q] = sbias[g][us];
-                wxn[(us * NT + nt) * 2 + e] = x;
+                A[mt][nt][q] = sbias[g][us];
+                WXN[(us * NT + nt) * 2 + e] = x;
               } else {
-                acc[mt][nt][q] = fmaf(C::gate_scale(g), x, sbias[g][us]);
+                A[mt][nt][q] = fmaf(C::gate_scale(g), x, sbias[g][us]);
               }
             }
-      if (SPLITK) {
-#pragma unroll
-        for (int mt = 0; mt < (SPLITK ? MT : 1); ++mt)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc2[mt][nt][q] = 0.f;
-      }
       return true;
     };
     if (!dead && T > 0 && !prep()) dead = true;
@@ -452,7 +452,28 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
           mbar_arrive_expect_tx(bar_h + 8 * (t & 1), htx);  // for h_{t+1}
       }
 
+      const bool send = t + 1 < T;
       if (!dead) {
+        if (EARLY_PREP) {
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) acc[mt][nt][q] = accp[mt][nt][q];
+          if (CELL == kGRU) {
+#pragma unroll
+            for (int ei = 0; ei < NE; ++ei) wxn[ei] = wxnp[ei];
+          }
+        }
+        if (SPLITK) {
+#pragma unroll
+          for (int mt = 0; mt < (SPLITK ? MT : 1); ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) acc2[mt][nt][q] = 0.f;
+        }
         // ---- acc += R^T h_{t-1}
         const uint32_t hb = s_h + (uint32_t)(t & 1) * NB * HPB + lm_off;
 #pragma unroll
@@ -492,6 +513,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
             }
           }
         }
+        // next step's Wx while the MMAs run
+        if (EARLY_PREP && send && !prep()) dead = true;
         if (SPLITK) {
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
@@ -598,7 +621,6 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 
         // ---- publish h_t
         const uint32_t nbuf = s_h + (uint32_t)((t + 1) & 1) * NB * HPB;
-        const bool send = t + 1 < T;
         if (CL) {
           // stage this warp's cells, then ship 16-byte chunks to every cluster CTA
           // (this one included) and store the h_seq chunk
@@ -659,7 +681,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
               }
         }
         // ---- prime the next step's accumulators while other warps finish
-        if (send && !prep()) dead = true;
+        if (!EARLY_PREP && send && !prep()) dead = true;
       }
       if (!CL) {
         // h_t visible to every compute warp; a dead warp stops all of them together

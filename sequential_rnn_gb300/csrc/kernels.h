@@ -85,11 +85,16 @@ struct BwdParams {
 int launch_bwd_bf16(const BwdParams& p, int cell, int Dh, cudaStream_t s, bool query_only,
                     LaunchInfo* info);
 
-// dR = sum_t h_{t-1}^T dG_t (bf16 operands, fp32 result) and db from partials.
-// dG: [T,B,NH,G*Dh] bf16 (dWx for LSTM / sLSTM, the recurrent gradient for GRU).
-int launch_grad_weights(const void* h_seq, const void* h0_bf16, const void* dG, float* dR,
-                        int T, int B, int NH, int Dh, int G, cudaStream_t s);
+// Weight-gradient helpers (grad_weights.cu): h0 -> bf16, db from per-slice partials.
 int launch_h0_to_bf16(const float* h0, void* out, int n, cudaStream_t s);
+// tcgen05 GEMMs (tc_gemm.cu).  dR[h] = sum_{t,b} h_{t-1}^T dG_t (fp32, overwritten),
+// h_{-1} = h0b, dG [T,B,NH,G*Dh] bf16 (dWx for LSTM / sLSTM, the recurrent gradient
+// for GRU); Wx = x W^T + bias (bf16).  status: device status word.
+int launch_dR_tc(const void* h_seq, const void* h0b, const void* dG, float* dR, int T, int B,
+                 int NH, int Dh, int G, int* status, unsigned long long timeout_ns,
+                 cudaStream_t s);
+int launch_input_proj_tc(const void* x, const void* W, const float* bias, void* Wx, int M, int N,
+                         int K, int* status, unsigned long long timeout_ns, cudaStream_t s);
 int launch_db_reduce(const float* part, float* db, int nslices, int n, cudaStream_t s);
 
 }  // namespace srnn

@@ -21,12 +21,12 @@ import numpy as np
 
 __all__ = [
     "TENSOR_IDS", "GATES", "WORKLOADS", "round_bf16", "bf16_bits",
-    "make_inputs", "workload_inputs",
+    "make_inputs", "workload_inputs", "make_projection_inputs",
 ]
 
 # One independent stream per tensor role.
 TENSOR_IDS = {"Wx": 1, "R": 2, "b": 3, "dh": 4, "h0": 5, "c0": 6, "n0": 7,
-              "m0": 8, "dhT": 9, "dcT": 10}
+              "m0": 8, "dhT": 9, "dcT": 10, "x": 11, "W": 12, "bW": 13}
 
 # Gates per cell.  Gate-major packing: column g*Dh + j of a G*Dh row is gate g
 # of hidden unit j.  LSTM / sLSTM order (i, f, z, o); GRU order (r, z, n).
@@ -133,3 +133,16 @@ def workload_inputs(name: str, *, seed: int = 0, **overrides) -> dict:
     w.update(overrides)
     return make_inputs(w["cell"], w["dtype"], w["T"], w["B"], w["NH"], w["Dh"], seed=seed,
                        bias=w["bias"], backward=w["backward"], states=w.get("states", "zero"))
+
+
+def make_projection_inputs(M: int, N: int, K: int, *, seed: int = 0) -> dict:
+    """Inputs of the input projection Wx = x W^T + b, rounded to bf16 (x, W).
+
+    x [M, K] ~ N(0, 1) (M = T*B rows of an input sequence), W [N, K] ~
+    N(0, 1/K) (so each output has unit variance, like the recurrence's Wx),
+    b [N] ~ N(0, 0.1^2) in fp32.
+    """
+    x = round_bf16(_rng(seed, "x").standard_normal((M, K)).astype(np.float32))
+    W = round_bf16((_rng(seed, "W").standard_normal((N, K)) / np.sqrt(max(K, 1))).astype(np.float32))
+    b = (0.1 * _rng(seed, "bW").standard_normal(N)).astype(np.float32)
+    return {"x": x, "W": W, "b": b}

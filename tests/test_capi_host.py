@@ -119,3 +119,30 @@ def test_backward_argument_checks(lib):
 def test_empty_batch_is_noop(lib):
     assert _fwd(lib, _desc(B=0)) == 0
     assert _fwd(lib, _desc(NH=0)) == 0
+
+
+def _proj(lib, M=300, N=3072, K=768, x=0x1000, W=0x2000, bias=0, Wx=0x3000, ws=0x8000,
+          ws_bytes=256):
+    P = ctypes.c_void_p
+    return lib.rnn_input_proj(M, N, K, P(x) if x else None, P(W) if W else None,
+                              P(bias) if bias else None, P(Wx) if Wx else None,
+                              P(ws) if ws else None, ws_bytes, None)
+
+
+def test_input_proj_argument_checks(lib):
+    assert _proj(lib, M=-1) == 1
+    assert _proj(lib, N=0) == 1
+    assert _proj(lib, K=0) == 1
+    assert _proj(lib, ws=0) == 1
+    assert _proj(lib, ws_bytes=128) == 1
+    assert _proj(lib, ws=0x8010) == 3                       # workspace 256-aligned
+    assert _proj(lib, K=12) == 2                            # K % 8
+    assert _proj(lib, N=200) == 2                           # N % 16
+    assert _proj(lib, M=65535 * 128 + 1) == 2
+    assert _proj(lib, x=0) == 1
+    assert _proj(lib, Wx=0) == 1
+    assert _proj(lib, x=0x1008) == 3
+    assert _proj(lib, W=0x2004) == 3
+    assert _proj(lib, Wx=0x3002) == 3
+    assert _proj(lib, bias=0x4002) == 3
+    assert _proj(lib, M=0, x=0, Wx=0) == 0                  # empty input: no-op

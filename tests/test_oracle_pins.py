@@ -292,3 +292,57 @@ def test_backward_finite_differences(cell):
             fd = (lp - lm) / (2 * eps)
             an = g[gname][idx]
             assert abs(fd - an) <= 1e-7 * max(1.0, abs(an)), (src, idx, fd, an)
+
+
+# ------------------------------------------------------ input projection ----
+def test_input_projection_closed_forms():
+    """Rank-1 inputs give K*a_m*c_n + b_n; a permutation W selects input columns."""
+    rng = np.random.default_rng(5)
+    M, N, K = 7, 12, 9
+    a, c, b = rng.standard_normal(M), rng.standard_normal(N), rng.standard_normal(N)
+    x = np.repeat(a[:, None], K, axis=1)
+    W = np.repeat(c[:, None], K, axis=1)
+    np.testing.assert_allclose(O.input_projection(x, W, b), K * np.outer(a, c) + b[None, :],
+                               rtol=1e-12, atol=1e-12)
+    # W[n, k] = 1 where k = sel[n]: output column n is input column sel[n] (+ b[n])
+    x = rng.standard_normal((M, K))
+    sel = rng.integers(0, K, N)
+    W = np.zeros((N, K))
+    W[np.arange(N), sel] = 1.0
+    np.testing.assert_array_equal(O.input_projection(x, W, b), x[:, sel] + b[None, :])
+    np.testing.assert_array_equal(O.input_projection(x, W), x[:, sel])
+
+
+def test_input_projection_matches_torch_linear():
+    rng = np.random.default_rng(6)
+    x, W, b = rng.standard_normal((11, 24)), rng.standard_normal((40, 24)), rng.standard_normal(40)
+    ref = torch.nn.functional.linear(torch.from_numpy(x), torch.from_numpy(W),
+                                     torch.from_numpy(b)).numpy()
+    np.testing.assert_allclose(O.input_projection(x, W, b), ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("cell", ["lstm", "gru"])
+def test_projection_then_recurrence_matches_torch_rnn(cell):
+    """torch.nn.LSTM / GRU with a real input weight == input_projection + the cell.
+
+    PyTorch applies W_ih x + b_ih inside the cell; the head-wise path takes it
+    as a precomputed Wx (gate order i,f,g,o / r,z,n is the gate-major order).
+    """
+    rng = np.random.default_rng(7)
+    T, B, Din, Dh = 6, 3, 10, 5
+    G = O.GATES[cell]
+    mod = (torch.nn.LSTM if cell == "lstm" else torch.nn.GRU)(Din, Dh, dtype=torch.float64)
+    x = rng.standard_normal((T, B, Din))
+    h0 = rng.standard_normal((B, Dh)) * 0.5
+    c0 = rng.standard_normal((B, Dh)) * 0.5
+    with torch.no_grad():
+        args = (torch.from_numpy(h0)[None], torch.from_numpy(c0)[None]) if cell == "lstm" \
+            else torch.from_numpy(h0)[None]
+        out = mod(torch.from_numpy(x), args)[0].numpy()
+    W_ih = mod.weight_ih_l0.detach().numpy()
+    b_ih = mod.bias_ih_l0.detach().numpy()
+    Wx = O.input_projection(x.reshape(T * B, Din), W_ih, b_ih).reshape(T, B, 1, G * Dh)
+    R = mod.weight_hh_l0.detach().numpy().T[None]
+    b_hh = mod.bias_hh_l0.detach().numpy()[None]
+    ref = O.forward(cell, Wx, R, b_hh, h0[:, None], c0[:, None])
+    np.testing.assert_allclose(ref["h_seq"][:, :, 0], out, rtol=1e-10, atol=1e-12)
