@@ -3,14 +3,20 @@
 //   dR[h] = sum_{t,b} h_{t-1}[b,h,:]^T dG_t[b,h,:]          (weight gradient)
 //   Wx    = x W^T + b                                       (input projection)
 //
-// One 128 x 128 fp32 output tile per CTA, accumulated in tensor memory by
-// tcgen05.mma (M=128, N=128, K=16 per instruction) from 128-byte-swizzled
-// shared-memory tiles that TMA loads through a 6-stage ring:
+// Persistent kernel, one CTA per SM, looping over work units (head z, 128-row
+// tile, BN-column tile, K split).  A unit's fp32 128 x BN tile accumulates in
+// tensor memory by tcgen05.mma (M=128, N=BN, K=16 per instruction) from
+// 128-byte-swizzled shared-memory tiles that TMA loads through a ring:
 //   warp 0   TMA producer (one lane) and TMEM owner (alloc / dealloc),
 //   warp 1   MMA issuer (one lane): 4 MMAs per 64-deep k block, then a
 //            tcgen05.commit that frees the ring stage once they completed,
+//            and one per unit that hands the accumulator to the epilogue,
 //   warps 2-5 epilogue: tcgen05.ld of their 32-lane TMEM quarter (one output
-//            row per thread), then fp32 or bf16(+bias) stores.
+//            row per thread), then fp32 (stored, or added for K splits) or
+//            bf16(+bias) stores.
+// The accumulator is double-buffered in TMEM (2 x BN columns), so a unit's
+// epilogue overlaps the next unit's MMAs, and the ring keeps streaming
+// across units.
 // Operands may be K-major (rows of K) or MN-major (rows of M / N, as both
 // operands of dR are: K = (t, b) is the row index of h_seq and of dG).
 // The K range is one or two segments, each with its own tensor maps and row
@@ -33,18 +39,24 @@
 namespace srnn {
 namespace {
 
-constexpr int TBM = 128, TBN = 128, TBK = 64, TSTG = 6;
-constexpr uint32_t TILE_A = TBM * TBK * 2;  // 16 KB
-constexpr uint32_t TILE_B = TBN * TBK * 2;  // 16 KB
-constexpr uint32_t STAGE_BYTES = TILE_A + TILE_B;
-constexpr uint32_t TMEM_COLS = 128;
-// ring + 1024 for aligning it + barriers (full, empty, accumulator) and the TMEM slot
-constexpr uint32_t SMEM_BYTES = TSTG * STAGE_BYTES + 1024 + (2 * TSTG + 2) * 8 + 16;
+constexpr int TBM = 128, TBK = 64;
 
-enum : int { kOutF32 = 0, kOutBf16Bias = 1 };
+template <int BN>
+struct TcCfg {
+  static constexpr uint32_t TILE_A = TBM * TBK * 2;        // 16 KB
+  static constexpr uint32_t TILE_B = BN * TBK * 2;         // 16 or 32 KB
+  static constexpr uint32_t STAGE = TILE_A + TILE_B;
+  static constexpr int NSTG = BN == 256 ? 4 : 6;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;            // two accumulator buffers
+  // ring + 1024 for aligning it + barriers (full, empty, tfull x2, tempty x2) + TMEM slot
+  static constexpr uint32_t SMEM = NSTG * STAGE + 1024 + (2 * NSTG + 4) * 8 + 16;
+};
+
+enum : int { kOutF32 = 0, kOutBf16Bias = 1, kOutF32Add = 2 };
 
 struct GemmArgs {
   int M, N;                // valid output rows / columns per batch item z
+  int Z, tiles_m, tiles_n, ksplit;
   int m_off_z, n_off_z;    // A's M and B's N coordinate offset per z (head)
   int nkb0, nkb1;          // 64-deep k blocks in segment 0 and 1
   int ka0[2], kb0[2];      // K coordinate offsets of A and B per segment
@@ -55,6 +67,26 @@ struct GemmArgs {
   int* status;
   unsigned long long timeout_ns;
 };
+
+struct Unit {
+  int z, m_base, n_base, kb_lo, kb_hi;
+};
+
+__device__ __forceinline__ Unit unit_of(const GemmArgs& g, int u) {
+  Unit w;
+  const int ks = u % g.ksplit;
+  int r = u / g.ksplit;
+  const int nt = r % g.tiles_n;
+  r /= g.tiles_n;
+  const int mt = r % g.tiles_m;
+  w.z = r / g.tiles_m;
+  w.m_base = mt * TBM;
+  w.n_base = nt;  // scaled by BN by the caller
+  const int nkb = g.nkb0 + g.nkb1;
+  w.kb_lo = (int)((long long)nkb * ks / g.ksplit);
+  w.kb_hi = (int)((long long)nkb * (ks + 1) / g.ksplit);
+  return w;
+}
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                              int* status, unsigned long long limit_ns) {
@@ -71,37 +103,42 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
   }
 }
 
-template <bool A_MN, bool B_MN, int OUT>
+template <bool A_MN, bool B_MN, int OUT, int BN>
 __global__ void __launch_bounds__(192, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mB0,
                    const __grid_constant__ CUtensorMap mA1, const __grid_constant__ CUtensorMap mB1,
                    const GemmArgs g) {
+  using C = TcCfg<BN>;
+  constexpr int NSTG = C::NSTG;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ int abort_flag_s;
-  __shared__ int consumed_s, issued_s;
+  __shared__ int issued_s, consumed_s;
   volatile int* abort_flag = &abort_flag_s;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t ring = (raw + 1023u) & ~1023u;  // 128-byte swizzle: 1024-byte aligned tiles
-  const uint32_t bar_full = ring + TSTG * STAGE_BYTES, bar_empty = bar_full + 8 * TSTG;
-  const uint32_t bar_acc = bar_empty + 8 * TSTG, tslot = bar_acc + 8;
+  const uint32_t bar_full = ring + NSTG * C::STAGE, bar_empty = bar_full + 8 * NSTG;
+  const uint32_t bar_tfull = bar_empty + 8 * NSTG, bar_tempty = bar_tfull + 16;
+  const uint32_t tslot = bar_tempty + 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int z = blockIdx.z, m_base = blockIdx.y * TBM, n_base = blockIdx.x * TBN;
-  const int nkb = g.nkb0 + g.nkb1;
+  const int nunits = g.Z * g.tiles_m * g.tiles_n * g.ksplit;
 
   if (threadIdx.x == 32) {
-    for (int s = 0; s < TSTG; ++s) {
+    for (int s = 0; s < NSTG; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    mbar_init(bar_acc, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_tfull + 8 * a, 1);
+      mbar_init(bar_tempty + 8 * a, 4);  // one arrival per epilogue warp
+    }
     abort_flag_s = 0;
-    consumed_s = 0;
     issued_s = 0;
+    consumed_s = 0;
     fence_mbar_init();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 0) {
-    tmem_alloc(tslot, TMEM_COLS);
+    tmem_alloc(tslot, C::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -120,102 +157,149 @@ __global__ void __launch_bounds__(192, 1)
         tma_prefetch_map(&mA1);
         tma_prefetch_map(&mB1);
       }
-      const int mA = m_base + z * g.m_off_z, nB = n_base + z * g.n_off_z;
-      int kb = 0;
-      for (; kb < nkb; ++kb) {
-        const int s = kb % TSTG, u = kb / TSTG;
-        if (kb >= TSTG && !wait_bounded(bar_empty + 8 * s, (u - 1) & 1, abort_flag, g.status, tlim))
-          break;
-        const int seg = kb < g.nkb0 ? 0 : 1;
-        const int kk = (seg ? kb - g.nkb0 : kb) * TBK;
-        const CUtensorMap* ma = seg ? &mA1 : &mA0;
-        const CUtensorMap* mb = seg ? &mB1 : &mB0;
-        const uint32_t sA = ring + s * STAGE_BYTES, sB = sA + TILE_A, fb = bar_full + 8 * s;
-        mbar_arrive_expect_tx(fb, STAGE_BYTES);
-        const int ka = (seg ? g.ka0[1] : g.ka0[0]) + kk, kbq = (seg ? g.kb0[1] : g.kb0[0]) + kk;
-        if (A_MN) {  // two 64(M) x 64(K) boxes
-          tma_load_2d(sA, ma, mA, ka, fb);
-          tma_load_2d(sA + TILE_A / 2, ma, mA + 64, ka, fb);
-        } else {  // one 64(K) x 128(M) box
-          tma_load_2d(sA, ma, ka, mA, fb);
-        }
-        if (B_MN) {
-          tma_load_2d(sB, mb, nB, kbq, fb);
-          tma_load_2d(sB + TILE_B / 2, mb, nB + 64, kbq, fb);
-        } else {
-          tma_load_2d(sB, mb, kbq, nB, fb);
+      int it = 0;  // ring position across all units
+      bool stop = false;
+      for (int u = blockIdx.x; u < nunits && !stop; u += gridDim.x) {
+        const Unit w = unit_of(g, u);
+        const int mA = w.m_base + w.z * g.m_off_z, nB = w.n_base * BN + w.z * g.n_off_z;
+        for (int kb = w.kb_lo; kb < w.kb_hi; ++kb, ++it) {
+          const int s = it % NSTG, ph = it / NSTG;
+          if (it >= NSTG &&
+              !wait_bounded(bar_empty + 8 * s, (ph - 1) & 1, abort_flag, g.status, tlim)) {
+            stop = true;
+            break;
+          }
+          const int seg = kb < g.nkb0 ? 0 : 1;
+          const int kk = (seg ? kb - g.nkb0 : kb) * TBK;
+          const CUtensorMap* ma = seg ? &mA1 : &mA0;
+          const CUtensorMap* mb = seg ? &mB1 : &mB0;
+          const uint32_t sA = ring + s * C::STAGE, sB = sA + C::TILE_A, fb = bar_full + 8 * s;
+          mbar_arrive_expect_tx(fb, C::STAGE);
+          const int ka = (seg ? g.ka0[1] : g.ka0[0]) + kk;
+          const int kq = (seg ? g.kb0[1] : g.kb0[0]) + kk;
+          if (A_MN) {  // 64(M) x 64(K) boxes
+            tma_load_2d(sA, ma, mA, ka, fb);
+            tma_load_2d(sA + 8192, ma, mA + 64, ka, fb);
+          } else {  // one 64(K) x 128(M) box
+            tma_load_2d(sA, ma, ka, mA, fb);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sB + j * 8192, mb, nB + 64 * j, kq, fb);
+          } else {  // one 64(K) x BN box
+            tma_load_2d(sB, mb, kq, nB, fb);
+          }
         }
       }
-      issued_s = kb;
+      issued_s = it;
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(TBM, TBN, A_MN, B_MN);
-      int kb = 0;
-      for (; kb < nkb; ++kb) {
-        const int s = kb % TSTG, u = kb / TSTG;
-        if (!wait_bounded(bar_full + 8 * s, u & 1, abort_flag, g.status, tlim)) break;
+      constexpr uint32_t idesc = idesc_bf16_f32(TBM, BN, A_MN, B_MN);
+      int it = 0, i = 0;
+      bool stop = false;
+      for (int u = blockIdx.x; u < nunits && !stop; u += gridDim.x, ++i) {
+        const Unit w = unit_of(g, u);
+        const int a = i & 1;
+        // the epilogue has drained this accumulator buffer (unit i - 2)
+        if (i >= 2 &&
+            !wait_bounded(bar_tempty + 8 * a, ((i >> 1) - 1) & 1, abort_flag, g.status, tlim))
+          break;
         tc_fence_after();
-        const uint32_t sA = ring + s * STAGE_BYTES, sB = sA + TILE_A;
+        const uint32_t dacc = tmem + (uint32_t)(a * BN);
+        for (int kb = w.kb_lo; kb < w.kb_hi; ++kb, ++it) {
+          const int s = it % NSTG, ph = it / NSTG;
+          if (!wait_bounded(bar_full + 8 * s, ph & 1, abort_flag, g.status, tlim)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = ring + s * C::STAGE, sB = sA + C::TILE_A;
 #pragma unroll
-        for (int k4 = 0; k4 < TBK / 16; ++k4) {
-          // K step of 16: 32 bytes along a K-major row, 16 rows (2048 B) of an MN-major tile
-          const uint64_t ad = A_MN ? sdesc_sw128(sA + k4 * 2048, TILE_A / 2, 1024)
-                                   : sdesc_sw128(sA + k4 * 32, 16, 1024);
-          const uint64_t bd = B_MN ? sdesc_sw128(sB + k4 * 2048, TILE_B / 2, 1024)
-                                   : sdesc_sw128(sB + k4 * 32, 16, 1024);
-          umma_bf16(tmem, ad, bd, idesc, (kb | k4) != 0);
+          for (int k4 = 0; k4 < TBK / 16; ++k4) {
+            // K step of 16: 32 bytes along a K-major row, 16 rows (2048 B) of an MN-major tile
+            const uint64_t ad = A_MN ? sdesc_sw128(sA + k4 * 2048, 8192, 1024)
+                                     : sdesc_sw128(sA + k4 * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(sB + k4 * 2048, 8192, 1024)
+                                     : sdesc_sw128(sB + k4 * 32, 16, 1024);
+            umma_bf16(dacc, ad, bd, idesc, (kb != w.kb_lo || k4 != 0) ? 1u : 0u);
+          }
+          umma_commit(bar_empty + 8 * s);  // stage reusable once these MMAs are done
         }
-        umma_commit(bar_empty + 8 * s);  // stage reusable once these MMAs are done
+        umma_commit(bar_tfull + 8 * a);  // this unit's MMAs complete -> epilogue
       }
-      consumed_s = kb;
-      umma_commit(bar_acc);  // every issued MMA complete -> accumulator ready
+      consumed_s = it;
     }
   } else {
     // ---------------------------------------------------------- epilogue --
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const bool ok = wait_bounded(bar_acc, 0, abort_flag, g.status, tlim);
-    tc_fence_after();
-    const int row = m_base + q * 32 + lane;
-    const bool row_ok = ok && !*abort_flag && row < g.M;
+    int i = 0;
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++i) {
+      const Unit w = unit_of(g, u);
+      const int a = i & 1;
+      if (!wait_bounded(bar_tfull + 8 * a, (i >> 1) & 1, abort_flag, g.status, tlim)) break;
+      tc_fence_after();
+      const int row = w.m_base + q * 32 + lane;
+      const bool row_ok = row < g.M;
+      const bool empty_k = w.kb_hi == w.kb_lo;
+      const int n_base = w.n_base * BN;
+      float* cf = static_cast<float*>(g.C) + w.z * g.c_stride_z + (size_t)row * g.ldc;
+      __nv_bfloat16* cb = static_cast<__nv_bfloat16*>(g.C) + w.z * g.c_stride_z + (size_t)row * g.ldc;
 #pragma unroll 1
-    for (int c = 0; c < TBN / 16; ++c) {
-      uint32_t r[16];
-      tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 16), r);
-      tmem_wait_ld();
-      const int n0 = n_base + c * 16;
-      if (!row_ok || n0 >= g.N) continue;
-      if (nkb == 0) {
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];  // columns n_base + 32c .. + 31 of this thread's row
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN + c * 32), r);
+        tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) r[j] = 0u;
-      }
-      if (OUT == kOutF32) {
-        float* dst = static_cast<float*>(g.C) + z * g.c_stride_z + (size_t)row * g.ldc + n0;
+        for (int h = 0; h < 2; ++h) {
+          const int n0 = n_base + c * 32 + h * 16;
+          if (!row_ok || n0 >= g.N) continue;
+          uint32_t* v = r + 16 * h;
+          if (empty_k) {  // no k blocks: the sum is zero
+            if constexpr (OUT == kOutF32Add) {
+              continue;
+            } else {
 #pragma unroll
-        for (int j = 0; j < 16; j += 4)
-          asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(dst + j), "r"(r[j]),
-                       "r"(r[j + 1]), "r"(r[j + 2]), "r"(r[j + 3])
-                       : "memory");
-      } else {
-        __nv_bfloat16* dst =
-            static_cast<__nv_bfloat16*>(g.C) + z * g.c_stride_z + (size_t)row * g.ldc + n0;
-        uint32_t pk[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float a = __uint_as_float(r[2 * j]), b = __uint_as_float(r[2 * j + 1]);
-          if (g.bias) {
-            a += g.bias[n0 + 2 * j];
-            b += g.bias[n0 + 2 * j + 1];
+              for (int j = 0; j < 16; ++j) v[j] = 0u;
+            }
           }
-          pk[j] = pack_bf16x2(a, b);
-        }
+          if (OUT == kOutF32) {
 #pragma unroll
-        for (int j = 0; j < 8; j += 4)
-          asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(dst + 2 * j), "r"(pk[j]),
-                       "r"(pk[j + 1]), "r"(pk[j + 2]), "r"(pk[j + 3])
-                       : "memory");
+            for (int j = 0; j < 16; j += 4)
+              asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(cf + n0 + j), "r"(v[j]),
+                           "r"(v[j + 1]), "r"(v[j + 2]), "r"(v[j + 3])
+                           : "memory");
+          } else if (OUT == kOutF32Add) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+              asm volatile("red.global.add.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(cf + n0 + j),
+                           "f"(__uint_as_float(v[j])), "f"(__uint_as_float(v[j + 1])),
+                           "f"(__uint_as_float(v[j + 2])), "f"(__uint_as_float(v[j + 3]))
+                           : "memory");
+          } else {
+            uint32_t pk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float x0 = __uint_as_float(v[2 * j]), x1 = __uint_as_float(v[2 * j + 1]);
+              if (g.bias) {
+                x0 += __ldg(g.bias + n0 + 2 * j);
+                x1 += __ldg(g.bias + n0 + 2 * j + 1);
+              }
+              pk[j] = pack_bf16x2(x0, x1);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; j += 4)
+              asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(cb + n0 + 2 * j),
+                           "r"(pk[j]), "r"(pk[j + 1]), "r"(pk[j + 2]), "r"(pk[j + 3])
+                           : "memory");
+          }
+        }
       }
+      // accumulator buffer a may be overwritten by unit i + 2
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tempty + 8 * a);
     }
   }
 
@@ -224,15 +308,15 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0) {
     if (lane == 0 && *abort_flag) {
       // let TMA copies that were issued but never consumed land before exit
-      for (int kb = consumed_s; kb < issued_s; ++kb) {
+      for (int k = consumed_s; k < issued_s; ++k) {
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar_full + 8 * (kb % TSTG), (kb / TSTG) & 1))
+        while (!mbar_try_wait(bar_full + 8 * (k % NSTG), (k / NSTG) & 1))
           if (globaltimer_ns() - t0 > 10000000ull) break;
       }
     }
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
@@ -270,14 +354,28 @@ int make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint
   return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
 }
 
-template <bool A_MN, bool B_MN, int OUT>
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+// grid: one CTA per SM (at most one per unit)
+template <bool A_MN, bool B_MN, int OUT, int BN>
 int launch_tc(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1,
-              const CUtensorMap& b1, const GemmArgs& g, int Z, cudaStream_t s) {
-  auto kern = tc_gemm_kernel<A_MN, B_MN, OUT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+              const CUtensorMap& b1, GemmArgs g, cudaStream_t s) {
+  using C = TcCfg<BN>;
+  auto kern = tc_gemm_kernel<A_MN, B_MN, OUT, BN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return (int)e;
-  const dim3 grid((g.N + TBN - 1) / TBN, (g.M + TBM - 1) / TBM, Z);
-  kern<<<grid, 192, SMEM_BYTES, s>>>(a0, b0, a1, b1, g);
+  g.tiles_m = (g.M + TBM - 1) / TBM;
+  g.tiles_n = (g.N + BN - 1) / BN;
+  const long long units = (long long)g.Z * g.tiles_m * g.tiles_n * g.ksplit;
+  if (units > 0x7fffffffLL) return (int)cudaErrorInvalidValue;
+  const int grid = (int)(units < num_sms() ? units : num_sms());
+  if (grid == 0) return 0;
+  kern<<<grid, 192, C::SMEM, s>>>(a0, b0, a1, b1, g);
   return (int)cudaGetLastError();
 }
 
@@ -300,6 +398,7 @@ int launch_dR_tc(const void* h_seq, const void* h0b, const void* dG, float* dR, 
   GemmArgs g{};
   g.M = Dh;
   g.N = GD;
+  g.Z = NH;
   g.m_off_z = Dh;
   g.n_off_z = GD;
   g.nkb0 = (B + TBK - 1) / TBK;
@@ -314,19 +413,31 @@ int launch_dR_tc(const void* h_seq, const void* h0b, const void* dG, float* dR, 
   g.bias = nullptr;
   g.status = status;
   g.timeout_ns = timeout_ns;
-  return launch_tc<true, true, kOutF32>(a0, b0, a1, b0, g, NH, s);
+  // split K (= T*B rows) until the tiles cover the SMs, keeping >= 16 k blocks per split
+  const int tiles = NH * ((Dh + TBM - 1) / TBM) * ((GD + 255) / 256);
+  const int nkb = g.nkb0 + g.nkb1;
+  int ks = num_sms() / (tiles > 0 ? tiles : 1);
+  if (ks > nkb / 16) ks = nkb / 16;
+  g.ksplit = ks > 1 ? ks : 1;
+  if (g.ksplit == 1) return launch_tc<true, true, kOutF32, 256>(a0, b0, a1, b0, g, s);
+  if (cudaMemsetAsync(dR, 0, (size_t)NH * Dh * GD * sizeof(float), s) != cudaSuccess)
+    return (int)cudaErrorInvalidValue;
+  return launch_tc<true, true, kOutF32Add, 256>(a0, b0, a1, b0, g, s);
 }
 
 int launch_input_proj_tc(const void* x, const void* W, const float* bias, void* Wx, int M, int N,
                          int K, int* status, unsigned long long timeout_ns, cudaStream_t s) {
+  const bool wide = N >= 256;
   CUtensorMap a0, b0;
   int e = make_map(&a0, x, (uint64_t)M, (uint64_t)K, (uint64_t)K, 64, 128);
   if (e) return e;
-  e = make_map(&b0, W, (uint64_t)N, (uint64_t)K, (uint64_t)K, 64, 128);
+  e = make_map(&b0, W, (uint64_t)N, (uint64_t)K, (uint64_t)K, 64, wide ? 256 : 128);
   if (e) return e;
   GemmArgs g{};
   g.M = M;
   g.N = N;
+  g.Z = 1;
+  g.ksplit = 1;
   g.nkb0 = (K + TBK - 1) / TBK;
   g.nkb1 = 0;
   g.C = Wx;
@@ -335,7 +446,8 @@ int launch_input_proj_tc(const void* x, const void* W, const float* bias, void* 
   g.bias = bias;
   g.status = status;
   g.timeout_ns = timeout_ns;
-  return launch_tc<false, false, kOutBf16Bias>(a0, b0, a0, b0, g, 1, s);
+  if (wide) return launch_tc<false, false, kOutBf16Bias, 256>(a0, b0, a0, b0, g, s);
+  return launch_tc<false, false, kOutBf16Bias, 128>(a0, b0, a0, b0, g, s);
 }
 
 }  // namespace srnn
