@@ -107,7 +107,6 @@ FwdParams base_params(const rnn_desc_t* d, const Plan& pl) {
   p.NH = d->NH;
   p.CS = pl.CS;
   p.U = pl.U;
-  p.NS = 2;
   p.nbslices = pl.nbslices;
   p.flags = d->flags;
   p.timeout_ns = (d->flags & RNN_FLAG_TEST_TIMEOUT) ? kTestTimeoutNs : kTimeoutNs;

@@ -80,7 +80,7 @@ int launch_sync_floor(const LaunchInfo& li, int T, int* status, cudaStream_t s) 
     floor_cta_kernel<<<li.grid, li.threads, 0, s>>>(T, 2);
     return (int)cudaGetLastError();
   }
-  const int NW = li.threads / 32 - 1;
+  const int NW = li.threads / 32;  // bf16 forward: compute warps only
   if (li.cluster <= 1) {
     floor_named_kernel<<<li.grid, li.threads, 0, s>>>(T, NW);
     return (int)cudaGetLastError();

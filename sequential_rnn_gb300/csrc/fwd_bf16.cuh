@@ -13,11 +13,13 @@
 // with R^T as the mma.sync A operand (fragments resident in registers; for
 // very large heads the k-steps >= KREG sit in shared memory in fragment order)
 // and h_{t-1} (bf16) as the B operand read by ldmatrix from a double buffer.
-// A producer warp streams Wx_t with 16-byte cp.async (all 32 lanes, each
-// lane's completion counted on the stage's mbarrier) into a ring of NS stages
-// (full/empty mbarriers); each thread picks up its Wx values with one
-// transposing ldmatrix, which lands them exactly in accumulator layout, and
-// the accumulators start from Wx + bias.  Gate math runs on the accumulator
+// Each compute warp streams its own Wx columns (G gates x UG units x 8 batch
+// rows: one 16-byte cp.async per lane and step for UG = 8) PD steps ahead into
+// a ring of PD stages, one cp.async group per step, so a step only waits on
+// its own warp's copies (cp.async.wait_group) and no producer warp competes
+// for an SM sub-partition's issue slots.  Each thread picks up its Wx values
+// with one transposing ldmatrix, which lands them exactly in accumulator
+// layout, and the accumulators start from Wx + bias.  Gate math runs on the accumulator
 // registers; each thread owns whole (unit, batch) cells, so no gate exchange
 // is needed.  Sigmoid gate rows of R, Wx and bias are pre-scaled by 1/2 so a
 // sigmoid is one hardware tanh and one FMA: sigmoid(x) = (1 + tanh(x/2)) / 2;
@@ -60,6 +62,8 @@ struct FwdCfg {
   static constexpr int NQ = (NTILE + 3) / 4;      // ldmatrix instructions for them
   // HS: h_{t-1} enters the MMA as a bf16 pair hi + lo (hi = bf16(h), lo = bf16(h - hi))
   static constexpr int HPARTS = HS ? 2 : 1;
+  // Wx prefetch depth in steps (ring stages): >= ~2 us of steps ahead
+  static constexpr int PD = DH >= 256 ? 4 : 8;
   // long k chains run as two interleaved accumulator sets
   static constexpr bool SPLITK = KS >= 8 || HS;
   static_assert(KS >= 2, "two k16 steps at least");
@@ -93,7 +97,8 @@ struct FwdSmem {
 };
 
 template <class C>
-__host__ __device__ inline FwdSmem fwd_smem_layout(int U, int NS) {
+__host__ __device__ inline FwdSmem fwd_smem_layout(int U) {
+  constexpr int NS = C::PD;
   FwdSmem L;
   const int NW = U / (C::MT * 16 / C::G);
   L.h = 0;
@@ -108,7 +113,7 @@ __host__ __device__ inline FwdSmem fwd_smem_layout(int U, int NS) {
   L.stg = o;  // per warp: h_t staging for the cluster exchange, two parities
   o += (uint32_t)NW * C::STG_BYTES * 2;
   L.bar = o;
-  o += (uint32_t)(2 * NS + 3) * 8;
+  o += 3 * 8;
   L.flag = o;
   o += 16;
   L.total = o;
@@ -150,7 +155,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   extern __shared__ __align__(128) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int U = p.U, NW = U / UG, CS = p.CS, NS = p.NS, T = p.T, B = p.B, NH = p.NH;
+  const int U = p.U, NW = U / UG, CS = p.CS, T = p.T, B = p.B, NH = p.NH;
+  constexpr int PD = C::PD;
   const uint32_t crank = CL ? cluster_ctarank() : 0u;
   const int cid = blockIdx.x / CS;
   const int head = cid / p.nbslices, bslice = cid % p.nbslices;
@@ -158,11 +164,10 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   const int b0 = bslice * NB;
   const int nvalid = min(NB, B - b0);
 
-  const FwdSmem L = fwd_smem_layout<C>(U, NS);
+  const FwdSmem L = fwd_smem_layout<C>(U);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t s_h = sbase + L.h, s_wx = sbase + L.wx, s_rf = sbase + L.rf;
-  const uint32_t bar_full = sbase + L.bar, bar_empty = bar_full + 8 * NS;
-  const uint32_t bar_h = bar_empty + 8 * NS;  // two: hfull[0], hfull[1]
+  const uint32_t bar_h = sbase + L.bar;  // two: hfull[0], hfull[1]
   const uint32_t bar_dummy = bar_h + 16;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flag);
   const uint32_t WP = C::wx_pitch(U);
@@ -172,10 +177,6 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 
   // ------------------------------------------------------------- set-up --
   if (tid == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(bar_full + 8 * s, 32);  // one cp.async-tracked arrival per producer lane
-      mbar_init(bar_empty + 8 * s, NW);
-    }
     mbar_init(bar_h, 1);
     mbar_init(bar_h + 8, 1);
     mbar_init(bar_dummy, 1);
@@ -185,7 +186,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   // batch rows past B: their ring rows stay zero forever (never copied into)
   if (nvalid < NB) {
     const int per = (NB - nvalid) * (int)WP / 4;
-    for (int i = tid; i < NS * per; i += blockDim.x) {
+    for (int i = tid; i < PD * per; i += blockDim.x) {
       const int s = i / per, r = i % per;
       *reinterpret_cast<uint32_t*>(smem + L.wx + s * stage_bytes + nvalid * WP + r * 4) = 0u;
     }
@@ -216,48 +217,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 
   const unsigned long long tlim = p.timeout_ns;
 
-  if (warp == NW) {
-    // ------------------------------------------------ Wx producer warp --
-    // The step's Wx slice is nvalid rows x G gates x U units; lane l copies the
-    // 16-byte chunks l, l+32, ... (offsets fixed for all steps, computed once).
-    constexpr int MAXCH = 32;
-    const int cpr = G * U / 8;  // chunks per batch row
-    const int nch = nvalid * cpr;
-    uint32_t dsto[MAXCH], srco[MAXCH];
-#pragma unroll
-    for (int i = 0; i < MAXCH; ++i) {
-      const int c = lane + 32 * i;
-      const int n = c / cpr, rem = c % cpr, g = rem / (U / 8), k = rem % (U / 8);
-      dsto[i] = (uint32_t)n * WP + (uint32_t)(g * U + 8 * k) * 2;
-      srco[i] = (uint32_t)(n * NH * GD + g * DH + 8 * k);
-    }
-    const __nv_bfloat16* Wx = static_cast<const __nv_bfloat16*>(p.Wx);
-    const size_t tstride = (size_t)B * NH * GD;
-    const __nv_bfloat16* rowt = Wx + ((size_t)b0 * NH + head) * GD + u0;
-    int s = 0;
-    uint32_t ph = 0;
-    for (int t = 0; t < T; ++t, rowt += tstride) {
-      bool stop = false;
-      if (lane == 0) {
-        if (t >= NS && !wait_phase<false>(bar_empty + 8 * s, ph ^ 1u, abort_flag, p.status, tlim))
-          stop = true;
-        if (*abort_flag) stop = true;
-      }
-      if (__shfl_sync(0xffffffffu, stop, 0)) break;
-      const uint32_t dst0 = s_wx + s * stage_bytes;
-#pragma unroll
-      for (int i = 0; i < MAXCH; ++i)
-        if (lane + 32 * i < nch) cp_async16(dst0 + dsto[i], rowt + srco[i]);
-      cp_async_mbar_arrive_noinc(bar_full + 8 * s);
-      if (++s == NS) {
-        s = 0;
-        ph ^= 1u;
-      }
-    }
-    // let every issued copy land before the CTA can exit
-    cp_async_wait_all();
-    __syncwarp();
-  } else {
+  {
     // ------------------------------------------------- compute warps --
     const uint16_t* Rb = static_cast<const uint16_t*>(p.R) + (size_t)head * DH * GD;
     const int ub = warp * UG;  // first CTA-local unit of this warp
@@ -381,8 +341,36 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
       if (!wait_phase<false>(bar_dummy, 0, abort_flag, p.status, tlim)) dead = true;
     }
 
-    int s = 0;
-    uint32_t ph = 0;
+    // this warp's Wx columns: G gates x UG units (UG/8 16-byte chunks) x nvalid
+    // rows; lane -> chunks lane, lane + 32 (offsets fixed for all steps)
+    constexpr int WCH = NB * G * (UG / 8), WCI = (WCH + 31) / 32;
+    uint32_t wdst[WCI], wsrc[WCI];
+    bool wok[WCI];
+#pragma unroll
+    for (int i = 0; i < WCI; ++i) {
+      const int c = lane + 32 * i;
+      const int n = c / (G * UG / 8), rem = c % (G * UG / 8), g = rem / (UG / 8), k = rem % (UG / 8);
+      wok[i] = c < WCH && n < nvalid;
+      wdst[i] = (uint32_t)n * WP + (uint32_t)(g * U + ub + 8 * k) * 2;
+      wsrc[i] = (uint32_t)(n * NH * GD + g * DH + u0 + ub + 8 * k);
+    }
+    const __nv_bfloat16* wx_base =
+        static_cast<const __nv_bfloat16*>(p.Wx) + ((size_t)b0 * NH + head) * GD;
+    const size_t wx_tstride = (size_t)B * NH * GD;
+    // copies of step tt into stage tt % PD, one commit group per step (empty past T)
+    auto fetch = [&](int tt) {
+      if (tt < T) {
+        const uint32_t stage = s_wx + (uint32_t)(tt % PD) * stage_bytes;
+        const __nv_bfloat16* src = wx_base + (size_t)tt * wx_tstride;
+#pragma unroll
+        for (int i = 0; i < WCI; ++i)
+          if (wok[i]) cp_async16(stage + wdst[i], src + wsrc[i]);
+      }
+      cp_async_commit();
+    };
+#pragma unroll 1
+    for (int tt = 0; tt < PD; ++tt) fetch(tt);
+    int np = 0;  // steps primed so far (step np is next; its stage is np % PD)
     // accumulators of the step about to run, primed with scale*(Wx + bias)
     float acc[MT][NT][4], acc2[SPLITK ? MT : 1][NT][4];
     float wxn[NE];  // GRU: Wx_n stays outside r*(R_n h + b_n)
@@ -393,8 +381,14 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     // the stage.  Runs while the step's MMAs are in flight (EARLY_PREP) or
     // after h_t is published, off the recurrence's critical path.
     auto prep = [&]() -> bool {
-      if (!wait_phase<false>(bar_full + 8 * s, ph, abort_flag, p.status, tlim)) return false;
-      const uint32_t stage = s_wx + s * stage_bytes;
+      // refill the stage the previous prime consumed (a whole step ago) with
+      // step np - 1 + PD, then wait for step np's group (PD - 1 younger ones
+      // may still be in flight)
+      if (np > 0) fetch(np - 1 + PD);
+      cp_async_wait<PD - 1>();
+      __syncwarp();
+      const uint32_t stage = s_wx + (uint32_t)(np % PD) * stage_bytes;
+      ++np;
       uint32_t wxr[NT][NQ * 4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -413,12 +407,6 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
             wxr[nt][4 * q + 1] = r2[1];
           }
         }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-      if (++s == NS) {
-        s = 0;
-        ph ^= 1u;
-      }
 #pragma unroll
       for (int us = 0; us < NSLOT; ++us)
 #pragma unroll
@@ -719,6 +707,9 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
             if (p.mT && CELL == kSLSTM) p.mT[si] = st_m[ei];
           }
     }
+    // let every issued Wx copy land before the CTA can exit
+    cp_async_wait_all();
+    __syncwarp();
   }
   // peers may still st.async into this CTA until they pass this point
   if (CL) cluster_sync();
@@ -731,16 +722,12 @@ int launch_fwd_bf16_v(const FwdParams& p_in, cudaStream_t stream, bool query_onl
   FwdParams p = p_in;
   auto kern = fwd_bf16_kernel<CELL, DH, UG, NT, KREG, HS, CL, TR>;
   const int NW = p.U / UG;
-  const int threads = (NW + 1) * 32;
+  const int threads = NW * 32;
   if (p.U % UG != 0 || NW < 1 || threads > C::MAXT) return (int)cudaErrorInvalidConfiguration;
-  // Wx ring depth: as deep as shared memory allows, 2..12 stages
   int dev = 0, max_smem = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  int ns = 12;
-  while (ns > 2 && fwd_smem_layout<C>(p.U, ns).total > (uint32_t)max_smem) --ns;
-  p.NS = ns;
-  const uint32_t smem = fwd_smem_layout<C>(p.U, ns).total;
+  const uint32_t smem = fwd_smem_layout<C>(p.U).total;
   if (smem > (uint32_t)max_smem) return (int)cudaErrorInvalidConfiguration;
   const int grid = p.NH * p.nbslices * p.CS;
   if (info) *info = LaunchInfo{grid, threads, p.CS, C::NB, (int)smem, CELL * 100 + DH / 32 + 50 * HS};

@@ -31,7 +31,6 @@ struct FwdParams {
   int T, B, NH;
   int CS;        // CTAs per (head, batch slice): thread-block cluster size
   int U;         // hidden units owned by one CTA (Dh / CS)
-  int NS;        // stages of the Wx ring
   int nbslices;  // batch slices per head
   int flags;
   unsigned long long timeout_ns;
