@@ -143,6 +143,50 @@ int rnn_input_proj(int32_t M, int32_t N, int32_t K, const void* x, const void* W
                    const float* bias, void* Wx, void* workspace, size_t workspace_bytes,
                    void* stream);
 
+/* Stacked layers run as a wavefront (FlashRNN blog page, paragraph on cuDNN
+ * and layer-level parallelism: layer l+1 can work on step t once layer l has
+ * produced h_t).  L layers of one cell and head shape (desc: RNN_BF16, no
+ * RNN_FLAG_TRAIN); layer 0 reads x, layer l > 0 reads layer l-1's h_seq; per
+ * layer Wx = in W^T + b_ih (as rnn_input_proj) feeds the recurrence.  Time is
+ * cut into chunks of `chunk` steps: layer l runs chunk c (its input projection,
+ * then the recurrence continuing from chunk c-1's final state) once layer l-1
+ * has finished chunk c, each layer on its own stream, so up to L layers run at
+ * once.  The result equals running the layers one after the other.
+ * Layouts (d = NH*Dh; the G*d projection rows are ordered [NH, G*Dh] like Wx):
+ *   x [T, B, Din] bf16;  W_ih0 [G*d, Din] bf16;  W_ih [L-1, G*d, d] bf16 (NULL if
+ *   L == 1);  b_ih [L, G*d] fp32 (NULL = 0);  R [L, NH, Dh, G*Dh] bf16;
+ *   bias [L, NH, G*Dh] fp32 (NULL = 0);  h0, c0, n0, m0 [L, B, NH, Dh] fp32
+ *   (NULL = 0);  h_seq [T, B, NH, Dh] bf16 (last layer);  hT, cT, nT, mT
+ *   [L, B, NH, Dh] fp32 (NULL = not written).
+ * chunk 0 = chosen by the plan search (rnn_plan), as are the CTAs per head when
+ * desc->cluster is 0 (so that the layers' recurrences fit the SMs together).
+ * Requires 1 <= L <= 8, chunk >= 0, Din % 8 == 0.  Alignment: bf16 arrays 16
+ * bytes, fp32 arrays 4, workspace 256 bytes and >= rnn_stack_workspace_size()
+ * (status word at offset 0, then the layers' intermediate h_seq, Wx chunks and
+ * carried states).  The per-layer streams and events are created on a device's
+ * first call and kept (host resources, no device memory); the enqueue is
+ * serialised across host threads.  `stream` waits for all of the work. */
+size_t rnn_stack_workspace_size(const rnn_desc_t* desc, int32_t L, int32_t chunk);
+int rnn_stack_fwd(const rnn_desc_t* desc, int32_t L, int32_t Din, int32_t chunk, const void* x,
+                  const void* W_ih0, const void* W_ih, const float* b_ih, const void* R,
+                  const float* bias, const float* h0, const float* c0, const float* n0,
+                  const float* m0, void* h_seq, float* hT, float* cT, float* nT, float* mT,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* The launch plan the library picks when desc->cluster is 0: an integer search
+ * over CTAs per head (1, 2, 4, 8, 16) -- and for L > 1 stacked layers the time
+ * chunk -- in the spirit of the FlashRNN card's ConstrINT (hardware limits as
+ * integer constraints with divisibility).  A candidate must split the head into
+ * whole unit groups of a warp, fit the compiled variant's register budget and
+ * shared memory, and (clusters) at most 16 CTAs; the cost is the per-step time
+ * (measured on GB300 per cell, Dh and CTAs per head; a latency model where not
+ * measured) times the waves the CTAs need over `sms` SMs, and for L > 1 the
+ * wavefront's stages given how many layers fit on the SMs at once.
+ * sms <= 0: the current device's SM count.  out5[0..4] = CTAs per head, time
+ * chunk (T for one layer), CTAs per layer, waves, predicted microseconds.
+ * RNN_BF16 only.  Host computation (no launch). */
+int rnn_plan(const rnn_desc_t* desc, int32_t L, int32_t sms, int32_t* out5);
+
 /* Synchronises `stream`, reads the device status word of `workspace` into
  * *device_status (RNN_OK or RNN_ERR_TIMEOUT).  Returns RNN_OK if the read
  * itself worked, else RNN_ERR_LAUNCH. */

@@ -52,7 +52,7 @@ import numpy as np
 
 __all__ = ["GATES", "forward", "backward", "lstm_forward", "gru_forward",
            "slstm_forward", "lstm_backward", "gru_backward", "slstm_backward",
-           "input_projection"]
+           "input_projection", "stack_forward"]
 
 GATES = {"lstm": 4, "gru": 3, "slstm": 4}
 
@@ -324,3 +324,36 @@ def input_projection(x, W, b=None):
     if b is not None:
         out = out + np.asarray(b, np.float64)[None, :]
     return out
+
+
+# ------------------------------------------------------------ stacked layers --
+def stack_forward(cell, x, W_ih0, W_ih, b_ih, R, b, h0=None, c0=None, n0=None, m0=None):
+    """L stacked head-wise layers (the blog page's layer-level parallelism
+    paragraph runs layers concurrently; the result is that of running them in
+    order): layer 0 reads x [T, B, Din], layer l > 0 reads layer l-1's h_seq.
+
+    W_ih0 [G*d, Din] and W_ih [L-1, G*d, d] (d = NH*Dh, rows ordered [NH, G*Dh]),
+    b_ih [L, G*d] or None, R [L, NH, Dh, G*Dh], b [L, NH, G*Dh] or None, initial
+    states [L, B, NH, Dh] or None.  Returns the last layer's h_seq and every
+    layer's final states stacked over L.
+    """
+    x = np.asarray(x, np.float64)
+    T, B, _ = x.shape
+    L, NH, Dh = R.shape[0], R.shape[1], R.shape[2]
+    G = GATES[cell]
+    inp = x.reshape(T * B, -1)
+    finals = {}
+    out = None
+    for l in range(L):
+        W = W_ih0 if l == 0 else W_ih[l - 1]
+        Wx = input_projection(inp, W, None if b_ih is None else b_ih[l]).reshape(T, B, NH, G * Dh)
+        pick = (lambda s: None if s is None else s[l])
+        out = forward(cell, Wx, R[l], pick(b), pick(h0), pick(c0), pick(n0), pick(m0))
+        for k in ("hT", "cT", "nT", "mT"):
+            if k in out:
+                finals.setdefault(k, []).append(out[k])
+        inp = out["h_seq"].reshape(T * B, NH * Dh)
+    res = {"h_seq": out["h_seq"]}
+    for k, v in finals.items():
+        res[k] = np.stack(v)
+    return res

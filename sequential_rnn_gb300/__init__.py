@@ -20,7 +20,8 @@ from ._lib import (CELLS, DTYPES, RNN_BF16, RNN_F32, RNN_FLAG_H_BF16, RNN_FLAG_T
 
 __all__ = ["RnnError", "make_desc", "rnn_workspace_size", "rnn_stash_size", "rnn_fwd", "rnn_bwd",
            "rnn_read_status", "rnn_sync_floor", "rnn_fwd_config", "rnn_status_str", "rnn_fwd_noalloc",
-           "rnn_input_proj", "forward", "backward", "input_proj", "GATES"]
+           "rnn_input_proj", "rnn_stack_workspace_size", "rnn_stack_fwd", "forward", "backward",
+           "input_proj", "stack_forward", "rnn_plan", "GATES"]
 
 GATES = {"lstm": 4, "gru": 3, "slstm": 4}
 
@@ -107,6 +108,27 @@ def rnn_input_proj(M: int, N: int, K: int, x, W, bias, Wx, workspace, stream=Non
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     return int(_lib.load().rnn_input_proj(int(M), int(N), int(K), _ptr(x), _ptr(W), _ptr(bias),
                                           _ptr(Wx), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def rnn_stack_workspace_size(desc: rnn_desc_t, L: int, chunk: int) -> int:
+    return int(_lib.load().rnn_stack_workspace_size(ctypes.byref(desc), int(L), int(chunk)))
+
+
+def rnn_stack_fwd(desc, L, Din, chunk, x, W_ih0, W_ih, b_ih, R, bias, h0, c0, n0, m0, h_seq, hT,
+                  cT, nT, mT, workspace, stream=None) -> int:
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return int(_lib.load().rnn_stack_fwd(
+        ctypes.byref(desc), int(L), int(Din), int(chunk), _ptr(x), _ptr(W_ih0), _ptr(W_ih),
+        _ptr(b_ih), _ptr(R), _ptr(bias), _ptr(h0), _ptr(c0), _ptr(n0), _ptr(m0), _ptr(h_seq),
+        _ptr(hT), _ptr(cT), _ptr(nT), _ptr(mT), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def rnn_plan(desc: rnn_desc_t, L: int = 1, sms: int = 0) -> dict:
+    out = (ctypes.c_int32 * 5)()
+    st = _lib.load().rnn_plan(ctypes.byref(desc), int(L), int(sms), out)
+    if st:
+        raise RnnError(st, "rnn_plan")
+    return dict(zip(("cluster", "chunk", "ctas", "waves", "us"), list(out)))
 
 
 def rnn_read_status(workspace, stream=None) -> int:
@@ -215,4 +237,41 @@ def input_proj(x, W, bias=None, *, stream=None, check=True):
         dst = rnn_read_status(ws, stream)
         if dst:
             raise RnnError(dst, "rnn_input_proj (device)")
+    return out
+
+
+def stack_forward(cell: str, x, W_ih0, W_ih, b_ih, R, bias=None, h0=None, c0=None, n0=None,
+                  m0=None, *, chunk=0, cluster=0, stream=None, check=True):
+    """L stacked layers through rnn_stack_fwd (layer wavefront over time chunks).
+
+    x [T, B, Din] bf16; W_ih0 [G*d, Din]; W_ih [L-1, G*d, d] or None; b_ih [L, G*d];
+    R [L, NH, Dh, G*Dh] bf16; bias [L, NH, G*Dh]; states [L, B, NH, Dh] fp32 or None.
+    chunk = 0 and cluster = 0 let the plan search choose.  Returns the last
+    layer's h_seq and every layer's final states.
+    """
+    T, B, Din = x.shape
+    L, NH, Dh = R.shape[0], R.shape[1], R.shape[2]
+    desc = make_desc(cell, "bf16", T, B, NH, Dh, 0, cluster)
+    dev = x.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = {"h_seq": torch.empty((T, B, NH, Dh), dtype=torch.bfloat16, device=dev),
+           "hT": torch.empty((L, B, NH, Dh), **f32)}
+    if cell != "gru":
+        out["cT"] = torch.empty((L, B, NH, Dh), **f32)
+    if cell == "slstm":
+        out["nT"] = torch.empty((L, B, NH, Dh), **f32)
+        out["mT"] = torch.empty((L, B, NH, Dh), **f32)
+    nbytes = rnn_stack_workspace_size(desc, L, chunk)
+    # no zero fill needed: the call clears its status word and writes every
+    # intermediate before reading it
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    st = rnn_stack_fwd(desc, L, Din, chunk, x, W_ih0, W_ih, b_ih, R, bias, h0, c0, n0, m0,
+                       out["h_seq"], out["hT"], out.get("cT"), out.get("nT"), out.get("mT"), ws,
+                       stream)
+    if st:
+        raise RnnError(st, "rnn_stack_fwd")
+    if check:
+        dst = rnn_read_status(ws, stream)
+        if dst:
+            raise RnnError(dst, "rnn_stack_fwd (device)")
     return out

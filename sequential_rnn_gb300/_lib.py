@@ -26,7 +26,7 @@ DTYPES = {"f32": RNN_F32, "bf16": RNN_BF16}
 # Every symbol include/rnn.h declares (checked by the CPU tests).
 EXPORTS = ("rnn_workspace_size", "rnn_stash_size", "rnn_fwd", "rnn_bwd", "rnn_read_status",
            "rnn_sync_floor", "rnn_fwd_config", "rnn_status_str", "rnn_fwd_noalloc",
-           "rnn_input_proj")
+           "rnn_input_proj", "rnn_stack_workspace_size", "rnn_stack_fwd", "rnn_plan")
 
 
 class rnn_desc_t(ctypes.Structure):
@@ -51,6 +51,9 @@ _SIGS = {
     "rnn_status_str": (ctypes.c_char_p, [_I]),
     "rnn_fwd_noalloc": (_I, [_DESC] + [_P] * 14),
     "rnn_input_proj": (_I, [ctypes.c_int32] * 3 + [_P] * 5 + [_SZ, _P]),
+    "rnn_stack_workspace_size": (_SZ, [_DESC, ctypes.c_int32, ctypes.c_int32]),
+    "rnn_stack_fwd": (_I, [_DESC] + [ctypes.c_int32] * 3 + [_P] * 16 + [_SZ, _P]),
+    "rnn_plan": (_I, [_DESC, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
 }
 
 _lib = None

@@ -759,6 +759,17 @@ int launch_fwd_bf16_v(const FwdParams& p_in, cudaStream_t stream, bool query_onl
   return (int)cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+// Launch limits of one compiled variant, for the host-side plan search: the
+// largest CTA its register budget allows, its unit group and the dynamic
+// shared memory a CTA of U units needs.
+template <int CELL, int DH, int UG, int NT, int KREG, int HS = 0>
+void fwd_bf16_limits_t(int U, FwdLimits* out) {
+  using C = FwdCfg<CELL, DH, UG, NT, KREG, HS>;
+  out->max_threads = C::MAXT;
+  out->unit_group = UG;
+  out->smem = (U > 0 && U % UG == 0) ? fwd_smem_layout<C>(U).total : 0u;
+}
+
 // Picks the cluster / training-stash variant of one (cell, Dh, unit group, KREG, HS).
 // Heads that cannot fit one SM (Dh >= 256) only exist as cluster variants.
 template <int CELL, int DH, int UG, int NT, int KREG, int HS = 0>

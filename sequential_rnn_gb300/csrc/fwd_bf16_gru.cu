@@ -17,4 +17,17 @@ int launch_fwd_bf16_gru(const FwdParams& p, int Dh, int NT, cudaStream_t s, bool
   }
 }
 
+
+// the same variants' launch limits, for the plan search
+int fwd_bf16_gru_limits(int Dh, int U, FwdLimits* o) {
+  switch (Dh) {
+    case 32: fwd_bf16_limits_t<kGRU, 32, 16, 1, 2>(U, o); return 0;
+    case 64: fwd_bf16_limits_t<kGRU, 64, 16, 1, 4>(U, o); return 0;
+    case 128: fwd_bf16_limits_t<kGRU, 128, 16, 1, 6>(U, o); return 0;
+    case 256: fwd_bf16_limits_t<kGRU, 256, 16, 1, 10>(U, o); return 0;
+    case 768: fwd_bf16_limits_t<kGRU, 768, 16, 1, 10>(U, o); return 0;
+    default: return 1;
+  }
+}
+
 }  // namespace srnn

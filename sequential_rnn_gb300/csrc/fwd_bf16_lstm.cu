@@ -17,4 +17,17 @@ int launch_fwd_bf16_lstm(const FwdParams& p, int Dh, int NT, cudaStream_t s, boo
   }
 }
 
+
+// the same variants' launch limits, for the plan search
+int fwd_bf16_lstm_limits(int Dh, int U, FwdLimits* o) {
+  switch (Dh) {
+    case 32: fwd_bf16_limits_t<kLSTM, 32, 8, 1, 2>(U, o); return 0;
+    case 64: fwd_bf16_limits_t<kLSTM, 64, 8, 1, 4>(U, o); return 0;
+    case 128: fwd_bf16_limits_t<kLSTM, 128, 8, 1, 8>(U, o); return 0;
+    case 256: fwd_bf16_limits_t<kLSTM, 256, 8, 1, 16>(U, o); return 0;
+    case 768: fwd_bf16_limits_t<kLSTM, 768, 8, 1, 20>(U, o); return 0;
+    default: return 1;
+  }
+}
+
 }  // namespace srnn

@@ -28,4 +28,26 @@ int launch_fwd_bf16_slstm(const FwdParams& p, int Dh, int NT, int hsplit, cudaSt
   }
 }
 
+
+// the same variants' launch limits, for the plan search
+int fwd_bf16_slstm_limits(int Dh, int hsplit, int U, FwdLimits* o) {
+  if (hsplit) {
+    switch (Dh) {
+      case 32: fwd_bf16_limits_t<kSLSTM, 32, 8, 1, 2, 1>(U, o); return 0;
+      case 64: fwd_bf16_limits_t<kSLSTM, 64, 8, 1, 4, 1>(U, o); return 0;
+      case 128: fwd_bf16_limits_t<kSLSTM, 128, 8, 1, 8, 1>(U, o); return 0;
+      case 256: fwd_bf16_limits_t<kSLSTM, 256, 8, 1, 12, 1>(U, o); return 0;
+      default: return 1;
+    }
+  }
+  switch (Dh) {
+    case 32: fwd_bf16_limits_t<kSLSTM, 32, 8, 1, 2>(U, o); return 0;
+    case 64: fwd_bf16_limits_t<kSLSTM, 64, 8, 1, 4>(U, o); return 0;
+    case 128: fwd_bf16_limits_t<kSLSTM, 128, 8, 1, 8>(U, o); return 0;
+    case 256: fwd_bf16_limits_t<kSLSTM, 256, 8, 1, 16>(U, o); return 0;
+    case 768: fwd_bf16_limits_t<kSLSTM, 768, 8, 1, 18>(U, o); return 0;
+    default: return 1;
+  }
+}
+
 }  // namespace srnn

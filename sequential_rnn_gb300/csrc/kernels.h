@@ -44,6 +44,17 @@ struct LaunchInfo {
 // With `query_only` nothing is launched.
 int launch_fwd_f32(const FwdParams& p, int cell, int Dh, cudaStream_t s, bool query_only,
                    LaunchInfo* info);
+// Launch limits of the compiled bf16 forward variant for (cell, Dh) (host only).
+struct FwdLimits {
+  int max_threads;     // CTA size the register budget allows
+  int unit_group;      // hidden units per warp
+  uint32_t smem;       // dynamic shared memory of a CTA owning U units
+};
+// each returns 0, or nonzero when no variant exists for Dh
+int fwd_bf16_lstm_limits(int Dh, int U, FwdLimits* o);
+int fwd_bf16_gru_limits(int Dh, int U, FwdLimits* o);
+int fwd_bf16_slstm_limits(int Dh, int hsplit, int U, FwdLimits* o);
+
 int launch_fwd_bf16_lstm(const FwdParams& p, int Dh, int NT, cudaStream_t s, bool query_only,
                          LaunchInfo* info);
 int launch_fwd_bf16_gru(const FwdParams& p, int Dh, int NT, cudaStream_t s, bool query_only,
@@ -92,8 +103,11 @@ int launch_h0_to_bf16(const float* h0, void* out, int n, cudaStream_t s);
 int launch_dR_tc(const void* h_seq, const void* h0b, const void* dG, float* dR, int T, int B,
                  int NH, int Dh, int G, int* status, unsigned long long timeout_ns,
                  cudaStream_t s);
+// max_ctas > 0 caps the persistent grid (SMs left free for concurrent kernels)
 int launch_input_proj_tc(const void* x, const void* W, const float* bias, void* Wx, int M, int N,
-                         int K, int* status, unsigned long long timeout_ns, cudaStream_t s);
+                         int K, int* status, unsigned long long timeout_ns, cudaStream_t s,
+                         int max_ctas = 0);
+int sm_count();
 int launch_db_reduce(const float* part, float* db, int nslices, int n, cudaStream_t s);
 
 }  // namespace srnn

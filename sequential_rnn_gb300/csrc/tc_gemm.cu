@@ -361,10 +361,10 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-// grid: one CTA per SM (at most one per unit)
+// grid: one CTA per SM (at most one per unit, at most max_ctas if > 0)
 template <bool A_MN, bool B_MN, int OUT, int BN>
 int launch_tc(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1,
-              const CUtensorMap& b1, GemmArgs g, cudaStream_t s) {
+              const CUtensorMap& b1, GemmArgs g, cudaStream_t s, int max_ctas = 0) {
   using C = TcCfg<BN>;
   auto kern = tc_gemm_kernel<A_MN, B_MN, OUT, BN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -373,13 +373,17 @@ int launch_tc(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a
   g.tiles_n = (g.N + BN - 1) / BN;
   const long long units = (long long)g.Z * g.tiles_m * g.tiles_n * g.ksplit;
   if (units > 0x7fffffffLL) return (int)cudaErrorInvalidValue;
-  const int grid = (int)(units < num_sms() ? units : num_sms());
+  int cap = num_sms();
+  if (max_ctas > 0 && max_ctas < cap) cap = max_ctas;
+  const int grid = (int)(units < cap ? units : cap);
   if (grid == 0) return 0;
   kern<<<grid, 192, C::SMEM, s>>>(a0, b0, a1, b1, g);
   return (int)cudaGetLastError();
 }
 
 }  // namespace
+
+int sm_count() { return num_sms(); }
 
 int launch_dR_tc(const void* h_seq, const void* h0b, const void* dG, float* dR, int T, int B,
                  int NH, int Dh, int G, int* status, unsigned long long timeout_ns,
@@ -426,7 +430,8 @@ int launch_dR_tc(const void* h_seq, const void* h0b, const void* dG, float* dR, 
 }
 
 int launch_input_proj_tc(const void* x, const void* W, const float* bias, void* Wx, int M, int N,
-                         int K, int* status, unsigned long long timeout_ns, cudaStream_t s) {
+                         int K, int* status, unsigned long long timeout_ns, cudaStream_t s,
+                         int max_ctas) {
   const bool wide = N >= 256;
   CUtensorMap a0, b0;
   int e = make_map(&a0, x, (uint64_t)M, (uint64_t)K, (uint64_t)K, 64, 128);
@@ -446,8 +451,8 @@ int launch_input_proj_tc(const void* x, const void* W, const float* bias, void* 
   g.bias = bias;
   g.status = status;
   g.timeout_ns = timeout_ns;
-  if (wide) return launch_tc<false, false, kOutBf16Bias, 256>(a0, b0, a0, b0, g, s);
-  return launch_tc<false, false, kOutBf16Bias, 128>(a0, b0, a0, b0, g, s);
+  if (wide) return launch_tc<false, false, kOutBf16Bias, 256>(a0, b0, a0, b0, g, s, max_ctas);
+  return launch_tc<false, false, kOutBf16Bias, 128>(a0, b0, a0, b0, g, s, max_ctas);
 }
 
 }  // namespace srnn

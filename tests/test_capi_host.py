@@ -146,3 +146,106 @@ def test_input_proj_argument_checks(lib):
     assert _proj(lib, Wx=0x3002) == 3
     assert _proj(lib, bias=0x4002) == 3
     assert _proj(lib, M=0, x=0, Wx=0) == 0                  # empty input: no-op
+
+
+def _stack(lib, desc=None, L=2, Din=96, chunk=16, x=0x1000, W0=0x2000, W=0x3000, R=0x4000,
+           h_seq=0x5000, ws=0x10000, ws_bytes=None, **fp):
+    P = ctypes.c_void_p
+    desc = desc or _desc()
+    if ws_bytes is None:
+        ws_bytes = lib.rnn_stack_workspace_size(ctypes.byref(desc), L if 1 <= L <= 8 else 1,
+                                                max(chunk, 1))
+    f = {k: (P(fp[k]) if fp.get(k) else None)
+         for k in ("b_ih", "bias", "h0", "c0", "n0", "m0", "hT", "cT", "nT", "mT")}
+    return lib.rnn_stack_fwd(ctypes.byref(desc), L, Din, chunk, P(x) if x else None,
+                             P(W0) if W0 else None, P(W) if W else None, f["b_ih"],
+                             P(R) if R else None, f["bias"], f["h0"], f["c0"], f["n0"], f["m0"],
+                             P(h_seq) if h_seq else None, f["hT"], f["cT"], f["nT"], f["mT"],
+                             P(ws) if ws else None, ws_bytes, None)
+
+
+def test_stack_workspace_size(lib):
+    d = _desc()  # LSTM bf16, see _desc
+    T, B, NH, Dh = d.T, d.B, d.NH, d.Dh
+    al = lambda v: (v + 255) // 256 * 256
+    dd = NH * Dh
+    tc = min(16, T)
+    want = 256 + al((2 - 1) * T * B * dd * 2) + 2 * al(tc * B * 4 * dd * 2) + 2 * 2 * 2 * al(B * dd * 4)
+    assert lib.rnn_stack_workspace_size(ctypes.byref(d), 2, 16) == want
+    assert lib.rnn_stack_workspace_size(ctypes.byref(d), 0, 16) == 0
+    assert lib.rnn_stack_workspace_size(ctypes.byref(d), 9, 16) == 0
+    assert lib.rnn_stack_workspace_size(ctypes.byref(d), 2, -1) == 0
+
+
+def test_stack_argument_checks(lib):
+    assert _stack(lib, L=0, ws_bytes=1 << 30) == 1
+    assert _stack(lib, L=9, ws_bytes=1 << 30) == 1
+    assert _stack(lib, chunk=-1, ws_bytes=1 << 30) == 1
+    assert _stack(lib, Din=0) == 1
+    assert _stack(lib, Din=12) == 2                        # Din % 8
+    assert _stack(lib, desc=_desc(dtype=0)) == 2           # bf16 only
+    assert _stack(lib, desc=_desc(flags=1)) == 2           # no training stash
+    assert _stack(lib, desc=_desc(Dh=48)) == 2
+    assert _stack(lib, ws_bytes=256) == 1
+    assert _stack(lib, ws=0) == 1
+    assert _stack(lib, ws=0x10010) == 3
+    assert _stack(lib, x=0) == 1
+    assert _stack(lib, W=0) == 1                           # L > 1 needs W_ih
+    assert _stack(lib, R=0) == 1
+    assert _stack(lib, x=0x1008) == 3
+    assert _stack(lib, W0=0x2004) == 3
+    assert _stack(lib, h0=0x6002) == 3
+    assert _stack(lib, desc=_desc(B=0)) == 0               # empty batch: no-op
+
+
+def _plan(lib, L=1, sms=148, **kw):
+    out = (ctypes.c_int32 * 5)()
+    st = lib.rnn_plan(ctypes.byref(_desc(**kw)), L, sms, out)
+    return st, list(out)
+
+
+@pytest.mark.parametrize("cell,Dh,NH,B,T,want", [
+    (0, 64, 12, 16, 1024, 4),    # LSTM 12 x 64: the 4-CTA cluster (measured best)
+    (1, 128, 6, 8, 2048, 4),     # GRU 6 x 128
+    (2, 256, 4, 4, 4096, 8),     # sLSTM 4 x 256 (hi + lo h)
+    (0, 768, 1, 16, 1024, 16),   # LSTM 1 x 768: only the 16-CTA split fits on chip
+    (1, 64, 12, 16, 512, 1),     # GRU 64: one CTA per head is fastest
+])
+def test_plan_picks_measured_best(lib, cell, Dh, NH, B, T, want):
+    st, out = _plan(lib, cell=cell, Dh=Dh, NH=NH, B=B, T=T)
+    assert st == 0 and out[0] == want, out
+    nb = (B + 7) // 8
+    assert out[2] == NH * nb * want and out[3] == -(-out[2] // 148)
+
+
+def test_plan_respects_constraints_and_occupancy(lib):
+    # every automatic plan splits the head into whole unit groups and legal clusters
+    for cell in (0, 1, 2):
+        for Dh in (32, 64, 128, 256, 768):
+            for NH, B in ((1, 4), (12, 16), (64, 256)):
+                st, out = _plan(lib, cell=cell, Dh=Dh, NH=NH, B=B, T=256)
+                assert st == 0, (cell, Dh)
+                cs = out[0]
+                ug = 16 if cell == 1 else 8
+                assert cs in (1, 2, 4, 8, 16) and Dh % cs == 0 and (Dh // cs) % ug == 0
+                assert (Dh // cs) // ug * 32 <= 1024
+                assert cs > 1 or Dh <= 128
+    # many heads and batch rows: waves over the SMs favour one CTA per head
+    assert _plan(lib, Dh=64, NH=64, B=256)[1][0] == 1
+    # few SMs: the 4-CTA split would need 4 waves
+    assert _plan(lib, Dh=64, NH=12, B=16, sms=24)[1][0] == 1
+    # an explicit cluster size is kept, and an impossible one is rejected
+    assert _plan(lib, Dh=64, cluster=8)[1][0] == 8
+    assert _plan(lib, Dh=256, cluster=2)[0] == 2
+    assert _plan(lib, dtype=0)[0] == 2
+
+
+def test_plan_for_stacked_layers(lib):
+    # three 12 x 64 layers: one CTA per head so the layers' recurrences run side by side
+    st, out = _plan(lib, L=3, Dh=64, NH=12, B=16, T=1024)
+    assert st == 0 and out[0] == 1 and out[1] in (64, 128, 256), out
+    assert 3 * out[2] <= 148
+    # the workspace size follows the planned chunk
+    d = _desc(Dh=64, NH=12, B=16, T=1024)
+    assert lib.rnn_stack_workspace_size(ctypes.byref(d), 3, 0) == \
+        lib.rnn_stack_workspace_size(ctypes.byref(d), 3, out[1])

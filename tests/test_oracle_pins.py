@@ -346,3 +346,32 @@ def test_projection_then_recurrence_matches_torch_rnn(cell):
     b_hh = mod.bias_hh_l0.detach().numpy()[None]
     ref = O.forward(cell, Wx, R, b_hh, h0[:, None], c0[:, None])
     np.testing.assert_allclose(ref["h_seq"][:, :, 0], out, rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("cell", ["lstm", "gru"])
+def test_stack_matches_torch_multilayer(cell):
+    """torch.nn.LSTM / GRU with num_layers = 3 == the oracle's stacked layers (one head)."""
+    rng = np.random.default_rng(8)
+    T, B, Din, Dh, L = 5, 2, 7, 4, 3
+    G = O.GATES[cell]
+    mod = (torch.nn.LSTM if cell == "lstm" else torch.nn.GRU)(Din, Dh, num_layers=L,
+                                                               dtype=torch.float64)
+    x = rng.standard_normal((T, B, Din))
+    h0 = rng.standard_normal((L, B, Dh)) * 0.5
+    c0 = rng.standard_normal((L, B, Dh)) * 0.5
+    with torch.no_grad():
+        args = (torch.from_numpy(h0), torch.from_numpy(c0)) if cell == "lstm" \
+            else torch.from_numpy(h0)
+        res = mod(torch.from_numpy(x), args)
+    out = res[0].numpy()
+    hn = (res[1][0] if cell == "lstm" else res[1]).numpy()
+    P = {n: p.detach().numpy() for n, p in mod.named_parameters()}
+    W_ih0 = P["weight_ih_l0"]
+    W_ih = np.stack([P[f"weight_ih_l{l}"] for l in range(1, L)])
+    b_ih = np.stack([P[f"bias_ih_l{l}"] for l in range(L)])
+    R = np.stack([P[f"weight_hh_l{l}"].T[None] for l in range(L)])
+    b = np.stack([P[f"bias_hh_l{l}"][None] for l in range(L)])
+    ref = O.stack_forward(cell, x, W_ih0, W_ih, b_ih, R, b, h0[:, :, None], c0[:, :, None])
+    np.testing.assert_allclose(ref["h_seq"][:, :, 0], out, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(ref["hT"][:, :, 0], hn, rtol=1e-10, atol=1e-12)
+    assert W_ih0.shape == (G * Dh, Din)
