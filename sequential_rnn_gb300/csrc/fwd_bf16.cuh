@@ -147,6 +147,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   // A cluster step is latency-bound (few warps per SM): two k chains and plain
   // fp32 tanh.  One CTA per head is throughput-bound: packed fp16x2 tanh.
   constexpr bool SPLITK = C::SPLITK || CL;
+  // hi/lo split over >= 8 k16 steps: hi and lo each on two chains (even/odd k pairs)
+  constexpr bool HS4 = HS && KS >= 8;
   constexpr bool PACKED_TANH = !CL;
   // One CTA per head (all warps meet at a barrier every step): the next step's
   // Wx is primed while this step's MMAs are in flight, in a second accumulator
@@ -373,6 +375,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     int np = 0;  // steps primed so far (step np is next; its stage is np % PD)
     // accumulators of the step about to run, primed with scale*(Wx + bias)
     float acc[MT][NT][4], acc2[SPLITK ? MT : 1][NT][4];
+    float acc3[HS4 ? MT : 1][NT][4], acc4[HS4 ? MT : 1][NT][4];
     float wxn[NE];  // GRU: Wx_n stays outside r*(R_n h + b_n)
     float accp[MT][NT][4], wxnp[NE];  // EARLY_PREP: primed for the next step
     float(*A)[NT][4] = EARLY_PREP ? accp : acc;
@@ -462,6 +465,14 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 #pragma unroll
               for (int q = 0; q < 4; ++q) acc2[mt][nt][q] = 0.f;
         }
+        if (HS4) {
+#pragma unroll
+          for (int mt = 0; mt < (HS4 ? MT : 1); ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) acc3[mt][nt][q] = acc4[mt][nt][q] = 0.f;
+        }
         // ---- acc += R^T h_{t-1}
         const uint32_t hb = s_h + (uint32_t)(t & 1) * NB * HPB + lm_off;
 #pragma unroll
@@ -488,7 +499,11 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
               }
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
-                if (HS) {  // hi and lo parts on two independent accumulator chains
+                if (HS4 && (kp & 1)) {  // odd k pairs: the second hi and lo chains
+                  mma_bf16_16816(acc3[HS4 ? mt : 0][nt], a, bfr[nt][2 * hf], bfr[nt][2 * hf + 1]);
+                  mma_bf16_16816(acc4[HS4 ? mt : 0][nt], a, bfl[HS ? nt : 0][2 * hf],
+                                 bfl[HS ? nt : 0][2 * hf + 1]);
+                } else if (HS) {  // hi and lo parts on two independent accumulator chains
                   mma_bf16_16816(acc[mt][nt], a, bfr[nt][2 * hf], bfr[nt][2 * hf + 1]);
                   mma_bf16_16816(acc2[SPLITK ? mt : 0][nt], a, bfl[HS ? nt : 0][2 * hf],
                                  bfl[HS ? nt : 0][2 * hf + 1]);
@@ -509,7 +524,13 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-              for (int q = 0; q < 4; ++q) acc[mt][nt][q] += acc2[SPLITK ? mt : 0][nt][q];
+              for (int q = 0; q < 4; ++q) {
+                if (HS4)
+                  acc[mt][nt][q] = (acc[mt][nt][q] + acc3[HS4 ? mt : 0][nt][q]) +
+                                   (acc2[mt][nt][q] + acc4[HS4 ? mt : 0][nt][q]);
+                else
+                  acc[mt][nt][q] += acc2[SPLITK ? mt : 0][nt][q];
+              }
         }
 
         // ---- gate math and state update, one (unit, batch) cell at a time
@@ -560,18 +581,21 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
               } else {
                 const float pi = r[0], pf = r[1], pz = r[2], po = r[3];
                 const float mn = fmaxf(pf + st_m[ei], pi);
-                // HS: accurate exp/tanh (the exponential gating amplifies rounding)
-                const float ig = HS ? expf(pi - mn) : __expf(pi - mn);
-                const float fg = HS ? expf(pf + st_m[ei] - mn) : __expf(pf + st_m[ei] - mn);
-                const float zt = HS ? tanhf(pz) : tanh_fast(pz);
+                // Exponentials from the ex2-based __expf (2 ulp).  HS: tanh z~ from
+                // the identity tanh(x) = 1 - 2 / (e^{2x} + 1) on it -- the hardware
+                // tanh.approx (~2^-11 relative) lets the exponential gating drift
+                // 3e-2 from the exact recurrence over 4096 steps, this ~1e-6.
+                const float ig = __expf(pi - mn);
+                const float fg = __expf(pf + st_m[ei] - mn);
+                const float zt = HS ? 1.f - __fdividef(2.f, __expf(2.f * pz) + 1.f) : tanh_fast(pz);
                 const float c = fmaf(fg, st_c[ei], ig * zt);
                 const float nn = fmaf(fg, st_n[ei], ig);
                 st_c[ei] = c;
                 st_n[ei] = nn;
                 st_m[ei] = mn;
                 // r[o] holds o~ (HS) or o~/2 (fast path)
-                const float og = HS ? 1.f / (1.f + expf(-po)) : fmaf(0.5f, tanh_fast(po), 0.5f);
-                h = og * (c / nn);
+                const float og = HS ? __fdividef(1.f, 1.f + __expf(-po)) : fmaf(0.5f, tanh_fast(po), 0.5f);
+                h = og * __fdividef(c, nn);
                 if (TR) {
                   act[0][TR ? ei : 0] = ig;
                   act[1][TR ? ei : 0] = fg;
