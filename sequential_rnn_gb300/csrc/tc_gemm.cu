@@ -41,18 +41,21 @@ namespace {
 
 constexpr int TBM = 128, TBK = 64;
 
-template <int BN>
+enum : int { kOutF32 = 0, kOutBf16Bias = 1, kOutF32Add = 2 };
+
+template <int BN, int OUT>
 struct TcCfg {
   static constexpr uint32_t TILE_A = TBM * TBK * 2;        // 16 KB
   static constexpr uint32_t TILE_B = BN * TBK * 2;         // 16 or 32 KB
   static constexpr uint32_t STAGE = TILE_A + TILE_B;
   static constexpr int NSTG = BN == 256 ? 4 : 6;
   static constexpr uint32_t TMEM_COLS = 2 * BN;            // two accumulator buffers
-  // ring + 1024 for aligning it + barriers (full, empty, tfull x2, tempty x2) + TMEM slot
-  static constexpr uint32_t SMEM = NSTG * STAGE + 1024 + (2 * NSTG + 4) * 8 + 16;
+  // bf16 output: per epilogue warp two 32-row x 64-column boxes staged for TMA stores
+  static constexpr uint32_t OUT_STAGE = OUT == kOutBf16Bias ? 4 * 8192 : 0;
+  // ring + output staging + 1024 for aligning them + barriers (full, empty,
+  // tfull x2, tempty x2) + TMEM slot
+  static constexpr uint32_t SMEM = NSTG * STAGE + OUT_STAGE + 1024 + (2 * NSTG + 4) * 8 + 16;
 };
-
-enum : int { kOutF32 = 0, kOutBf16Bias = 1, kOutF32Add = 2 };
 
 struct GemmArgs {
   int M, N;                // valid output rows / columns per batch item z
@@ -107,8 +110,8 @@ template <bool A_MN, bool B_MN, int OUT, int BN>
 __global__ void __launch_bounds__(192, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mB0,
                    const __grid_constant__ CUtensorMap mA1, const __grid_constant__ CUtensorMap mB1,
-                   const GemmArgs g) {
-  using C = TcCfg<BN>;
+                   const __grid_constant__ CUtensorMap mC, const GemmArgs g) {
+  using C = TcCfg<BN, OUT>;
   constexpr int NSTG = C::NSTG;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ int abort_flag_s;
@@ -116,7 +119,8 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* abort_flag = &abort_flag_s;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t ring = (raw + 1023u) & ~1023u;  // 128-byte swizzle: 1024-byte aligned tiles
-  const uint32_t bar_full = ring + NSTG * C::STAGE, bar_empty = bar_full + 8 * NSTG;
+  const uint32_t out_stage = ring + NSTG * C::STAGE;  // 1024-byte aligned
+  const uint32_t bar_full = out_stage + C::OUT_STAGE, bar_empty = bar_full + 8 * NSTG;
   const uint32_t bar_tfull = bar_empty + 8 * NSTG, bar_tempty = bar_tfull + 16;
   const uint32_t tslot = bar_tempty + 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -244,8 +248,56 @@ __global__ void __launch_bounds__(192, 1)
       const bool row_ok = row < g.M;
       const bool empty_k = w.kb_hi == w.kb_lo;
       const int n_base = w.n_base * BN;
+      if constexpr (OUT == kOutBf16Bias) {
+        // bf16 (+ bias) through shared memory and TMA stores: the warp's 32 rows x
+        // 128 columns at a time as two 32 x 64 boxes in the 128-byte swizzled layout
+        // (16-byte chunk j of row r at chunk j ^ (r % 8)); the TMA engine writes
+        // whole row segments and drops rows / columns past the output's extent.
+        const uint32_t stg = out_stage + (uint32_t)q * 8192;
+#pragma unroll 1
+        for (int hh = 0; hh < BN / 128; ++hh) {
+          if (lane == 0) bulk_wait_read_all();  // the previous boxes left this buffer
+          __syncwarp();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];  // columns n_base + 128 hh + 32 c .. + 31 of this thread's row
+            tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN + hh * 128 + c * 32), r);
+            tmem_wait_ld();
+            const int n0 = n_base + hh * 128 + c * 32;
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              float x0 = empty_k ? 0.f : __uint_as_float(r[2 * j]);
+              float x1 = empty_k ? 0.f : __uint_as_float(r[2 * j + 1]);
+              if (g.bias && n0 + 2 * j + 1 < g.N) {
+                x0 += __ldg(g.bias + n0 + 2 * j);
+                x1 += __ldg(g.bias + n0 + 2 * j + 1);
+              }
+              pk[j] = pack_bf16x2(x0, x1);
+            }
+            const uint32_t rowb = stg + (uint32_t)(c >> 1) * 4096 + (uint32_t)lane * 128;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t chunk = (uint32_t)(((c & 1) * 4 + k) ^ (lane & 7));
+              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + chunk * 16),
+                           "r"(pk[4 * k]), "r"(pk[4 * k + 1]), "r"(pk[4 * k + 2]), "r"(pk[4 * k + 3])
+                           : "memory");
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the TMA engine
+          __syncwarp();
+          if (lane == 0) {
+            const int mr = w.m_base + q * 32;
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+              const int nc = n_base + hh * 128 + b * 64;
+              if (nc < g.N && mr < g.M) tma_store_2d(&mC, nc, mr, stg + (uint32_t)b * 4096);
+            }
+            bulk_commit();
+          }
+        }
+      } else {
       float* cf = static_cast<float*>(g.C) + w.z * g.c_stride_z + (size_t)row * g.ldc;
-      __nv_bfloat16* cb = static_cast<__nv_bfloat16*>(g.C) + w.z * g.c_stride_z + (size_t)row * g.ldc;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];  // columns n_base + 32c .. + 31 of this thread's row
@@ -270,31 +322,16 @@ __global__ void __launch_bounds__(192, 1)
               asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(cf + n0 + j), "r"(v[j]),
                            "r"(v[j + 1]), "r"(v[j + 2]), "r"(v[j + 3])
                            : "memory");
-          } else if (OUT == kOutF32Add) {
+          } else {
 #pragma unroll
             for (int j = 0; j < 16; j += 4)
               asm volatile("red.global.add.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(cf + n0 + j),
                            "f"(__uint_as_float(v[j])), "f"(__uint_as_float(v[j + 1])),
                            "f"(__uint_as_float(v[j + 2])), "f"(__uint_as_float(v[j + 3]))
                            : "memory");
-          } else {
-            uint32_t pk[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              float x0 = __uint_as_float(v[2 * j]), x1 = __uint_as_float(v[2 * j + 1]);
-              if (g.bias) {
-                x0 += __ldg(g.bias + n0 + 2 * j);
-                x1 += __ldg(g.bias + n0 + 2 * j + 1);
-              }
-              pk[j] = pack_bf16x2(x0, x1);
-            }
-#pragma unroll
-            for (int j = 0; j < 8; j += 4)
-              asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(cb + n0 + 2 * j),
-                           "r"(pk[j]), "r"(pk[j + 1]), "r"(pk[j + 2]), "r"(pk[j + 3])
-                           : "memory");
           }
         }
+      }
       }
       // accumulator buffer a may be overwritten by unit i + 2
       tc_fence_before();
@@ -303,6 +340,7 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
 
+  if (OUT == kOutBf16Bias && warp >= 2 && lane == 0) bulk_wait_all();  // output stores done
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -364,8 +402,9 @@ int num_sms() {
 // grid: one CTA per SM (at most one per unit, at most max_ctas if > 0)
 template <bool A_MN, bool B_MN, int OUT, int BN>
 int launch_tc(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1,
-              const CUtensorMap& b1, GemmArgs g, cudaStream_t s, int max_ctas = 0) {
-  using C = TcCfg<BN>;
+              const CUtensorMap& b1, const CUtensorMap& c, GemmArgs g, cudaStream_t s,
+              int max_ctas = 0) {
+  using C = TcCfg<BN, OUT>;
   auto kern = tc_gemm_kernel<A_MN, B_MN, OUT, BN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return (int)e;
@@ -377,7 +416,7 @@ int launch_tc(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a
   if (max_ctas > 0 && max_ctas < cap) cap = max_ctas;
   const int grid = (int)(units < cap ? units : cap);
   if (grid == 0) return 0;
-  kern<<<grid, 192, C::SMEM, s>>>(a0, b0, a1, b1, g);
+  kern<<<grid, 192, C::SMEM, s>>>(a0, b0, a1, b1, c, g);
   return (int)cudaGetLastError();
 }
 
@@ -423,20 +462,22 @@ int launch_dR_tc(const void* h_seq, const void* h0b, const void* dG, float* dR, 
   int ks = num_sms() / (tiles > 0 ? tiles : 1);
   if (ks > nkb / 16) ks = nkb / 16;
   g.ksplit = ks > 1 ? ks : 1;
-  if (g.ksplit == 1) return launch_tc<true, true, kOutF32, 256>(a0, b0, a1, b0, g, s);
+  if (g.ksplit == 1) return launch_tc<true, true, kOutF32, 256>(a0, b0, a1, b0, a0, g, s);
   if (cudaMemsetAsync(dR, 0, (size_t)NH * Dh * GD * sizeof(float), s) != cudaSuccess)
     return (int)cudaErrorInvalidValue;
-  return launch_tc<true, true, kOutF32Add, 256>(a0, b0, a1, b0, g, s);
+  return launch_tc<true, true, kOutF32Add, 256>(a0, b0, a1, b0, a0, g, s);
 }
 
 int launch_input_proj_tc(const void* x, const void* W, const float* bias, void* Wx, int M, int N,
                          int K, int* status, unsigned long long timeout_ns, cudaStream_t s,
                          int max_ctas) {
   const bool wide = N >= 256;
-  CUtensorMap a0, b0;
+  CUtensorMap a0, b0, c0;
   int e = make_map(&a0, x, (uint64_t)M, (uint64_t)K, (uint64_t)K, 64, 128);
   if (e) return e;
   e = make_map(&b0, W, (uint64_t)N, (uint64_t)K, (uint64_t)K, 64, wide ? 256 : 128);
+  if (e) return e;
+  e = make_map(&c0, Wx, (uint64_t)M, (uint64_t)N, (uint64_t)N, 64, 32);  // output boxes
   if (e) return e;
   GemmArgs g{};
   g.M = M;
@@ -451,8 +492,8 @@ int launch_input_proj_tc(const void* x, const void* W, const float* bias, void* 
   g.bias = bias;
   g.status = status;
   g.timeout_ns = timeout_ns;
-  if (wide) return launch_tc<false, false, kOutBf16Bias, 256>(a0, b0, a0, b0, g, s, max_ctas);
-  return launch_tc<false, false, kOutBf16Bias, 128>(a0, b0, a0, b0, g, s, max_ctas);
+  if (wide) return launch_tc<false, false, kOutBf16Bias, 256>(a0, b0, a0, b0, c0, g, s, max_ctas);
+  return launch_tc<false, false, kOutBf16Bias, 128>(a0, b0, a0, b0, c0, g, s, max_ctas);
 }
 
 }  // namespace srnn
