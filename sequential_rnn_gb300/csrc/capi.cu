@@ -47,14 +47,14 @@ struct StepRow {
   float ns[5];
 };
 const StepRow kStepTable[] = {
-    {RNN_LSTM, 32, {329, 398, 385, 0, 0}},        {RNN_LSTM, 64, {435, 417, 400, 421, 0}},
-    {RNN_LSTM, 128, {0, 535, 440, 446, 499}},     {RNN_LSTM, 256, {0, 0, 771, 610, 704}},
-    {RNN_LSTM, 768, {0, 0, 0, 0, 1930}},          {RNN_GRU, 32, {328, 389, 0, 0, 0}},
-    {RNN_GRU, 64, {378, 415, 428, 0, 0}},         {RNN_GRU, 128, {688, 501, 494, 506, 0}},
-    {RNN_GRU, 256, {0, 970, 753, 713, 781}},      {RNN_GRU, 768, {0, 0, 0, 0, 1990}},
-    {RNN_SLSTM, 32, {529, 596, 609, 0, 0}},       {RNN_SLSTM, 64, {699, 642, 642, 708, 0}},
-    {RNN_SLSTM, 128, {0, 984, 801, 808, 845}},    {RNN_SLSTM, 256, {0, 0, 1756, 1473, 1511}},
-    {RNN_SLSTM, 768, {0, 0, 0, 0, 1998}},
+    {RNN_LSTM, 32, {332, 400, 388, 0, 0}},        {RNN_LSTM, 64, {438, 416, 405, 415, 0}},
+    {RNN_LSTM, 128, {0, 533, 442, 455, 505}},     {RNN_LSTM, 256, {0, 0, 776, 617, 708}},
+    {RNN_LSTM, 768, {0, 0, 0, 0, 1933}},          {RNN_GRU, 32, {334, 393, 0, 0, 0}},
+    {RNN_GRU, 64, {377, 417, 428, 0, 0}},         {RNN_GRU, 128, {697, 506, 498, 509, 0}},
+    {RNN_GRU, 256, {0, 970, 753, 715, 791}},      {RNN_GRU, 768, {0, 0, 0, 0, 1996}},
+    {RNN_SLSTM, 32, {403, 452, 464, 0, 0}},       {RNN_SLSTM, 64, {571, 507, 510, 576, 0}},
+    {RNN_SLSTM, 128, {0, 897, 679, 690, 727}},    {RNN_SLSTM, 256, {0, 0, 1425, 1128, 1172}},
+    {RNN_SLSTM, 768, {0, 0, 0, 0, 2013}},
 };
 constexpr int kClusterSizes[5] = {1, 2, 4, 8, 16};
 constexpr int kMaxSmemOptin = 232448;       // dynamic shared memory per CTA (sm_103)
