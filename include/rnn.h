@@ -128,6 +128,28 @@ int rnn_bwd(const rnn_desc_t* desc, const void* R, const float* h0, const float*
             float* dh0, float* dc0, float* dn0, void* workspace, size_t workspace_bytes,
             void* stream);
 
+/* rnn_fwd for a sequence in (pinned) host memory: Wx_host [T, B, NH, G*Dh] is
+ * read from and h_seq_host [T, B, NH, Dh] written to host memory while the
+ * recurrence runs.  Time is cut into chunks of `chunk` steps (0 = automatic:
+ * T/4, at least 64); chunk c's Wx is copied in on a copy stream while chunk
+ * c-1 runs, and chunk c-1's h_seq is copied out on another, so only the first
+ * chunk's upload and the last chunk's download are not hidden behind the
+ * recurrence.  Each chunk continues from the previous chunk's final state,
+ * which gives results identical to one rnn_fwd over all T steps.  R, bias,
+ * the initial and final states and the workspace are device memory (as for
+ * rnn_fwd); no RNN_FLAG_TRAIN.  The copy streams and events are created on a
+ * device's first call and kept (host resources); the enqueue is serialised
+ * across host threads; `stream` waits for all of it.  Alignment: R 16 bytes,
+ * fp32 pointers 4, workspace 256 and >= rnn_fwd_host_workspace_size() bytes
+ * (status word at offset 0, then two Wx chunks, two h_seq chunks and the
+ * carried states).  Host memory that is not pinned still works, without the
+ * overlap. */
+size_t rnn_fwd_host_workspace_size(const rnn_desc_t* desc, int32_t chunk);
+int rnn_fwd_host(const rnn_desc_t* desc, int32_t chunk, const void* Wx_host, const void* R,
+                 const float* bias, const float* h0, const float* c0, const float* n0,
+                 const float* m0, void* h_seq_host, float* hT, float* cT, float* nT, float* mT,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
 /* Input projection, the dense step in front of the recurrence (FlashRNN blog
  * page, register-caching paragraph: only the recurrent weight R has to stay on
  * chip through the sequential time loop; the input weight is applied to all

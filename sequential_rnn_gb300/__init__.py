@@ -21,7 +21,8 @@ from ._lib import (CELLS, DTYPES, RNN_BF16, RNN_F32, RNN_FLAG_H_BF16, RNN_FLAG_T
 __all__ = ["RnnError", "make_desc", "rnn_workspace_size", "rnn_stash_size", "rnn_fwd", "rnn_bwd",
            "rnn_read_status", "rnn_sync_floor", "rnn_fwd_config", "rnn_status_str", "rnn_fwd_noalloc",
            "rnn_input_proj", "rnn_stack_workspace_size", "rnn_stack_fwd", "forward", "backward",
-           "input_proj", "stack_forward", "rnn_plan", "GATES"]
+           "input_proj", "stack_forward", "rnn_plan", "rnn_fwd_host_workspace_size",
+           "rnn_fwd_host", "forward_host", "GATES"]
 
 GATES = {"lstm": 4, "gru": 3, "slstm": 4}
 
@@ -44,6 +45,17 @@ def _ptr(t):
         raise TypeError("expected a torch.Tensor or None")
     if t.numel() and not t.is_cuda:
         raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
+
+
+def _host_ptr(t):
+    """Pointer of a contiguous host (preferably pinned) tensor."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError("expected a host tensor")
     if not t.is_contiguous():
         raise ValueError("tensor must be contiguous")
     return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
@@ -129,6 +141,19 @@ def rnn_plan(desc: rnn_desc_t, L: int = 1, sms: int = 0) -> dict:
     if st:
         raise RnnError(st, "rnn_plan")
     return dict(zip(("cluster", "chunk", "ctas", "waves", "us"), list(out)))
+
+
+def rnn_fwd_host_workspace_size(desc: rnn_desc_t, chunk: int = 0) -> int:
+    return int(_lib.load().rnn_fwd_host_workspace_size(ctypes.byref(desc), int(chunk)))
+
+
+def rnn_fwd_host(desc, chunk, Wx_host, R, bias, h0, c0, n0, m0, h_seq_host, hT, cT, nT, mT,
+                 workspace, stream=None) -> int:
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return int(_lib.load().rnn_fwd_host(
+        ctypes.byref(desc), int(chunk), _host_ptr(Wx_host), _ptr(R), _ptr(bias), _ptr(h0),
+        _ptr(c0), _ptr(n0), _ptr(m0), _host_ptr(h_seq_host), _ptr(hT), _ptr(cT), _ptr(nT),
+        _ptr(mT), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def rnn_read_status(workspace, stream=None) -> int:
@@ -274,4 +299,37 @@ def stack_forward(cell: str, x, W_ih0, W_ih, b_ih, R, bias=None, h0=None, c0=Non
         dst = rnn_read_status(ws, stream)
         if dst:
             raise RnnError(dst, "rnn_stack_fwd (device)")
+    return out
+
+
+def forward_host(cell: str, Wx_host, R, bias=None, h0=None, c0=None, n0=None, m0=None, *,
+                 h_seq_host=None, chunk=0, cluster=0, workspace=None, stream=None, check=True):
+    """rnn_fwd_host: Wx_host [T,B,NH,G*Dh] and h_seq in pinned host memory, the
+    copies pipelined with the recurrence over time chunks.  R and the states
+    live on the device.  Returns h_seq (host) and the final states (device)."""
+    T, B, NH, _ = Wx_host.shape
+    Dh = R.shape[1]
+    desc = make_desc(cell, _dtype_name(Wx_host), T, B, NH, Dh, 0, cluster)
+    dev = R.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    if h_seq_host is None:
+        h_seq_host = torch.empty((T, B, NH, Dh), dtype=Wx_host.dtype, pin_memory=True)
+    out = {"desc": desc, "h_seq": h_seq_host, "hT": torch.empty((B, NH, Dh), **f32)}
+    if cell != "gru":
+        out["cT"] = torch.empty((B, NH, Dh), **f32)
+    if cell == "slstm":
+        out["nT"] = torch.empty((B, NH, Dh), **f32)
+        out["mT"] = torch.empty((B, NH, Dh), **f32)
+    need = max(rnn_fwd_host_workspace_size(desc, chunk), 256)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    out["workspace"] = workspace
+    st = rnn_fwd_host(desc, chunk, Wx_host, R, bias, h0, c0, n0, m0, h_seq_host, out["hT"],
+                      out.get("cT"), out.get("nT"), out.get("mT"), workspace, stream)
+    if st:
+        raise RnnError(st, "rnn_fwd_host")
+    if check:
+        dst = rnn_read_status(workspace, stream)
+        if dst:
+            raise RnnError(dst, "rnn_fwd_host (device)")
     return out

@@ -26,7 +26,8 @@ DTYPES = {"f32": RNN_F32, "bf16": RNN_BF16}
 # Every symbol include/rnn.h declares (checked by the CPU tests).
 EXPORTS = ("rnn_workspace_size", "rnn_stash_size", "rnn_fwd", "rnn_bwd", "rnn_read_status",
            "rnn_sync_floor", "rnn_fwd_config", "rnn_status_str", "rnn_fwd_noalloc",
-           "rnn_input_proj", "rnn_stack_workspace_size", "rnn_stack_fwd", "rnn_plan")
+           "rnn_input_proj", "rnn_stack_workspace_size", "rnn_stack_fwd", "rnn_plan",
+           "rnn_fwd_host_workspace_size", "rnn_fwd_host")
 
 
 class rnn_desc_t(ctypes.Structure):
@@ -54,6 +55,8 @@ _SIGS = {
     "rnn_stack_workspace_size": (_SZ, [_DESC, ctypes.c_int32, ctypes.c_int32]),
     "rnn_stack_fwd": (_I, [_DESC] + [ctypes.c_int32] * 3 + [_P] * 16 + [_SZ, _P]),
     "rnn_plan": (_I, [_DESC, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
+    "rnn_fwd_host_workspace_size": (_SZ, [_DESC, ctypes.c_int32]),
+    "rnn_fwd_host": (_I, [_DESC, ctypes.c_int32] + [_P] * 13 + [_SZ, _P]),
 }
 
 _lib = None

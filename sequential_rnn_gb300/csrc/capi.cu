@@ -592,6 +592,161 @@ int rnn_stack_fwd(const rnn_desc_t* d, int32_t L, int32_t Din, int32_t chunk, co
   return err;
 }
 
+// ------------------------------------------------- host-memory forward --
+int host_chunk(const rnn_desc_t* d, int chunk) {
+  if (chunk > 0) return chunk;
+  const int c = (d->T + 3) / 4;  // four chunks: the first copy-in is the only one not hidden
+  return c < 64 ? 64 : c;
+}
+
+size_t rnn_fwd_host_workspace_size(const rnn_desc_t* d, int32_t chunk) {
+  if (check_desc(d) != RNN_OK || chunk < 0) return 0;
+  const int tc0 = host_chunk(d, chunk);
+  const size_t tc = (size_t)(tc0 < d->T ? tc0 : (d->T > 0 ? d->T : 1));
+  const size_t e = d->dtype == RNN_BF16 ? 2 : 4, G = gates_of(d->cell);
+  const size_t rows = (size_t)d->B * d->NH;
+  size_t o = kStatusBytes;
+  o += 2 * align_up(tc * rows * G * d->Dh * e, 256);                      // Wx chunks
+  o += 2 * align_up(tc * rows * d->Dh * e, 256);                          // h_seq chunks
+  o += 2 * (size_t)state_arrays(d->cell) * align_up(rows * d->Dh * 4, 256);  // carried states
+  return o;
+}
+
+int rnn_fwd_host(const rnn_desc_t* d, int32_t chunk, const void* Wx_host, const void* R,
+                 const float* bias, const float* h0, const float* c0, const float* n0,
+                 const float* m0, void* h_seq_host, float* hT, float* cT, float* nT, float* mT,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_desc(d);
+  if (st != RNN_OK) return st;
+  if (chunk < 0) return RNN_ERR_INVALID_ARG;
+  if (d->flags & RNN_FLAG_TRAIN) return RNN_ERR_UNSUPPORTED;
+  if (d->B == 0 || d->NH == 0) return RNN_OK;
+  Plan pl;
+  if ((st = make_plan(d, &pl)) != RNN_OK) return st;
+  if (workspace == nullptr || workspace_bytes < rnn_fwd_host_workspace_size(d, chunk))
+    return RNN_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return RNN_ERR_MISALIGNED;
+  const float* fp[] = {bias, h0, c0, n0, m0, hT, cT, nT, mT};
+  for (const float* q : fp)
+    if (!aligned(q, 4)) return RNN_ERR_MISALIGNED;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const size_t nstate = (size_t)d->B * d->NH * d->Dh;
+  const int ns = state_arrays(d->cell);
+  const float* init[4] = {h0, c0, n0, m0};
+  float* fin[4] = {hT, cT, nT, mT};
+  auto slot = [&](int k) { return k < ns ? k : -1; };
+  if (d->T == 0) {
+    for (int k = 0; k < 4; ++k)
+      if (slot(k) >= 0 && (st = copy_state(fin[k], init[k], nstate, cs)) != RNN_OK) return st;
+    return RNN_OK;
+  }
+  if (Wx_host == nullptr || R == nullptr || h_seq_host == nullptr) return RNN_ERR_INVALID_ARG;
+  if (!aligned(R, 16)) return RNN_ERR_MISALIGNED;
+
+  const int tch = host_chunk(d, chunk);
+  const size_t e = d->dtype == RNN_BF16 ? 2 : 4, G = gates_of(d->cell);
+  const size_t rows = (size_t)d->B * d->NH;
+  const size_t wx_step = rows * G * d->Dh * e, h_step = rows * d->Dh * e;
+  const size_t tcmax = (size_t)(tch < d->T ? tch : d->T);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws);
+  size_t o = kStatusBytes;
+  uint8_t* wxb[2];
+  uint8_t* hb[2];
+  for (int b = 0; b < 2; ++b) {
+    wxb[b] = ws + o;
+    o += align_up(tcmax * wx_step, 256);
+  }
+  for (int b = 0; b < 2; ++b) {
+    hb[b] = ws + o;
+    o += align_up(tcmax * h_step, 256);
+  }
+  float* sbuf[2][4] = {};
+  for (int b = 0; b < 2; ++b)
+    for (int k = 0; k < ns; ++k) {
+      sbuf[b][k] = reinterpret_cast<float*>(ws + o);
+      o += align_up(nstate * 4, 256);
+    }
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RNN_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lock(g_stack_mu);
+  LayerStreams* ls = nullptr;
+  if ((st = layer_streams(dev, &ls)) != RNN_OK) return st;
+  // copy-in on stream 0, copy-out on stream 1; the recurrence on the caller's stream.
+  // events: ev[b] = chunk copied in, ev[2 + b] = chunk computed, ev[4 + b] = chunk copied out
+  cudaStream_t sin = ls->s[0], sout = ls->s[1];
+  if (cudaMemsetAsync(status, 0, sizeof(int), cs) != cudaSuccess ||
+      cudaEventRecord(ls->fork, cs) != cudaSuccess ||
+      cudaStreamWaitEvent(sin, ls->fork, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(sout, ls->fork, 0) != cudaSuccess)
+    return RNN_ERR_LAUNCH;
+  const int nch = (d->T + tch - 1) / tch;
+  int err = RNN_OK;
+  for (int c = 0; c < nch && err == RNN_OK; ++c) {
+    const int b = c & 1;
+    const size_t t0 = (size_t)c * tch;
+    const int tc = (int)((size_t)d->T - t0 < (size_t)tch ? (size_t)d->T - t0 : (size_t)tch);
+    // in: Wx of chunk c once chunk c-2 no longer reads the buffer
+    if ((c >= 2 && cudaStreamWaitEvent(sin, ls->ev[2 + b], 0) != cudaSuccess) ||
+        cudaMemcpyAsync(wxb[b], static_cast<const uint8_t*>(Wx_host) + t0 * wx_step,
+                        (size_t)tc * wx_step, cudaMemcpyHostToDevice, sin) != cudaSuccess ||
+        cudaEventRecord(ls->ev[b], sin) != cudaSuccess) {
+      err = RNN_ERR_LAUNCH;
+      break;
+    }
+    // compute: the recurrence over chunk c, from chunk c-1's final state
+    if (cudaStreamWaitEvent(cs, ls->ev[b], 0) != cudaSuccess ||
+        (c >= 2 && cudaStreamWaitEvent(cs, ls->ev[4 + b], 0) != cudaSuccess)) {
+      err = RNN_ERR_LAUNCH;
+      break;
+    }
+    rnn_desc_t dc = *d;
+    dc.T = tc;
+    FwdParams p = base_params(&dc, pl);
+    p.Wx = wxb[b];
+    p.R = R;
+    p.bias = bias;
+    const float* sin_st[4];
+    float* sout_st[4];
+    for (int k = 0; k < 4; ++k) {
+      const int q = slot(k);
+      sin_st[k] = q < 0 ? nullptr : (c == 0 ? init[k] : sbuf[(c - 1) & 1][q]);
+      sout_st[k] = q < 0 ? nullptr : (c == nch - 1 ? fin[k] : sbuf[c & 1][q]);
+    }
+    p.h0 = sin_st[0];
+    p.c0 = d->cell == RNN_GRU ? nullptr : sin_st[1];
+    p.n0 = sin_st[2];
+    p.m0 = sin_st[3];
+    p.hT = sout_st[0];
+    p.cT = d->cell == RNN_GRU ? nullptr : sout_st[1];
+    p.nT = sout_st[2];
+    p.mT = sout_st[3];
+    p.h_seq = hb[b];
+    p.status = status;
+    const int le = launch_forward(&dc, pl, p, cs, false, nullptr);
+    if (le != 0 || cudaEventRecord(ls->ev[2 + b], cs) != cudaSuccess) {
+      err = le != 0 ? map_launch_error(le) : RNN_ERR_LAUNCH;
+      break;
+    }
+    // out: h_seq of chunk c
+    if (cudaStreamWaitEvent(sout, ls->ev[2 + b], 0) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<uint8_t*>(h_seq_host) + t0 * h_step, hb[b], (size_t)tc * h_step,
+                        cudaMemcpyDeviceToHost, sout) != cudaSuccess ||
+        cudaEventRecord(ls->ev[4 + b], sout) != cudaSuccess) {
+      err = RNN_ERR_LAUNCH;
+      break;
+    }
+  }
+  // the caller's stream waits for both copy streams (also after an error)
+  if (cudaEventRecord(ls->done[0], sin) != cudaSuccess ||
+      cudaEventRecord(ls->done[1], sout) != cudaSuccess ||
+      cudaStreamWaitEvent(cs, ls->done[0], 0) != cudaSuccess ||
+      cudaStreamWaitEvent(cs, ls->done[1], 0) != cudaSuccess)
+    err = RNN_ERR_LAUNCH;
+  return err;
+}
+
 int rnn_plan(const rnn_desc_t* d, int32_t L, int32_t sms, int32_t* out5) {
   int st = check_desc(d);
   if (st != RNN_OK) return st;

@@ -249,3 +249,39 @@ def test_plan_for_stacked_layers(lib):
     d = _desc(Dh=64, NH=12, B=16, T=1024)
     assert lib.rnn_stack_workspace_size(ctypes.byref(d), 3, 0) == \
         lib.rnn_stack_workspace_size(ctypes.byref(d), 3, out[1])
+
+
+def _fwd_host(lib, desc=None, chunk=0, wx=0x1000, r=0x2000, hseq=0x3000, ws=0x10000,
+              ws_bytes=None):
+    P = ctypes.c_void_p
+    desc = desc or _desc()
+    if ws_bytes is None:
+        ws_bytes = lib.rnn_fwd_host_workspace_size(ctypes.byref(desc), max(chunk, 0))
+    return lib.rnn_fwd_host(ctypes.byref(desc), chunk, P(wx) if wx else None,
+                            P(r) if r else None, None, None, None, None, None,
+                            P(hseq) if hseq else None, None, None, None, None,
+                            P(ws) if ws else None, ws_bytes, None)
+
+
+def test_fwd_host_workspace_size(lib):
+    d = _desc(T=100, B=4, NH=2, Dh=64)   # LSTM bf16
+    al = lambda v: (v + 255) // 256 * 256
+    rows = 4 * 2
+    for chunk, tc in ((0, 64), (10, 10), (500, 100)):
+        want = 256 + 2 * al(tc * rows * 4 * 64 * 2) + 2 * al(tc * rows * 64 * 2) + 2 * 2 * al(rows * 64 * 4)
+        assert lib.rnn_fwd_host_workspace_size(ctypes.byref(d), chunk) == want, chunk
+    assert lib.rnn_fwd_host_workspace_size(ctypes.byref(d), -1) == 0
+
+
+def test_fwd_host_argument_checks(lib):
+    assert _fwd_host(lib, chunk=-1, ws_bytes=1 << 30) == 1
+    assert _fwd_host(lib, desc=_desc(flags=1)) == 2          # no training stash
+    assert _fwd_host(lib, desc=_desc(Dh=48)) == 2
+    assert _fwd_host(lib, ws=0) == 1
+    assert _fwd_host(lib, ws_bytes=256) == 1
+    assert _fwd_host(lib, ws=0x10010) == 3
+    assert _fwd_host(lib, wx=0) == 1
+    assert _fwd_host(lib, hseq=0) == 1
+    assert _fwd_host(lib, r=0) == 1
+    assert _fwd_host(lib, r=0x2008) == 3
+    assert _fwd_host(lib, desc=_desc(B=0)) == 0
