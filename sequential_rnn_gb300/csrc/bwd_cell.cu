@@ -443,18 +443,11 @@ int launch_t(const BwdParams& p_in, cudaStream_t s, bool query_only, LaunchInfo*
   p.CS = K::CS;
   p.U = K::U;
   auto kern = bwd_cell_kernel<CELL, DH>;
-  int dev = 0, max_smem = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if (K::TOTAL > (uint32_t)max_smem) return (int)cudaErrorInvalidConfiguration;
   const int grid = p.NH * p.nbslices * K::CS;
   if (info) *info = LaunchInfo{grid, K::NTH, K::CS, kNB, (int)K::TOTAL, 500 + CELL * 100 + DH / 32};
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::TOTAL);
-  if (e != cudaSuccess) return (int)e;
-  if (K::CS > 8) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return (int)e;
-  }
+  static int prepared[64][5];
+  const int e = prepare_launch(prepared, kern, K::TOTAL, K::NTH, K::CS);
+  if (e != 0) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(K::NTH);
@@ -467,12 +460,6 @@ int launch_t(const BwdParams& p_in, cudaStream_t s, bool query_only, LaunchInfo*
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = K::CS > 1 ? 1 : 0;
-  if (K::CS > 1) {
-    int ncl = 0;
-    e = cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg);
-    if (e != cudaSuccess) return (int)e;
-    if (ncl < 1) return -1;
-  }
   if (query_only) return 0;
   return (int)cudaLaunchKernelEx(&cfg, kern, p);
 }

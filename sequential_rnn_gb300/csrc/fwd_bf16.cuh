@@ -748,19 +748,12 @@ int launch_fwd_bf16_v(const FwdParams& p_in, cudaStream_t stream, bool query_onl
   const int NW = p.U / UG;
   const int threads = NW * 32;
   if (p.U % UG != 0 || NW < 1 || threads > C::MAXT) return (int)cudaErrorInvalidConfiguration;
-  int dev = 0, max_smem = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   const uint32_t smem = fwd_smem_layout<C>(p.U).total;
-  if (smem > (uint32_t)max_smem) return (int)cudaErrorInvalidConfiguration;
   const int grid = p.NH * p.nbslices * p.CS;
   if (info) *info = LaunchInfo{grid, threads, p.CS, C::NB, (int)smem, CELL * 100 + DH / 32 + 50 * HS};
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return (int)e;
-  if (p.CS > 8) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return (int)e;
-  }
+  static int prepared[64][5];
+  const int e = prepare_launch(prepared, kern, smem, threads, p.CS);
+  if (e != 0) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(threads);
@@ -773,12 +766,6 @@ int launch_fwd_bf16_v(const FwdParams& p_in, cudaStream_t stream, bool query_onl
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.CS > 1 ? 1 : 0;
-  if (p.CS > 1) {
-    int ncl = 0;
-    e = cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg);
-    if (e != cudaSuccess) return (int)e;
-    if (ncl < 1) return -1;  // cluster cannot be co-scheduled
-  }
   if (query_only) return 0;
   return (int)cudaLaunchKernelEx(&cfg, kern, p);
 }

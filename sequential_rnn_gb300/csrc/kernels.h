@@ -6,6 +6,56 @@
 
 namespace srnn {
 
+// Once-per-device preparation of a kernel's launches: dynamic shared memory and
+// non-portable cluster-size attributes, and for clusters the co-scheduling
+// check.  Cached per (device, cluster size) in `state` (0 = not prepared,
+// 1 = ready, -1 = the cluster cannot be co-scheduled, else 1000 + CUDA error),
+// so launches after the first make no driver queries.  Preparing twice is
+// harmless, so concurrent first calls need no lock.
+template <class Kern>
+inline int prepare_launch(int (&state)[64][5], Kern kern, uint32_t smem, int threads, int cs) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return (int)cudaErrorInvalidDevice;
+  const int ci = cs <= 1 ? 0 : cs == 2 ? 1 : cs == 4 ? 2 : cs == 8 ? 3 : 4;
+  const bool cache = dev >= 0 && dev < 64;
+  if (cache && state[dev][ci] != 0)
+    return state[dev][ci] == 1 ? 0 : (state[dev][ci] == -1 ? -1 : state[dev][ci] - 1000);
+  int r = 0, max_smem = 0;
+  cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (smem > (uint32_t)max_smem) r = (int)cudaErrorInvalidConfiguration;
+  // the attribute is per kernel, shared by every cluster size (each with its own
+  // shared-memory need): allow all the device's opt-in amount the kernel's
+  // static shared memory leaves
+  if (r == 0) {
+    cudaFuncAttributes fa;
+    r = (int)cudaFuncGetAttributes(&fa, kern);
+    if (r == 0 && smem + fa.sharedSizeBytes > (size_t)max_smem) r = (int)cudaErrorInvalidConfiguration;
+    if (r == 0)
+      r = (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    max_smem - (int)fa.sharedSizeBytes);
+  }
+  if (r == 0 && cs > 8)
+    r = (int)cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (r == 0 && cs > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int ncl = 0;
+    r = (int)cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg);
+    if (r == 0 && ncl < 1) r = -1;  // the cluster cannot be co-scheduled
+  }
+  if (cache) state[dev][ci] = r == 0 ? 1 : (r == -1 ? -1 : r + 1000);
+  return r;
+}
+
 enum : int { kLSTM = 0, kGRU = 1, kSLSTM = 2 };
 enum : int { kStatusTimeout = 1 };  // bits of the device status word
 

@@ -406,8 +406,9 @@ int launch_tc(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a
               int max_ctas = 0) {
   using C = TcCfg<BN, OUT>;
   auto kern = tc_gemm_kernel<A_MN, B_MN, OUT, BN>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (e != cudaSuccess) return (int)e;
+  static int prepared[64][5];
+  const int e = prepare_launch(prepared, kern, C::SMEM, 192, 1);
+  if (e != 0) return e;
   g.tiles_m = (g.M + TBM - 1) / TBM;
   g.tiles_n = (g.N + BN - 1) / BN;
   const long long units = (long long)g.Z * g.tiles_m * g.tiles_n * g.ksplit;
