@@ -33,6 +33,20 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_exports_no_undeclared_c_symbols(lib):
+    """Every unmangled function the library exports is one the header declares."""
+    import shutil
+    import subprocess
+    from sequential_rnn_gb300 import _lib
+    if shutil.which("nm") is None:
+        pytest.skip("nm not available")
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = {f[2] for f in (l.split() for l in out.splitlines())
+                if len(f) == 3 and f[1] == "T" and not f[2].startswith(("_", "cuda", "cu"))}
+    assert exported == set(_declared_symbols()), exported ^ set(_declared_symbols())
+
+
 def _desc(**kw):
     from sequential_rnn_gb300._lib import rnn_desc_t
     d = dict(cell=0, dtype=1, T=8, B=4, NH=2, Dh=64, flags=0, cluster=0)
