@@ -50,7 +50,10 @@ template <int CELL, int DH, int UG, int NT, int KREG, int HS>
 struct FwdCfg {
   static constexpr int G = CELL == kGRU ? 3 : 4;
   static constexpr int GD = G * DH;
-  static constexpr int MT = UG * G / 16;  // m16 tiles per warp
+  // m16 tiles per warp; GRU with 8 units per warp pads its 24 gate rows to 32
+  static constexpr int MT = (UG * G + 15) / 16;
+  static constexpr int ROWS = UG * G;     // gate rows that exist (the rest is padding)
+  static constexpr int UGW = UG;          // hidden units per warp
   static constexpr int KS = DH / 16;      // k16 steps
   static constexpr int KSM = KS - KREG;   // k-steps whose A fragments live in smem
   static constexpr int NB = NT * 8;       // batch rows per CTA
@@ -76,10 +79,10 @@ struct FwdCfg {
   static constexpr int MAXT_R = (65536 / REG_EST) / 32 * 32;
   static constexpr int MAXT = MAXT_R < 17 * 32 ? MAXT_R : 17 * 32;
   static_assert(UG == 8 || UG == 16, "unit group");
-  static_assert(UG * G % 16 == 0, "gate rows per warp must fill m16 tiles");
+  static_assert(UG * G % 16 == 0 || (UG == 8 && G == 3), "gate rows per warp fill m16 tiles");
   static_assert(DH % 32 == 0, "Dh multiple of 32");
   static_assert(KREG >= 0 && KREG <= KS, "KREG");
-  static_assert(NTILE % 2 == 0, "Wx tiles come in pairs");
+  static_assert(NTILE % 2 == 0 || NTILE == 3, "Wx tiles come in pairs (or three: one x4 load)");
   // scale of gate g's preactivation: 1/2 for sigmoid gates on the fast path
   __host__ __device__ static constexpr float gate_scale(int g) {
     return HS ? 1.f
@@ -100,7 +103,7 @@ template <class C>
 __host__ __device__ inline FwdSmem fwd_smem_layout(int U) {
   constexpr int NS = C::PD;
   FwdSmem L;
-  const int NW = U / (C::MT * 16 / C::G);
+  const int NW = U / C::UGW;  // compute warps
   L.h = 0;
   uint32_t o = 2u * C::HPARTS * C::NB * C::HPB;
   o = (o + 127) & ~127u;
@@ -229,6 +232,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     uint32_t areg[MT][KREG > 0 ? KREG : 1][4];
     const uint32_t rf_warp = s_rf + (uint32_t)warp * MT * KSM * 512 + lane * 16;
     auto rval = [&](int k, int col, float sc) -> uint32_t {
+      if (col < 0) return 0u;
       const uint16_t v = Rb[(size_t)k * GD + col];
       if (sc == 1.f) return v;
       const __nv_bfloat16 x = __float2bfloat16_rn(__uint_as_float((uint32_t)v << 16) * sc);
@@ -238,8 +242,9 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     for (int mt = 0; mt < MT; ++mt) {
       const int ra = mt * 16 + (lane >> 2), rb = ra + 8;
       const int ga = ra / UG, gb = rb / UG;
-      const int ca = ga * DH + u0 + ub + (ra % UG);
-      const int cb = gb * DH + u0 + ub + (rb % UG);
+      // padding rows (GRU, 8 units per warp) get zero fragments
+      const int ca = ra < C::ROWS ? ga * DH + u0 + ub + (ra % UG) : -1;
+      const int cb = rb < C::ROWS ? gb * DH + u0 + ub + (rb % UG) : -1;
       const float sa = C::gate_scale(ga), sb = C::gate_scale(gb);
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
@@ -398,7 +403,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
           const uint32_t addr = stage + nt * 8 * WP + wx_off[q];
-          if (4 * q + 4 <= NTILE) {
+          if (4 * q + 4 <= NTILE || NTILE - 4 * q == 3) {
             uint32_t r4[4];
             ldmatrix_x4_trans(r4, addr);
 #pragma unroll
@@ -429,6 +434,10 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 A[mt][nt][q] = fmaf(C::gate_scale(g), x, sbias[g][us]);
               }
             }
+      if (C::ROWS < MT * 16) {  // padding rows (GRU, 8 units per warp): start at zero
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) A[MT - 1][nt][2] = A[MT - 1][nt][3] = 0.f;
+      }
       return true;
     };
     if (!dead && T > 0 && !prep()) dead = true;

@@ -113,7 +113,10 @@ int launch_fwd_bf16_gru(const FwdParams& p, int Dh, int NT, cudaStream_t s, bool
 int launch_fwd_bf16_slstm(const FwdParams& p, int Dh, int NT, int hsplit, cudaStream_t s,
                           bool query_only, LaunchInfo* info);
 // Units handled by one warp in the bf16 kernels (gate rows of one warp = UG * G).
-inline int bf16_unit_group(int cell) { return cell == kGRU ? 16 : 8; }
+// hidden units per warp of the bf16 forward variant for (cell, Dh, units per CTA)
+inline int bf16_unit_group(int cell, int Dh, int U) {
+  return cell == kGRU && (Dh > 128 || U > 64) ? 16 : 8;
+}
 
 // Empty-step kernel with the launch shape of a bf16/fp32 forward.
 int launch_sync_floor(const LaunchInfo& li, int T, int* status, cudaStream_t s);

@@ -28,9 +28,9 @@ struct StepRow {
 const StepRow kStepTable[] = {
     {RNN_LSTM, 32, {332, 400, 388, 0, 0}},        {RNN_LSTM, 64, {438, 416, 405, 415, 0}},
     {RNN_LSTM, 128, {0, 533, 442, 455, 505}},     {RNN_LSTM, 256, {0, 0, 776, 617, 708}},
-    {RNN_LSTM, 768, {0, 0, 0, 0, 1933}},          {RNN_GRU, 32, {334, 393, 0, 0, 0}},
-    {RNN_GRU, 64, {377, 417, 428, 0, 0}},         {RNN_GRU, 128, {697, 506, 498, 509, 0}},
-    {RNN_GRU, 256, {0, 970, 753, 715, 791}},      {RNN_GRU, 768, {0, 0, 0, 0, 1996}},
+    {RNN_LSTM, 768, {0, 0, 0, 0, 1933}},          {RNN_GRU, 32, {302, 381, 372, 0, 0}},
+    {RNN_GRU, 64, {405, 398, 387, 397, 0}},         {RNN_GRU, 128, {692, 543, 424, 431, 479}},
+    {RNN_GRU, 256, {0, 976, 753, 719, 783}},      {RNN_GRU, 768, {0, 0, 0, 0, 1971}},
     {RNN_SLSTM, 32, {403, 452, 464, 0, 0}},       {RNN_SLSTM, 64, {571, 507, 510, 576, 0}},
     {RNN_SLSTM, 128, {0, 897, 679, 690, 727}},    {RNN_SLSTM, 256, {0, 0, 1425, 1128, 1172}},
     {RNN_SLSTM, 768, {0, 0, 0, 0, 2013}},
@@ -50,7 +50,7 @@ bool hsplit_of(const rnn_desc_t* d) {
 // fixed latency chain plus tensor-pipe issue (8-cycle mma.sync per sub-partition).
 double model_step_ns(const rnn_desc_t* d, int cs, int unit_group) {
   const int G = gates_of(d->cell), U = d->Dh / cs, NW = U / unit_group;
-  const int per_warp = unit_group * G / 16 * (d->Dh / 16) * (hsplit_of(d) ? 2 : 1);
+  const int per_warp = (unit_group * G + 15) / 16 * (d->Dh / 16) * (hsplit_of(d) ? 2 : 1);
   const double w = (double)per_warp * ((NW + 3) / 4);
   const double floor_ns = cs == 1 ? 160.0 : 205.0 + 4.0 * cs;
   return floor_ns + 150.0 + 7.0 * w;
@@ -174,7 +174,7 @@ int make_plan(const rnn_desc_t* d, Plan* pl) {
     if (cs != 1 && cs != 2 && cs != 4 && cs != 8 && cs != 16) return RNN_ERR_UNSUPPORTED;
     if (d->Dh % cs) return RNN_ERR_UNSUPPORTED;
     const int U = d->Dh / cs;
-    if (U % bf16_unit_group(d->cell)) return RNN_ERR_UNSUPPORTED;
+    if (U % bf16_unit_group(d->cell, d->Dh, U)) return RNN_ERR_UNSUPPORTED;
     pl->f32 = false;
     pl->CS = cs;
     pl->U = U;
