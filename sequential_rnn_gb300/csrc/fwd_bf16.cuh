@@ -642,6 +642,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 
         // ---- publish h_t
         const uint32_t nbuf = s_h + (uint32_t)((t + 1) & 1) * NB * HPB;
+        uint32_t xv[4] = {0u, 0u, 0u, 0u};  // cluster: this lane's 16-byte chunk of h_t
         if (CL) {
           // stage this warp's cells, then ship 16-byte chunks to every cluster CTA
           // (this one included) and store the h_seq chunk
@@ -666,18 +667,12 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 }
               }
           __syncwarp();
-          uint32_t v[4];
-          lds128(v, stg + (uint32_t)x_c * 16);
+          lds128(xv, stg + (uint32_t)x_c * 16);
           if (send) {
             const uint32_t lbar = bar_h + 8 * ((t + 1) & 1);
             const uint32_t ldst = nbuf + x_dst;
-            for (int rk = x_r0; rk < CS; rk += RSTEP) st_async_v4(mapa(ldst, rk), v, mapa(lbar, rk));
+            for (int rk = x_r0; rk < CS; rk += RSTEP) st_async_v4(mapa(ldst, rk), xv, mapa(lbar, rk));
           }
-          if (x_store)
-            asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(hseq_x), "r"(v[0]), "r"(v[1]),
-                         "r"(v[2]), "r"(v[3])
-                         : "memory");
-          hseq_x += hseq_tstride;
         } else {
           // own cells into the next buffer (also at the last step: h_seq is stored
           // from there after the barrier)
@@ -703,6 +698,14 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
         }
         // ---- prime the next step's accumulators while other warps finish
         if (!EARLY_PREP && send && !prep()) dead = true;
+        if (CL) {
+          // this warp's h_seq chunk, after the exchange is on its way
+          if (x_store)
+            asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(hseq_x), "r"(xv[0]),
+                         "r"(xv[1]), "r"(xv[2]), "r"(xv[3])
+                         : "memory");
+          hseq_x += hseq_tstride;
+        }
       }
       if (!CL) {
         // h_t visible to every compute warp; a dead warp stops all of them together
