@@ -25,6 +25,8 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline int state_arrays(int cell) { return cell == RNN_LSTM ? 2 : (cell == RNN_GRU ? 1 : 4); }
 
 int check_desc(const rnn_desc_t* d);
+// sLSTM h operand of the bf16 forward: 0 bf16, 1 hi + lo operands, 2 hi + lo in one n8 tile
+int hsplit_mode(const rnn_desc_t* d);
 bool bf16_dh_supported(int Dh);
 
 // Launch plan of one forward: fp32 or bf16 path, CTAs per head (CS), units per

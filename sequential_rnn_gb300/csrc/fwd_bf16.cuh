@@ -56,15 +56,20 @@ struct FwdCfg {
   static constexpr int UGW = UG;          // hidden units per warp
   static constexpr int KS = DH / 16;      // k16 steps
   static constexpr int KSM = KS - KREG;   // k-steps whose A fragments live in smem
-  static constexpr int NB = NT * 8;       // batch rows per CTA
+  static constexpr int NB = NT * 8;       // rows of the h buffer per CTA (n8 tiles)
+  // HS = 1: h_{t-1} enters the MMA as a bf16 pair hi + lo (hi = bf16(h),
+  // lo = bf16(h - hi)) in two B operands.  HS = 2: the pair shares one n8
+  // tile -- rows 0-3 hold hi of four batch rows, rows 4-7 their lo -- so one
+  // MMA covers both and the two column halves are summed by a lane shuffle.
+  static constexpr int NBV = HS == 2 ? 4 : NB;  // batch rows per CTA
+  static_assert(HS != 2 || NT == 1, "hi/lo n-tile pairing uses one n8 tile");
   // h row pitch in bytes: 16-byte chunks per row odd -> ldmatrix conflict-free
   static constexpr int HPB = ((DH * 2 / 16) % 2 == 0) ? DH * 2 + 16 : DH * 2;
   static constexpr int NSLOT = UG == 16 ? 2 : 1;  // units per thread
   static constexpr int NE = NSLOT * NT * 2;       // (unit, batch) cells per thread
   static constexpr int NTILE = G * NSLOT;         // 8x8 Wx tiles per thread and n-tile
   static constexpr int NQ = (NTILE + 3) / 4;      // ldmatrix instructions for them
-  // HS: h_{t-1} enters the MMA as a bf16 pair hi + lo (hi = bf16(h), lo = bf16(h - hi))
-  static constexpr int HPARTS = HS ? 2 : 1;
+  static constexpr int HPARTS = HS == 1 ? 2 : 1;  // h buffer parts
   // Wx prefetch depth in steps (ring stages): >= ~2 us of steps ahead
   static constexpr int PD = DH >= 256 ? 4 : 8;
   // long k chains run as two interleaved accumulator sets
@@ -75,7 +80,7 @@ struct FwdCfg {
   static constexpr int STG_BYTES = STG_CH * 16;
   static_assert(32 % STG_CH == 0, "staging chunks must tile a warp");
   // register estimate per compute thread -> largest CTA the register file holds
-  static constexpr int REG_EST = MT * KREG * 4 + MT * NT * 8 + 88 + HS * NT * 8;
+  static constexpr int REG_EST = MT * KREG * 4 + MT * NT * 8 + 88 + (HS == 1) * NT * 8;
   static constexpr int MAXT_R = (65536 / REG_EST) / 32 * 32;
   static constexpr int MAXT = MAXT_R < 17 * 32 ? MAXT_R : 17 * 32;
   static_assert(UG == 8 || UG == 16, "unit group");
@@ -150,8 +155,10 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   // A cluster step is latency-bound (few warps per SM): two k chains and plain
   // fp32 tanh.  One CTA per head is throughput-bound: packed fp16x2 tanh.
   constexpr bool SPLITK = C::SPLITK || CL;
-  // hi/lo split over >= 8 k16 steps: hi and lo each on two chains (even/odd k pairs)
-  constexpr bool HS4 = HS && KS >= 8;
+  // HS = 1 (hi and lo as separate B operands) over >= 8 k16 steps: hi and lo
+  // each on two chains (even/odd k pairs).  HS = 2: hi and lo in one n8 tile.
+  constexpr bool HLO = HS == 1, HN = HS == 2;
+  constexpr bool HS4 = HLO && KS >= 8;
   constexpr bool PACKED_TANH = !CL;
   // One CTA per head (all warps meet at a barrier every step): the next step's
   // Wx is primed while this step's MMAs are in flight, in a second accumulator
@@ -166,8 +173,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   const int cid = blockIdx.x / CS;
   const int head = cid / p.nbslices, bslice = cid % p.nbslices;
   const int u0 = (int)crank * U;
-  const int b0 = bslice * NB;
-  const int nvalid = min(NB, B - b0);
+  const int b0 = bslice * C::NBV;
+  const int nvalid = min(C::NBV, B - b0);
 
   const FwdSmem L = fwd_smem_layout<C>(U);
   const uint32_t sbase = smem_u32(smem);
@@ -197,16 +204,22 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     }
   }
   // h_{-1} = bf16(h0) for all Dh units of this batch slice into buffer 0
+  // (HN: rows 4-7 take the residual parts of rows 0-3)
   for (int i = tid; i < NB * DH / 2; i += blockDim.x) {
     const int n = i / (DH / 2), j = 2 * (i % (DH / 2));
+    const int nb = HN ? (n & 3) : n;
     float v0 = 0.f, v1 = 0.f;
-    if (p.h0 != nullptr && n < nvalid) {
-      const float* src = p.h0 + ((size_t)(b0 + n) * NH + head) * DH + j;
+    if (p.h0 != nullptr && nb < nvalid) {
+      const float* src = p.h0 + ((size_t)(b0 + nb) * NH + head) * DH + j;
       v0 = src[0];
       v1 = src[1];
     }
+    if (HN && n >= 4) {
+      v0 -= bf16_round(v0);
+      v1 -= bf16_round(v1);
+    }
     *reinterpret_cast<uint32_t*>(smem + L.h + n * HPB + j * 2) = pack_bf16x2(v0, v1);
-    if (HS)
+    if (HLO)
       *reinterpret_cast<uint32_t*>(smem + L.h + hpart + n * HPB + j * 2) =
           pack_bf16x2(v0 - bf16_round(v0), v1 - bf16_round(v1));
   }
@@ -275,6 +288,12 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 #pragma unroll
       for (int g = 0; g < G; ++g)
         sbias[g][us] = C::gate_scale(g) * (p.bias ? p.bias[(size_t)head * GD + g * DH + j] : 0.f);
+      // HN: the lo columns (lanes with lane & 2) start from zero; the shuffle
+      // adds them onto the hi columns, which carry Wx and the bias
+      if (HN && (lane & 2)) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) sbias[g][us] = 0.f;
+      }
     }
     float st_c[NE], st_n[NE], st_m[NE], st_h[NE];
 #pragma unroll
@@ -284,7 +303,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int ei = (us * NT + nt) * 2 + e;
-          const int n = nt * 8 + 2 * (lane & 3) + e;
+          // HN: a lo-column lane mirrors the state of its hi partner (lane ^ 2)
+          const int n = (nt * 8 + 2 * (lane & 3) + e) & (HN ? 3 : 255);
           const int j = u0 + ub + (lane >> 2) + 8 * us;
           const size_t si = ((size_t)(b0 + n) * NH + head) * DH + j;
           const bool ok = n < nvalid;
@@ -486,13 +506,13 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
         const uint32_t hb = s_h + (uint32_t)(t & 1) * NB * HPB + lm_off;
 #pragma unroll
         for (int kp = 0; kp < KS / 2; ++kp) {
-          uint32_t bfr[NT][4], bfl[HS ? NT : 1][4];
+          uint32_t bfr[NT][4], bfl[HLO ? NT : 1][4];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) ldmatrix_x4(bfr[nt], hb + nt * 8 * HPB + kp * 64);
-          if (HS) {
+          if (HLO) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
-              ldmatrix_x4(bfl[HS ? nt : 0], hb + hpart + nt * 8 * HPB + kp * 64);
+              ldmatrix_x4(bfl[HLO ? nt : 0], hb + hpart + nt * 8 * HPB + kp * 64);
           }
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
@@ -510,12 +530,12 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
               for (int nt = 0; nt < NT; ++nt) {
                 if (HS4 && (kp & 1)) {  // odd k pairs: the second hi and lo chains
                   mma_bf16_16816(acc3[HS4 ? mt : 0][nt], a, bfr[nt][2 * hf], bfr[nt][2 * hf + 1]);
-                  mma_bf16_16816(acc4[HS4 ? mt : 0][nt], a, bfl[HS ? nt : 0][2 * hf],
-                                 bfl[HS ? nt : 0][2 * hf + 1]);
-                } else if (HS) {  // hi and lo parts on two independent accumulator chains
+                  mma_bf16_16816(acc4[HS4 ? mt : 0][nt], a, bfl[HLO ? nt : 0][2 * hf],
+                                 bfl[HLO ? nt : 0][2 * hf + 1]);
+                } else if (HLO) {  // hi and lo parts on two independent accumulator chains
                   mma_bf16_16816(acc[mt][nt], a, bfr[nt][2 * hf], bfr[nt][2 * hf + 1]);
-                  mma_bf16_16816(acc2[SPLITK ? mt : 0][nt], a, bfl[HS ? nt : 0][2 * hf],
-                                 bfl[HS ? nt : 0][2 * hf + 1]);
+                  mma_bf16_16816(acc2[SPLITK ? mt : 0][nt], a, bfl[HLO ? nt : 0][2 * hf],
+                                 bfl[HLO ? nt : 0][2 * hf + 1]);
                 } else if (SPLITK && hf == 1) {
                   mma_bf16_16816(acc2[SPLITK ? mt : 0][nt], a, bfr[nt][2], bfr[nt][3]);
                 } else {
@@ -540,6 +560,12 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 else
                   acc[mt][nt][q] += acc2[SPLITK ? mt : 0][nt][q];
               }
+        }
+        if (HN) {  // hi column + lo column; both lanes of a pair get the same sum
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[mt][0][q] += __shfl_xor_sync(0xffffffffu, acc[mt][0][q], 2);
         }
 
         // ---- gate math and state update, one (unit, batch) cell at a time
@@ -654,12 +680,13 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 const float hvv = hv[(us * NT + nt) * 2 + e];
-                const __nv_bfloat16 hi = __float2bfloat16_rn(hvv);
+                __nv_bfloat16 hi = __float2bfloat16_rn(hvv);
+                if (HN && (lane & 2)) hi = __float2bfloat16_rn(hvv - __bfloat162float(hi));
                 const uint32_t addr = stg + stg_cell[us][nt] + e * (UG * 2);
                 asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr),
                              "h"(*reinterpret_cast<const uint16_t*>(&hi))
                              : "memory");
-                if (HS) {  // residual part: bf16(h - bf16(h))
+                if (HLO) {  // residual part: bf16(h - bf16(h))
                   const __nv_bfloat16 lo = __float2bfloat16_rn(hvv - __bfloat162float(hi));
                   asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr + NB * UG * 2),
                                "h"(*reinterpret_cast<const uint16_t*>(&lo))
@@ -683,12 +710,13 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 const float hvv = hv[(us * NT + nt) * 2 + e];
-                const __nv_bfloat16 hi = __float2bfloat16_rn(hvv);
+                __nv_bfloat16 hi = __float2bfloat16_rn(hvv);
+                if (HN && (lane & 2)) hi = __float2bfloat16_rn(hvv - __bfloat162float(hi));
                 const uint32_t addr = nbuf + h_off1[us][nt] + e * HPB;
                 asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr),
                              "h"(*reinterpret_cast<const uint16_t*>(&hi))
                              : "memory");
-                if (HS) {  // residual part: bf16(h - bf16(h))
+                if (HLO) {  // residual part: bf16(h - bf16(h))
                   const __nv_bfloat16 lo = __float2bfloat16_rn(hvv - __bfloat162float(hi));
                   asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr + hpart),
                                "h"(*reinterpret_cast<const uint16_t*>(&lo))
@@ -762,7 +790,7 @@ int launch_fwd_bf16_v(const FwdParams& p_in, cudaStream_t stream, bool query_onl
   if (p.U % UG != 0 || NW < 1 || threads > C::MAXT) return (int)cudaErrorInvalidConfiguration;
   const uint32_t smem = fwd_smem_layout<C>(p.U).total;
   const int grid = p.NH * p.nbslices * p.CS;
-  if (info) *info = LaunchInfo{grid, threads, p.CS, C::NB, (int)smem, CELL * 100 + DH / 32 + 50 * HS};
+  if (info) *info = LaunchInfo{grid, threads, p.CS, C::NBV, (int)smem, CELL * 100 + DH / 32 + 50 * HS};
   static int prepared[64][5];
   const int e = prepare_launch(prepared, kern, smem, threads, p.CS);
   if (e != 0) return e;

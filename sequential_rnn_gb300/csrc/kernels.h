@@ -109,7 +109,8 @@ int launch_fwd_bf16_lstm(const FwdParams& p, int Dh, int NT, cudaStream_t s, boo
                          LaunchInfo* info);
 int launch_fwd_bf16_gru(const FwdParams& p, int Dh, int NT, cudaStream_t s, bool query_only,
                         LaunchInfo* info);
-// hsplit: h_{t-1} as a bf16 hi + lo pair and accurate gate math (sLSTM only)
+// hsplit: h_{t-1} as a bf16 hi + lo pair and accurate gate math (sLSTM only):
+// 1 = two B operands, 2 = both halves of one n8 tile (4 batch rows per CTA)
 int launch_fwd_bf16_slstm(const FwdParams& p, int Dh, int NT, int hsplit, cudaStream_t s,
                           bool query_only, LaunchInfo* info);
 // Units handled by one warp in the bf16 kernels (gate rows of one warp = UG * G).

@@ -42,15 +42,22 @@ constexpr double kProjTflops = 600.0;       // input-projection GEMM rate on all
 
 int log2_cs(int cs) { return cs == 1 ? 0 : cs == 2 ? 1 : cs == 4 ? 2 : cs == 8 ? 3 : 4; }
 
-bool hsplit_of(const rnn_desc_t* d) {
-  return d->cell == RNN_SLSTM && !(d->flags & RNN_FLAG_H_BF16) && d->Dh <= 256;
+}  // namespace
+
+// sLSTM h_{t-1} operand: 0 plain bf16; 1 bf16 hi + lo pair as two MMA operands;
+// 2 the pair packed into one n8 tile (batches of at most 4 rows per head).
+int hsplit_mode(const rnn_desc_t* d) {
+  if (d->cell != RNN_SLSTM || (d->flags & RNN_FLAG_H_BF16) || d->Dh > 256) return 0;
+  return d->B <= 4 ? 2 : 1;
 }
+
+namespace {
 
 // Fallback model for unmeasured points: sync floor of the launch shape plus a
 // fixed latency chain plus tensor-pipe issue (8-cycle mma.sync per sub-partition).
 double model_step_ns(const rnn_desc_t* d, int cs, int unit_group) {
   const int G = gates_of(d->cell), U = d->Dh / cs, NW = U / unit_group;
-  const int per_warp = (unit_group * G + 15) / 16 * (d->Dh / 16) * (hsplit_of(d) ? 2 : 1);
+  const int per_warp = (unit_group * G + 15) / 16 * (d->Dh / 16) * (hsplit_mode(d) == 1 ? 2 : 1);
   const double w = (double)per_warp * ((NW + 3) / 4);
   const double floor_ns = cs == 1 ? 160.0 : 205.0 + 4.0 * cs;
   return floor_ns + 150.0 + 7.0 * w;
@@ -62,7 +69,7 @@ bool cs_limits(const rnn_desc_t* d, int cs, FwdLimits* lim) {
   int e = 1;
   if (d->cell == RNN_LSTM) e = fwd_bf16_lstm_limits(d->Dh, U, lim);
   else if (d->cell == RNN_GRU) e = fwd_bf16_gru_limits(d->Dh, U, lim);
-  else e = fwd_bf16_slstm_limits(d->Dh, hsplit_of(d) ? 1 : 0, U, lim);
+  else e = fwd_bf16_slstm_limits(d->Dh, hsplit_mode(d), U, lim);
   if (e || U % lim->unit_group) return false;
   if (U / lim->unit_group * 32 > lim->max_threads) return false;       // registers
   if (lim->smem == 0 || lim->smem > (uint32_t)kMaxSmemOptin) return false;  // shared memory
@@ -94,7 +101,8 @@ int device_sms() {
 // L = 1: one layer over T steps; L > 1: the stacked wavefront (chunk_req 0 =
 // choose the chunk).  d->cluster != 0 restricts the search to that size.
 int plan_search(const rnn_desc_t* d, int L, int sms, int chunk_req, PlanChoice* out) {
-  const int nb = (d->B + 7) / 8;
+  const int nbr = hsplit_mode(d) == 2 ? 4 : 8;  // batch rows per CTA
+  const int nb = (d->B + nbr - 1) / nbr;
   const int T = d->T > 0 ? d->T : 1;
   bool found = false;
   PlanChoice best{};
@@ -179,7 +187,7 @@ int make_plan(const rnn_desc_t* d, Plan* pl) {
     pl->CS = cs;
     pl->U = U;
     pl->NT = 1;
-    pl->NB = 8;
+    pl->NB = hsplit_mode(d) == 2 ? 4 : 8;
   }
   pl->nbslices = (d->B + pl->NB - 1) / pl->NB;
   return RNN_OK;
@@ -201,9 +209,7 @@ int launch_forward(const rnn_desc_t* d, const Plan& pl, const FwdParams& p, cuda
     case RNN_GRU: return launch_fwd_bf16_gru(p, d->Dh, pl.NT, s, query_only, info);
     default:
       // hi+lo split of h for the sLSTM while it fits on chip (Dh <= 256)
-      return launch_fwd_bf16_slstm(p, d->Dh, pl.NT,
-                                   ((d->flags & RNN_FLAG_H_BF16) || d->Dh > 256) ? 0 : 1, s,
-                                   query_only, info);
+      return launch_fwd_bf16_slstm(p, d->Dh, pl.NT, hsplit_mode(d), s, query_only, info);
   }
 }
 

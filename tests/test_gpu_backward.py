@@ -105,6 +105,7 @@ CELL_CASES = [
     ("gru", 768, 4, 1, 6), ("gru", 64, 1, 1, 1),
     ("slstm", 32, 3, 2, 17), ("slstm", 64, 13, 2, 9), ("slstm", 128, 9, 1, 12),
     ("slstm", 256, 5, 2, 10), ("slstm", 768, 4, 1, 5), ("slstm", 64, 1, 1, 1),
+    ("slstm", 256, 3, 2, 10),  # forward with hi and lo in one n8 tile
 ]
 
 

@@ -83,6 +83,9 @@ SWEEP = [
     ("gru", "bf16", 256, 3, 1, 21), ("gru", "bf16", 768, 5, 1, 7), ("gru", "bf16", 128, 1, 2, 2),
     ("slstm", "bf16", 32, 7, 2, 15), ("slstm", "bf16", 64, 16, 1, 31), ("slstm", "bf16", 128, 3, 2, 9),
     ("slstm", "bf16", 256, 9, 1, 40), ("slstm", "bf16", 768, 2, 1, 6), ("slstm", "bf16", 256, 1, 1, 1),
+    # sLSTM with at most 4 batch rows: hi and lo halves of h share one n8 tile
+    ("slstm", "bf16", 32, 3, 3, 19), ("slstm", "bf16", 64, 4, 2, 33), ("slstm", "bf16", 128, 1, 2, 12),
+    ("slstm", "bf16", 256, 2, 2, 37), ("slstm", "bf16", 256, 4, 1, 64),
 ]
 
 
@@ -92,19 +95,20 @@ def test_forward_small_sweep(S, cell, dtype, Dh, B, NH, T):
     compare(run(S, d), oracle(d), dtype, f"{cell}/{dtype}/Dh{Dh}/B{B}/NH{NH}/T{T}")
 
 
-@pytest.mark.parametrize("cell,Dh,clusters", [
+@pytest.mark.parametrize("cell,Dh,clusters,B", [
     # (a split too coarse for the register file is rejected with UNSUPPORTED)
-    ("lstm", 64, (1, 2, 4, 8)), ("gru", 128, (1, 2, 4, 8)), ("slstm", 256, (4, 8, 16)),
-    ("lstm", 256, (8, 16)), ("gru", 256, (4, 8, 16)), ("slstm", 64, (1, 2, 4)),
-    ("lstm", 128, (2, 4, 8)), ("lstm", 32, (1, 2, 4)),
+    ("lstm", 64, (1, 2, 4, 8), 10), ("gru", 128, (1, 2, 4, 8), 10), ("slstm", 256, (4, 8, 16), 10),
+    ("lstm", 256, (8, 16), 10), ("gru", 256, (4, 8, 16), 10), ("slstm", 64, (1, 2, 4), 10),
+    ("lstm", 128, (2, 4, 8), 10), ("lstm", 32, (1, 2, 4), 10),
+    ("slstm", 256, (4, 8, 16), 3), ("slstm", 128, (2, 4, 8), 4), ("slstm", 64, (1, 2, 4), 1),
 ])
-def test_cluster_split_is_bitwise_identical(S, cell, Dh, clusters):
+def test_cluster_split_is_bitwise_identical(S, cell, Dh, clusters, B):
     """Splitting a head over 2..16 CTAs changes who computes, not the arithmetic.
 
     The one-CTA variant uses packed fp16x2 tanh for the gates and a single k
     chain (throughput-bound regime), so it is compared through the oracle only.
     """
-    d = make_inputs(cell, "bf16", 14, 10, 2, Dh, seed=5, bias="normal0.1", states="random")
+    d = make_inputs(cell, "bf16", 14, B, 2, Dh, seed=5, bias="normal0.1", states="random")
     g = dev(d)
     ref = oracle(d)
     outs = {c: run(S, d, cluster=c, g=g) for c in clusters}
@@ -137,6 +141,28 @@ def test_slstm_single_bf16_h_matches_rounded_oracle(S, Dh, clusters):
     split = [c for c in clusters if c > 1]
     for c in split[1:]:
         assert torch.equal(outs[c]["h_seq"], outs[split[0]]["h_seq"]), f"cluster {c}"
+
+
+@pytest.mark.parametrize("Dh,cluster", [(64, 1), (128, 2), (256, 8)])
+def test_slstm_small_batch_rows_are_independent(S, Dh, cluster):
+    """With at most 4 batch rows the hi and lo halves of h share one n8 tile and
+    the lanes holding the lo half mirror the state of their hi partners.  Batch
+    rows never interact, so the first 3 rows of a 4-row run equal a 3-row run
+    bit for bit, and the run of row 2 alone equals that row."""
+    d = make_inputs("slstm", "bf16", 21, 4, 2, Dh, seed=23, bias="normal0.1", states="random")
+    g = dev(d)
+    full = run(S, d, cluster=cluster, g=g)
+    compare(full, oracle(d), "bf16", f"Dh{Dh} B4")
+    for rows in (slice(0, 3), slice(2, 3)):
+        gs = {k: (v[:, rows].contiguous() if k == "Wx" else
+                  v[rows].contiguous() if k in ("h0", "c0", "n0", "m0") else v) for k, v in g.items()}
+        part = S.forward("slstm", gs["Wx"], gs["R"], gs["b"], gs["h0"], gs["c0"], gs["n0"], gs["m0"],
+                         cluster=cluster)
+        torch.cuda.synchronize()
+        for k in ("h_seq",):
+            assert torch.equal(part[k], full[k][:, rows]), (rows, k)
+        for k in ("hT", "cT", "nT", "mT"):
+            assert torch.equal(part[k], full[k][rows]), (rows, k)
 
 
 def test_training_stash_same_for_cluster_splits(S):
