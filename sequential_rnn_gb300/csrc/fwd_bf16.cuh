@@ -82,7 +82,11 @@ struct FwdCfg {
   // register estimate per compute thread -> largest CTA the register file holds
   static constexpr int REG_EST = MT * KREG * 4 + MT * NT * 8 + 88 + (HS == 1) * NT * 8;
   static constexpr int MAXT_R = (65536 / REG_EST) / 32 * 32;
-  static constexpr int MAXT = MAXT_R < 17 * 32 ? MAXT_R : 17 * 32;
+  static constexpr int MAXT_0 = MAXT_R < 16 * 32 ? MAXT_R : 16 * 32;
+  // The register file is split over the SM's four sub-partitions and warps are
+  // spread over them, so a bound of 9 warps costs registers like 12 would; CTAs
+  // come in 2^k warps (Dh 768: 3 x 2^k), so round to whole sub-partition rows.
+  static constexpr int MAXT = MAXT_0 >= 256 ? MAXT_0 / 128 * 128 : MAXT_0;
   static_assert(UG == 8 || UG == 16, "unit group");
   static_assert(UG * G % 16 == 0 || (UG == 8 && G == 3), "gate rows per warp fill m16 tiles");
   static_assert(DH % 32 == 0, "Dh multiple of 32");
@@ -159,6 +163,11 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   // each on two chains (even/odd k pairs).  HS = 2: hi and lo in one n8 tile.
   constexpr bool HLO = HS == 1, HN = HS == 2;
   constexpr bool HS4 = HLO && KS >= 8;
+  // A cluster step with >= 16 k16 steps: four k chains per m tile (k pair
+  // parity x k16 half) -- the dependent mma.sync chain, not the issue rate,
+  // bounds it (4x256 sLSTM: 8-long chains took ~640 cycles for 32 MMAs).
+  // At 8 k16 steps two chains per tile measured faster.
+  constexpr bool CH4 = !HLO && CL && KS >= 16;
   constexpr bool PACKED_TANH = !CL;
   // One CTA per head (all warps meet at a barrier every step): the next step's
   // Wx is primed while this step's MMAs are in flight, in a second accumulator
@@ -400,7 +409,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     int np = 0;  // steps primed so far (step np is next; its stage is np % PD)
     // accumulators of the step about to run, primed with scale*(Wx + bias)
     float acc[MT][NT][4], acc2[SPLITK ? MT : 1][NT][4];
-    float acc3[HS4 ? MT : 1][NT][4], acc4[HS4 ? MT : 1][NT][4];
+    float acc3[HS4 || CH4 ? MT : 1][NT][4], acc4[HS4 || CH4 ? MT : 1][NT][4];
     float wxn[NE];  // GRU: Wx_n stays outside r*(R_n h + b_n)
     float accp[MT][NT][4], wxnp[NE];  // EARLY_PREP: primed for the next step
     float(*A)[NT][4] = EARLY_PREP ? accp : acc;
@@ -494,9 +503,9 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 #pragma unroll
               for (int q = 0; q < 4; ++q) acc2[mt][nt][q] = 0.f;
         }
-        if (HS4) {
+        if (HS4 || CH4) {
 #pragma unroll
-          for (int mt = 0; mt < (HS4 ? MT : 1); ++mt)
+          for (int mt = 0; mt < (HS4 || CH4 ? MT : 1); ++mt)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -529,9 +538,12 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
                 if (HS4 && (kp & 1)) {  // odd k pairs: the second hi and lo chains
-                  mma_bf16_16816(acc3[HS4 ? mt : 0][nt], a, bfr[nt][2 * hf], bfr[nt][2 * hf + 1]);
-                  mma_bf16_16816(acc4[HS4 ? mt : 0][nt], a, bfl[HLO ? nt : 0][2 * hf],
+                  mma_bf16_16816(acc3[HS4 || CH4 ? mt : 0][nt], a, bfr[nt][2 * hf], bfr[nt][2 * hf + 1]);
+                  mma_bf16_16816(acc4[HS4 || CH4 ? mt : 0][nt], a, bfl[HLO ? nt : 0][2 * hf],
                                  bfl[HLO ? nt : 0][2 * hf + 1]);
+                } else if (CH4 && (kp & 1)) {  // odd k pairs: chains 3 and 4
+                  mma_bf16_16816(hf ? acc4[HS4 || CH4 ? mt : 0][nt] : acc3[HS4 || CH4 ? mt : 0][nt], a,
+                                 bfr[nt][2 * hf], bfr[nt][2 * hf + 1]);
                 } else if (HLO) {  // hi and lo parts on two independent accumulator chains
                   mma_bf16_16816(acc[mt][nt], a, bfr[nt][2 * hf], bfr[nt][2 * hf + 1]);
                   mma_bf16_16816(acc2[SPLITK ? mt : 0][nt], a, bfl[HLO ? nt : 0][2 * hf],
@@ -554,9 +566,9 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
-                if (HS4)
-                  acc[mt][nt][q] = (acc[mt][nt][q] + acc3[HS4 ? mt : 0][nt][q]) +
-                                   (acc2[mt][nt][q] + acc4[HS4 ? mt : 0][nt][q]);
+                if (HS4 || CH4)
+                  acc[mt][nt][q] = (acc[mt][nt][q] + acc3[HS4 || CH4 ? mt : 0][nt][q]) +
+                                   (acc2[mt][nt][q] + acc4[HS4 || CH4 ? mt : 0][nt][q]);
                 else
                   acc[mt][nt][q] += acc2[SPLITK ? mt : 0][nt][q];
               }
@@ -615,22 +627,35 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 }
               } else {
                 const float pi = r[0], pf = r[1], pz = r[2], po = r[3];
-                const float mn = fmaxf(pf + st_m[ei], pi);
+                // m_t = max(f~ + m_{t-1}, i~): one of the two stabilised gates is
+                // e^0 = 1, the other e^{-|f~ + m_{t-1} - i~|}
+                const float fm = pf + st_m[ei];
+                const bool fmax_ = fm >= pi;
+                const float mn = fmax_ ? fm : pi;
+                const float ex = __expf(-fabsf(fm - pi));
+                const float ig = fmax_ ? ex : 1.f;
+                const float fg = fmax_ ? 1.f : ex;
                 // Exponentials from the ex2-based __expf (2 ulp).  HS: tanh z~ from
                 // the identity tanh(x) = 1 - 2 / (e^{2x} + 1) on it -- the hardware
                 // tanh.approx (~2^-11 relative) lets the exponential gating drift
                 // 3e-2 from the exact recurrence over 4096 steps, this ~1e-6.
-                const float ig = __expf(pi - mn);
-                const float fg = __expf(pf + st_m[ei] - mn);
                 const float zt = HS ? 1.f - __fdividef(2.f, __expf(2.f * pz) + 1.f) : tanh_fast(pz);
                 const float c = fmaf(fg, st_c[ei], ig * zt);
                 const float nn = fmaf(fg, st_n[ei], ig);
                 st_c[ei] = c;
                 st_n[ei] = nn;
                 st_m[ei] = mn;
-                // r[o] holds o~ (HS) or o~/2 (fast path)
-                const float og = HS ? __fdividef(1.f, 1.f + __expf(-po)) : fmaf(0.5f, tanh_fast(po), 0.5f);
-                h = og * __fdividef(c, nn);
+                // r[o] holds o~ (HS) or o~/2 (fast path).  HS: h = c / (n (1 + e^{-o~})),
+                // one reciprocal for the output gate and the normaliser together.
+                float og;
+                if (HS) {
+                  const float eo = 1.f + __expf(-po);
+                  og = TR ? __fdividef(1.f, eo) : 0.f;
+                  h = __fdividef(c, eo * nn);
+                } else {
+                  og = fmaf(0.5f, tanh_fast(po), 0.5f);
+                  h = og * __fdividef(c, nn);
+                }
                 if (TR) {
                   act[0][TR ? ei : 0] = ig;
                   act[1][TR ? ei : 0] = fg;
