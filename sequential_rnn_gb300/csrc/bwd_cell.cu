@@ -85,6 +85,12 @@ struct BwdK {
   static constexpr uint32_t FLAG = BAR + 16;
   static constexpr uint32_t TOTAL = FLAG + 16;
   static constexpr bool SPLIT = MTW <= 2;      // two k chains when registers allow
+  // Per-cell inputs: loaded two steps ahead into registers where registers
+  // allow (PFD = 2).  At Dh = 768 (168 registers) the allocator spills values
+  // held across the MMA phase, and the spill store of a load in flight waits
+  // out the whole memory latency; there (PFD = 0) the step's lines are
+  // prefetched into L1 a step ahead and loaded while the step waits for dh_rec.
+  static constexpr int PFD = DH >= 768 ? 0 : 2;
 };
 
 template <bool CLUSTER_ACQ>
@@ -220,11 +226,32 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
     }
     v[NV - 1] = __bfloat162float(dhs[row * DH + j]);
   };
-  float bufA[EPT][NV], bufB[EPT][NV];  // inputs of steps t (A) and t-1 (B)
+  constexpr int PFD = K::PFD;
+  // the same cell's input lines, into L1 only
+  auto prefetch_step = [&](int t, int e) {
+    if (t < 0 || !cok[e]) return;
+    const size_t row = ((size_t)t * B + b0 + cn[e]) * NH + head;
+    const int j = u0 + cu[e];
+    const float* sg = p.stash_gates + row * 4 * DH + j;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) prefetch_l1(sg + g * DH);
+    prefetch_l1(p.stash_c + row * DH + j);
+    if (t > 0) prefetch_l1(p.stash_c + (row - tstep) * DH + j);
+    if (CELL == kSLSTM) {
+      prefetch_l1(p.stash_n + row * DH + j);
+      if (t > 0) prefetch_l1(p.stash_n + (row - tstep) * DH + j);
+    }
+    prefetch_l1(dhs + row * DH + j);
+  };
+  float bufA[EPT][NV], bufB[PFD == 2 ? EPT : 1][NV];  // inputs of steps t (A) and t-1 (B)
 #pragma unroll
   for (int e = 0; e < EPT; ++e) {
-    load_step(T - 1, e, bufA[e]);
-    load_step(T - 2, e, bufB[e]);
+    if (PFD == 2) {
+      load_step(T - 1, e, bufA[e]);
+      load_step(T - 2, e, bufB[PFD == 2 ? e : 0]);
+    } else {
+      prefetch_step(T - 1, e);
+    }
   }
 
   // B operand (dG) ldmatrix address of this lane
@@ -232,10 +259,15 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
   bool dead = false;
 
   // one reverse step s (t = T-1-s) on the inputs in `cur`; refills `cur` with the
-  // inputs of step t-2 (two buffers alternate: the loads get two steps to land).
+  // inputs of step t-2 (two buffers alternate: the loads get two steps to land),
+  // or (PFD = 0) loads them at the start of the step from L1.
   // Returns true when the loop ends (s == T yields dh0, or every thread gave up).
   auto rstep = [&](int s, float (&cur)[EPT][NV]) -> bool {
     const int t = T - 1 - s;
+    if (PFD == 0 && s < T) {
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) load_step(t, e, cur[e]);
+    }
     // ---- dh_rec[t] from the partials of step s-1
     if (s > 0) {
       if (CL) {
@@ -324,7 +356,10 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
       }
       // inputs of step t-2 arrive while the exchange runs
 #pragma unroll
-      for (int e = 0; e < EPT; ++e) load_step(t - 2, e, cur[e]);
+      for (int e = 0; e < EPT; ++e) {
+        if (PFD == 2) load_step(t - 2, e, cur[e]);
+        else prefetch_step(t - 1, e);
+      }
     }
     // dG of all cells in shared memory (and the previous dh_rec fully read)
     if (bar_red_or(1, NTH, dead)) return true;
@@ -402,7 +437,11 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
   };
   for (int s = 0;; s += 2) {
     if (rstep(s, bufA)) break;
-    if (rstep(s + 1, bufB)) break;
+    if constexpr (PFD == 2) {
+      if (rstep(s + 1, bufB)) break;
+    } else {
+      if (rstep(s + 1, bufA)) break;
+    }
   }
 
   // ---- initial-state gradients and this slice's bias-gradient partial (every
