@@ -20,20 +20,23 @@ namespace {
 // the cost is the per-step time times the waves the CTAs need over the SMs
 // (and, for a stack, how many layers' recurrences can be resident at once).
 // Per-step times: measured on GB300 (bf16 forward, T = 512, inputs in L2), by
-// CTAs per head 1, 2, 4, 8, 16; 0 = not measured -> model below.
+// CTAs per head 1, 2, 4, 8, 16; 0 = not measured -> model below.  `hn`: the
+// sLSTM rows for at most 4 batch rows (h's hi and lo halves in one n8 tile).
 struct StepRow {
-  int cell, Dh;
+  int cell, Dh, hn;
   float ns[5];
 };
 const StepRow kStepTable[] = {
-    {RNN_LSTM, 32, {332, 400, 388, 0, 0}},        {RNN_LSTM, 64, {438, 416, 405, 415, 0}},
-    {RNN_LSTM, 128, {0, 533, 442, 455, 505}},     {RNN_LSTM, 256, {0, 0, 776, 617, 708}},
-    {RNN_LSTM, 768, {0, 0, 0, 0, 1933}},          {RNN_GRU, 32, {302, 381, 372, 0, 0}},
-    {RNN_GRU, 64, {405, 398, 387, 397, 0}},         {RNN_GRU, 128, {692, 543, 424, 431, 479}},
-    {RNN_GRU, 256, {0, 976, 753, 719, 783}},      {RNN_GRU, 768, {0, 0, 0, 0, 1971}},
-    {RNN_SLSTM, 32, {403, 452, 464, 0, 0}},       {RNN_SLSTM, 64, {571, 507, 510, 576, 0}},
-    {RNN_SLSTM, 128, {0, 897, 679, 690, 727}},    {RNN_SLSTM, 256, {0, 0, 1425, 1128, 1172}},
-    {RNN_SLSTM, 768, {0, 0, 0, 0, 2013}},
+    {RNN_LSTM, 32, 0, {332, 400, 388, 0, 0}},       {RNN_LSTM, 64, 0, {438, 416, 405, 415, 0}},
+    {RNN_LSTM, 128, 0, {0, 533, 442, 455, 505}},    {RNN_LSTM, 256, 0, {0, 0, 775, 625, 793}},
+    {RNN_LSTM, 768, 0, {0, 0, 0, 0, 1945}},         {RNN_GRU, 32, 0, {302, 381, 372, 0, 0}},
+    {RNN_GRU, 64, 0, {405, 398, 387, 397, 0}},      {RNN_GRU, 128, 0, {692, 543, 424, 431, 479}},
+    {RNN_GRU, 256, 0, {0, 1022, 761, 743, 820}},    {RNN_GRU, 768, 0, {0, 0, 0, 0, 1995}},
+    {RNN_SLSTM, 32, 0, {403, 452, 464, 0, 0}},      {RNN_SLSTM, 64, 0, {571, 507, 510, 576, 0}},
+    {RNN_SLSTM, 128, 0, {0, 897, 679, 690, 727}},   {RNN_SLSTM, 256, 0, {0, 0, 1413, 1084, 1105}},
+    {RNN_SLSTM, 768, 0, {0, 0, 0, 0, 2015}},        {RNN_SLSTM, 32, 1, {402, 449, 438, 0, 0}},
+    {RNN_SLSTM, 64, 1, {498, 477, 465, 482, 0}},    {RNN_SLSTM, 128, 1, {0, 588, 500, 509, 562}},
+    {RNN_SLSTM, 256, 1, {0, 0, 893, 678, 758}},
 };
 constexpr int kClusterSizes[5] = {1, 2, 4, 8, 16};
 constexpr int kMaxSmemOptin = 232448;       // dynamic shared memory per CTA (sm_103)
@@ -78,8 +81,10 @@ bool cs_limits(const rnn_desc_t* d, int cs, FwdLimits* lim) {
 }
 
 double step_ns(const rnn_desc_t* d, int cs, const FwdLimits& lim) {
+  const int hn = hsplit_mode(d) == 2 ? 1 : 0;
   for (const StepRow& r : kStepTable)
-    if (r.cell == d->cell && r.Dh == d->Dh && r.ns[log2_cs(cs)] > 0) return r.ns[log2_cs(cs)];
+    if (r.cell == d->cell && r.Dh == d->Dh && r.hn == hn && r.ns[log2_cs(cs)] > 0)
+      return r.ns[log2_cs(cs)];
   return model_step_ns(d, cs, lim.unit_group);
 }
 

@@ -224,11 +224,15 @@ def _plan(lib, L=1, sms=148, **kw):
     (2, 256, 4, 4, 4096, 8),     # sLSTM 4 x 256 (hi + lo h)
     (0, 768, 1, 16, 1024, 16),   # LSTM 1 x 768: only the 16-CTA split fits on chip
     (1, 32, 8, 16, 512, 1),      # GRU 32: one CTA per head is fastest
+    (2, 64, 12, 4, 512, 4),      # sLSTM 12 x 64 with 4 batch rows (hi + lo in one n8 tile)
+    (2, 128, 6, 3, 512, 4),      # sLSTM 6 x 128, 3 batch rows
+    (2, 64, 12, 16, 512, 2),     # sLSTM 12 x 64, 16 batch rows (hi + lo operands)
 ])
 def test_plan_picks_measured_best(lib, cell, Dh, NH, B, T, want):
     st, out = _plan(lib, cell=cell, Dh=Dh, NH=NH, B=B, T=T)
     assert st == 0 and out[0] == want, out
-    nb = (B + 7) // 8
+    rows = 4 if cell == 2 and B <= 4 and Dh <= 256 else 8  # batch rows per CTA
+    nb = (B + rows - 1) // rows
     assert out[2] == NH * nb * want and out[3] == -(-out[2] // 148)
 
 
