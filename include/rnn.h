@@ -131,7 +131,7 @@ int rnn_bwd(const rnn_desc_t* desc, const void* R, const float* h0, const float*
 /* rnn_fwd for a sequence in (pinned) host memory: Wx_host [T, B, NH, G*Dh] is
  * read from and h_seq_host [T, B, NH, Dh] written to host memory while the
  * recurrence runs.  Time is cut into chunks of `chunk` steps (0 = automatic:
- * T/4, at least 64); chunk c's Wx is copied in on a copy stream while chunk
+ * T/8, at least 64); chunk c's Wx is copied in on a copy stream while chunk
  * c-1 runs, and chunk c-1's h_seq is copied out on another, so only the first
  * chunk's upload and the last chunk's download are not hidden behind the
  * recurrence.  Each chunk continues from the previous chunk's final state,

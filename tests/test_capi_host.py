@@ -289,6 +289,11 @@ def test_fwd_host_workspace_size(lib):
         want = 256 + 2 * al(tc * rows * 4 * 64 * 2) + 2 * al(tc * rows * 64 * 2) + 2 * 2 * al(rows * 64 * 4)
         assert lib.rnn_fwd_host_workspace_size(ctypes.byref(d), chunk) == want, chunk
     assert lib.rnn_fwd_host_workspace_size(ctypes.byref(d), -1) == 0
+    # the automatic chunk is T/8 steps (at least 64)
+    d = _desc(T=2048, B=4, NH=2, Dh=64)
+    tc = 256
+    want = 256 + 2 * al(tc * rows * 4 * 64 * 2) + 2 * al(tc * rows * 64 * 2) + 2 * 2 * al(rows * 64 * 4)
+    assert lib.rnn_fwd_host_workspace_size(ctypes.byref(d), 0) == want
 
 
 def test_fwd_host_argument_checks(lib):
