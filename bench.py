@@ -346,8 +346,9 @@ def run_ours(args, w, rank, world, local_rank):
     # ---- end to end through the C ABI with pinned host buffers: every step copies
     #      that step's Wx in from host memory and h_seq back out.  Forward: the
     #      host-memory entry point (rnn_fwd_host), which pipelines the copies with
-    #      the recurrence over time chunks; training: Wx and R copied in, then the
-    #      device-resident step, then h_seq copied out.
+    #      the recurrence over time chunks; training: Wx and R double-buffered on
+    #      the device, step i+1's copied in on a copy stream while step i runs, and
+    #      h_seq copied out after each step.
     hWx = g["Wx"].cpu().pin_memory()
     hh = torch.empty(h_seq.shape, dtype=dt).pin_memory()
     e2e_steps = max(3, min(args.steps, 50))
@@ -366,14 +367,29 @@ def run_ours(args, w, rank, world, local_rank):
         h2d = hWx.numel() * hWx.element_size()
     else:
         hR = g["R"].cpu().pin_memory()
-        dWx = torch.empty_like(g["Wx"])
-        dR = torch.empty_like(g["R"])
+        bufs = [(torch.empty_like(g["Wx"]), torch.empty_like(g["R"])) for _ in range(2)]
+        cstream = torch.cuda.Stream(dev)
+        ready = [torch.cuda.Event() for _ in range(2)]  # buffer b holds the next inputs
+        done = [torch.cuda.Event() for _ in range(2)]   # the step reading buffer b ended
+        nstep = [0]
+
+        def upload(b):
+            cstream.wait_event(done[b])
+            with torch.cuda.stream(cstream):
+                bufs[b][0].copy_(hWx, non_blocking=True)
+                bufs[b][1].copy_(hR, non_blocking=True)
+            ready[b].record(cstream)
 
         def e2e_step():
-            dWx.copy_(hWx, non_blocking=True)
-            dR.copy_(hR, non_blocking=True)
-            step(dWx, dR)
+            b = nstep[0] & 1
+            if nstep[0] == 0:
+                upload(0)
+            stream.wait_event(ready[b])
+            upload(1 - b)  # the next step's inputs, while this one runs
+            step(*bufs[b])
+            done[b].record(stream)
             hh.copy_(h_seq, non_blocking=True)
+            nstep[0] += 1
         h2d = hWx.numel() * hWx.element_size() + hR.numel() * hR.element_size()
     for _ in range(2):
         e2e_step()
@@ -381,6 +397,8 @@ def run_ours(args, w, rank, world, local_rank):
     ee[0].record(stream)
     for _ in range(e2e_steps):
         e2e_step()
+    if w["backward"]:  # the last upload (inputs of the step after) is inside the region too
+        stream.wait_event(ready[nstep[0] & 1])
     ee[1].record(stream)
     barrier()
     if not w["backward"] and S.rnn_read_status(hws):
