@@ -33,7 +33,8 @@
  * gates on the hardware tanh).  For the sLSTM, whose exponential gating
  * amplifies per-step rounding of h by ~10^3 over 4096 steps, h_{t-1} enters
  * the tensor cores as a bf16 pair hi + lo (hi = bf16(h), lo = bf16(h - hi),
- * two MMAs into fp32) and tanh(z~) is evaluated as 1 - 2/(e^{2z~}+1) on the
+ * both products accumulated in fp32; with B <= 4 the two halves share one
+ * MMA tile) and tanh(z~) is evaluated as 1 - 2/(e^{2z~}+1) on the
  * 2-ulp exponential instead of the ~2^-11 hardware tanh, for Dh <= 256
  * (Dh = 768 runs the plain bf16 operand: the pair does not fit on chip beside
  * R); RNN_FLAG_H_BF16 turns this off.
