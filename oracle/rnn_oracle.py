@@ -43,7 +43,7 @@ input weight applied to all steps at once) is the plain definition
 
 Everything is fp64 numpy; a library batched matmul is the only "primitive".
 Optionally ``emulate_bf16_h`` rounds h_{t-1} to bf16 before the contraction,
-mirroring a bf16 MMA operand; it is a diagnosis aid, parity is judged against
+mirroring a bf16 MMA operand; it is a diagnosis aid, parity is checked against
 the plain fp64 run.
 """
 from __future__ import annotations
