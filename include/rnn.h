@@ -132,7 +132,9 @@ int rnn_bwd(const rnn_desc_t* desc, const void* R, const float* h0, const float*
 /* rnn_fwd for a sequence in (pinned) host memory: Wx_host [T, B, NH, G*Dh] is
  * read from and h_seq_host [T, B, NH, Dh] written to host memory while the
  * recurrence runs.  Time is cut into chunks of `chunk` steps (0 = automatic:
- * T/8, at least 64); chunk c's Wx is copied in on a copy stream while chunk
+ * T/8, at least 64 -- or, for bf16 runs that consume Wx at under ~64 GB/s by
+ * the plan's step time and pinned, mapped host buffers, the RNN_HOST_DIRECT
+ * mode below); chunk c's Wx is copied in on a copy stream while chunk
  * c-1 runs, and chunk c-1's h_seq is copied out on another, so only the first
  * chunk's upload and the last chunk's download are not hidden behind the
  * recurrence.  Each chunk continues from the previous chunk's final state,
@@ -144,7 +146,16 @@ int rnn_bwd(const rnn_desc_t* desc, const void* R, const float* h0, const float*
  * fp32 pointers 4, workspace 256 and >= rnn_fwd_host_workspace_size() bytes
  * (status word at offset 0, then two Wx chunks, two h_seq chunks and the
  * carried states).  Host memory that is not pinned still works, without the
- * overlap. */
+ * overlap.
+ *
+ * chunk = RNN_HOST_DIRECT: no staging copies; one rnn_fwd whose kernel reads
+ * Wx_host and writes h_seq_host through their device mapping (page-locked host
+ * memory on a unified-addressing system, reached over the CPU-GPU link; on
+ * Grace-Blackwell NVLink-C2C).  Both buffers must be page-locked and mapped
+ * (cudaHostAlloc / cudaMallocHost, or cudaHostRegister with mapping), else
+ * RNN_ERR_INVALID_ARG; alignment as for rnn_fwd (16 bytes); workspace as for
+ * rnn_fwd. */
+#define RNN_HOST_DIRECT (-1)
 size_t rnn_fwd_host_workspace_size(const rnn_desc_t* desc, int32_t chunk);
 int rnn_fwd_host(const rnn_desc_t* desc, int32_t chunk, const void* Wx_host, const void* R,
                  const float* bias, const float* h0, const float* c0, const float* n0,

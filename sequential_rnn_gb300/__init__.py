@@ -15,7 +15,7 @@ import torch
 
 from . import _lib
 from ._lib import (CELLS, DTYPES, RNN_BF16, RNN_F32, RNN_FLAG_H_BF16, RNN_FLAG_TEST_TIMEOUT,
-                   RNN_FLAG_TRAIN,
+                   RNN_FLAG_TRAIN, RNN_HOST_DIRECT,
                    STATUS, rnn_desc_t)
 
 __all__ = ["RnnError", "make_desc", "rnn_workspace_size", "rnn_stash_size", "rnn_fwd", "rnn_bwd",

@@ -17,6 +17,7 @@ RNN_F32, RNN_BF16 = 0, 1
 RNN_FLAG_TRAIN = 1
 RNN_FLAG_H_BF16 = 2
 RNN_FLAG_TEST_TIMEOUT = 1 << 30
+RNN_HOST_DIRECT = -1  # rnn_fwd_host chunk: the kernel reads / writes the mapped host buffers
 STATUS = {0: "RNN_OK", 1: "RNN_ERR_INVALID_ARG", 2: "RNN_ERR_UNSUPPORTED",
           3: "RNN_ERR_MISALIGNED", 4: "RNN_ERR_LAUNCH", 5: "RNN_ERR_TIMEOUT",
           6: "RNN_ERR_NO_CLUSTER", 7: "RNN_ERR_SCRATCH_LIMIT"}

@@ -43,6 +43,9 @@ struct PlanChoice {
 };
 
 int device_sms();
+// Planned time of one recurrence step (ns) of the bf16 forward with CS CTAs per
+// head (measured table, else the latency model); 0 when no variant fits.
+double plan_step_ns(const rnn_desc_t* d, int cs);
 // L = 1: one forward over T steps; L > 1: the stacked wavefront (chunk_req 0 =
 // choose the chunk).  d->cluster != 0 restricts the search to that size.
 int plan_search(const rnn_desc_t* d, int L, int sms, int chunk_req, PlanChoice* out);

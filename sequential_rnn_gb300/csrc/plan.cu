@@ -90,6 +90,12 @@ double step_ns(const rnn_desc_t* d, int cs, const FwdLimits& lim) {
 
 }  // namespace
 
+double plan_step_ns(const rnn_desc_t* d, int cs) {
+  FwdLimits lim;
+  if (d->dtype != RNN_BF16 || !bf16_dh_supported(d->Dh) || !cs_limits(d, cs, &lim)) return 0.0;
+  return step_ns(d, cs, lim);
+}
+
 int device_sms() {
   static int cached[64] = {};
   int dev = 0;

@@ -288,7 +288,7 @@ def test_fwd_host_workspace_size(lib):
     for chunk, tc in ((0, 64), (10, 10), (500, 100)):
         want = 256 + 2 * al(tc * rows * 4 * 64 * 2) + 2 * al(tc * rows * 64 * 2) + 2 * 2 * al(rows * 64 * 4)
         assert lib.rnn_fwd_host_workspace_size(ctypes.byref(d), chunk) == want, chunk
-    assert lib.rnn_fwd_host_workspace_size(ctypes.byref(d), -1) == 0
+    assert lib.rnn_fwd_host_workspace_size(ctypes.byref(d), -2) == 0
     # the automatic chunk is T/8 steps (at least 64)
     d = _desc(T=2048, B=4, NH=2, Dh=64)
     tc = 256
@@ -308,3 +308,15 @@ def test_fwd_host_argument_checks(lib):
     assert _fwd_host(lib, r=0) == 1
     assert _fwd_host(lib, r=0x2008) == 3
     assert _fwd_host(lib, desc=_desc(B=0)) == 0
+
+
+def test_fwd_host_direct_mode_arguments(lib):
+    """chunk = RNN_HOST_DIRECT (-1): the workspace is the forward's status word;
+    chunks below it are invalid; an empty batch is a no-op; pointers the driver
+    does not report as mapped host memory are refused (here: no device at all)."""
+    d = _desc(T=100, B=4, NH=2, Dh=64)
+    assert lib.rnn_fwd_host_workspace_size(ctypes.byref(d), -1) == 256
+    assert lib.rnn_fwd_host_workspace_size(ctypes.byref(d), -2) == 0
+    assert _fwd_host(lib, chunk=-2) == 1
+    assert _fwd_host(lib, desc=_desc(B=0), chunk=-1) == 0
+    assert _fwd_host(lib, chunk=-1) == 1

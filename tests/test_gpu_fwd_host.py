@@ -58,6 +58,44 @@ def test_fwd_host_equals_device_forward(S, cell, dtype, Dh, B, NH, T, chunk):
             assert torch.equal(got[k], ref[k]), k
 
 
+@pytest.mark.parametrize("cell,Dh,B,NH,T", [
+    ("lstm", 64, 16, 12, 300), ("gru", 128, 5, 2, 41), ("slstm", 256, 4, 2, 40),
+    ("slstm", 64, 9, 3, 17),
+])
+def test_fwd_host_direct_equals_device_forward(S, cell, Dh, B, NH, T):
+    """RNN_HOST_DIRECT: the kernel streams Wx from and writes h_seq to the mapped
+    pinned buffers; the arithmetic is the device forward's, bit for bit."""
+    d = make_inputs(cell, "bf16", T, B, NH, Dh, seed=T + Dh + 1, bias="normal0.1", states="random")
+    got, ref = both(S, d, S.RNN_HOST_DIRECT)
+    assert torch.equal(got["h_seq"], ref["h_seq"].cpu())
+    for k in ("hT", "cT", "nT", "mT"):
+        if k in ref:
+            assert torch.equal(got[k], ref[k]), k
+
+
+def test_fwd_host_direct_rejects_unmapped_buffers(S):
+    """Pageable host memory or device memory is refused before anything runs."""
+    d = make_inputs("lstm", "bf16", 9, 3, 2, 64, seed=3)
+    R = torch.from_numpy(d["R"]).to("cuda", torch.bfloat16)
+    pageable = torch.from_numpy(d["Wx"]).to(torch.bfloat16)  # not pinned
+    with pytest.raises(S.RnnError) as e:
+        S.forward_host("lstm", pageable, R, chunk=S.RNN_HOST_DIRECT)
+    assert "INVALID_ARG" in str(e.value)
+    # device memory as the "host" h_seq, through the C ABI (the binding refuses it earlier)
+    import ctypes
+    from sequential_rnn_gb300 import _lib
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    desc = S.make_desc("lstm", "bf16", 9, 3, 2, 64)
+    wx_pin = pageable.pin_memory()
+    hs_dev = torch.empty((9, 3, 2, 64), dtype=torch.bfloat16, device="cuda")
+    fin = [torch.empty((3, 2, 64), device="cuda") for _ in range(2)]
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    st = _lib.load().rnn_fwd_host(ctypes.byref(desc), S.RNN_HOST_DIRECT, P(wx_pin), P(R), None, None,
+                                  None, None, None, P(hs_dev), P(fin[0]), P(fin[1]), None, None,
+                                  P(ws), 256, None)
+    assert st == 1  # RNN_ERR_INVALID_ARG
+
+
 def test_fwd_host_full_workload_against_oracle(S):
     d = workload_inputs("lstm_bf16_12x64_b16_t1024")
     got, _ = both(S, d, 0)
