@@ -193,15 +193,16 @@ def run_reference(args, w, rank):
                     "d2h_bytes_per_step": 0}}
 
 
-# host-only multi-launch runtimes (layer wavefront, host-memory forward): no
-# device code, no launch parameter of a single-call entry point
-HOST_ONLY_SOURCES = ("runtime.cu",)
+# host-only sources (argument checks, the launch plan, the multi-launch
+# runtimes): no device code.  The plan's effect on a measured launch is its
+# shape, which the committed traffic entries record and ncu_traffic compares.
+HOST_ONLY_SOURCES = ("api.h", "capi.cu", "plan.cu", "runtime.cu")
 
 
 def kernel_source_hash():
-    """Hash of the sources that define the kernels and their launches (every
-    file under csrc but the host-only runtimes): ncu counters taken at another
-    hash no longer describe the kernels that run."""
+    """Hash of the sources that hold device code (every file under csrc but the
+    host-only ones): ncu counters taken at another hash no longer describe the
+    kernels that run."""
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "sequential_rnn_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
@@ -212,8 +213,9 @@ def kernel_source_hash():
     return h.hexdigest()[:12]
 
 
-def ncu_traffic(workload):
-    """DRAM bytes per launch from a committed ncu summary, if it matches these sources."""
+def ncu_traffic(workload, launch=None):
+    """DRAM bytes per launch from a committed ncu summary, if it matches these
+    sources and (when both are known) the forward's launch shape."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -221,6 +223,9 @@ def ncu_traffic(workload):
         j = json.load(f)
     e = j.get(workload)
     if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    shape = e.get("launch")
+    if shape and launch and any(shape[k] != launch.get(k) for k in shape):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -439,7 +444,7 @@ def run_ours(args, w, rank, world, local_rank):
             "roofline_ns": t_roof * 1e9, "frac": t_roof / t_meas_step,
             "peaks": f"{peak_kind}: {hbm} GB/s, {tflops_peak} TFLOP/s bf16"},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved_gbs / hbm, "traffic": ncu_traffic(args.workload),
+                     "frac": achieved_gbs / hbm, "traffic": ncu_traffic(args.workload, cfg),
                      "note": roof_note},
         "e2e": {"value": world * fl_step / t_e2e / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
