@@ -375,3 +375,26 @@ def test_stack_matches_torch_multilayer(cell):
     np.testing.assert_allclose(ref["h_seq"][:, :, 0], out, rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(ref["hT"][:, :, 0], hn, rtol=1e-10, atol=1e-12)
     assert W_ih0.shape == (G * Dh, Din)
+
+
+def test_slstm_stabilised_gate_pair_has_a_unit_member():
+    """With m_t = max(f~ + m_{t-1}, i~), one of the stabilised gates is exactly
+    e^0 = 1 at every step and the other lies in (0, 1]: the identity the
+    kernels use to form the pair with a single exponential.  A stabiliser
+    update without the carried m (or with the wrong sign) breaks it."""
+    d = _inp("slstm", T=25, B=3, NH=2, Dh=6, seed=9)
+    out = O.slstm_forward(d["Wx"], d["R"], d["b"], d["h0"], d["c0"], d["n0"], d["m0"], keep=True)
+    for (_, _, _, i, f, _, _, _, _) in out["_saved"]:
+        assert np.all(np.maximum(i, f) == 1.0)
+        assert np.all(np.minimum(i, f) > 0.0) and np.all(np.minimum(i, f) <= 1.0)
+    # the same pair from one exponential of -|f~ + m_{t-1} - i~|
+    m = d["m0"].astype(np.float64)
+    Dh = d["R"].shape[1]
+    h = d["h0"].astype(np.float64)
+    for t, (h_prev, _, _, i, f, _, _, _, _) in enumerate(out["_saved"]):
+        pre = d["Wx"][t] + np.einsum("bhk,hkg->bhg", h_prev, d["R"].astype(np.float64)) + d["b"]
+        gi, gf = pre[..., :Dh], pre[..., Dh:2 * Dh]
+        e = np.exp(-np.abs(gf + m - gi))
+        np.testing.assert_allclose(np.where(gf + m >= gi, e, 1.0), i, rtol=1e-13, atol=0)
+        np.testing.assert_allclose(np.where(gf + m >= gi, 1.0, e), f, rtol=1e-13, atol=0)
+        m = np.maximum(gf + m, gi)
