@@ -43,8 +43,9 @@ input weight applied to all steps at once) is the plain definition
 
 Everything is fp64 numpy; a library batched matmul is the only "primitive".
 Optionally ``emulate_bf16_h`` rounds h_{t-1} to bf16 before the contraction,
-mirroring a bf16 MMA operand; it is a diagnosis aid, parity is checked against
-the plain fp64 run.
+mirroring a bf16 MMA operand, and (sLSTM) ``emulate_bf16_pair_h`` replaces it
+by bf16(h) + bf16(h - bf16(h)), the two-part operand; both are diagnosis aids,
+parity is checked against the plain fp64 run.
 """
 from __future__ import annotations
 
@@ -153,7 +154,7 @@ def gru_forward(Wx, R, b=None, h0=None, emulate_bf16_h=False, keep=False):
 
 
 def slstm_forward(Wx, R, b=None, h0=None, c0=None, n0=None, m0=None,
-                  emulate_bf16_h=False, keep=False):
+                  emulate_bf16_h=False, keep=False, emulate_bf16_pair_h=False):
     Dh = R.shape[1]
     Wx, R, b, (h, c, n, m) = _prep(Wx, R, b, {"h0": h0, "c0": c0, "n0": n0, "m0": m0},
                                    ("h0", "c0", "n0", "m0"), Dh)
@@ -162,6 +163,9 @@ def slstm_forward(Wx, R, b=None, h0=None, c0=None, n0=None, m0=None,
     saved = []
     for t in range(T):
         hin = _to_bf16_f64(h) if emulate_bf16_h else h
+        if emulate_bf16_pair_h:  # h as the sum of two bf16 parts: bf16(h) + bf16(h - bf16(h))
+            hi = _to_bf16_f64(h)
+            hin = hi + _to_bf16_f64(h - hi)
         pre = Wx[t] + _recurrent(hin, R) + b
         gi, gf, gz, go = _split(pre, 4)
         m_new = np.maximum(gf + m, gi)

@@ -398,3 +398,19 @@ def test_slstm_stabilised_gate_pair_has_a_unit_member():
         np.testing.assert_allclose(np.where(gf + m >= gi, e, 1.0), i, rtol=1e-13, atol=0)
         np.testing.assert_allclose(np.where(gf + m >= gi, 1.0, e), f, rtol=1e-13, atol=0)
         m = np.maximum(gf + m, gi)
+
+
+def test_slstm_workload_needs_more_than_a_bf16_h_operand():
+    """The premise of the sLSTM operand reading, on the 4x256, B=4, T=4096
+    workload's inputs: the exponentially gated recurrence is not contractive,
+    so rounding h to bf16 before every contraction (all else fp64) ends far
+    from the exact recurrence, beyond the 2e-2 bar, while the two-part operand
+    bf16(h) + bf16(h - bf16(h)) stays well inside it."""
+    from synth import workload_inputs
+    d = workload_inputs("slstm_bf16_4x256_b4_t4096")
+    args = (d["Wx"], d["R"], d["b"], d["h0"], d["c0"], d["n0"], d["m0"])
+    exact = O.slstm_forward(*args)["h_seq"]
+    one = O.slstm_forward(*args, emulate_bf16_h=True)["h_seq"]
+    pair = O.slstm_forward(*args, emulate_bf16_pair_h=True)["h_seq"]
+    assert np.abs(one - exact).max() > 0.1
+    assert np.abs(pair - exact).max() < 1e-2
