@@ -40,6 +40,7 @@ PINS = {
                        P.test_slstm_R0_weighted_average(), P.test_T1_scalar_closed_forms()),
     "fd": lambda: [P.test_backward_finite_differences(c) for c in ("lstm", "gru", "slstm")],
     "unstab": lambda: P.test_slstm_equals_unstabilised_form(),
+    "stab_pair": lambda: P.test_slstm_stabilised_gate_pair_has_a_unit_member(),
 }
 
 
