@@ -10,8 +10,11 @@ before every timed step, outside the timed events.  ``value`` is recurrent
 TFLOP/s = 2*B*NH*Dh*G*Dh*T / step time (backward counts twice that), summed
 over ranks (weak scaling: every rank runs its own independent batch).
 ``e2e`` repeats the measurement through the same C ABI with pinned host
-buffers: host->device copy of the step's inputs and device->host copy of
-h_seq inside the timed region.  ``--impl reference`` times the fp64 CPU
+buffers: host->device transfer of the step's inputs and device->host transfer
+of h_seq inside the timed region (forward workloads: rnn_fwd_host's automatic
+mode -- staged copies pipelined over eight time chunks, or, for a Wx stream
+under 64 GB/s, the kernel reading and writing the mapped host buffers; the
+training workload: double-buffered copies).  ``--impl reference`` times the fp64 CPU
 oracle (the reference arm) on a bounded sample of the same workload.
 """
 from __future__ import annotations
