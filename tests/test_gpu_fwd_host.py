@@ -47,6 +47,7 @@ def both(S, d, chunk):
     ("slstm", "bf16", 256, 4, 2, 40, 9),
     ("lstm", "f32", 64, 4, 1, 33, 10),
     ("gru", "bf16", 32, 3, 2, 12, 100),       # one chunk
+    ("slstm", "bf16", 256, 4, 4, 40, 0),      # automatic: slow Wx stream -> direct reads
 ])
 def test_fwd_host_equals_device_forward(S, cell, dtype, Dh, B, NH, T, chunk):
     d = make_inputs(cell, dtype, T, B, NH, Dh, seed=T + Dh, bias="normal0.1", states="random")
