@@ -320,3 +320,30 @@ def test_fwd_host_direct_mode_arguments(lib):
     assert _fwd_host(lib, chunk=-2) == 1
     assert _fwd_host(lib, desc=_desc(B=0), chunk=-1) == 0
     assert _fwd_host(lib, chunk=-1) == 1
+
+
+def test_binding_constants_match_the_header():
+    """Every enum value and #define of include/rnn.h that the binding mirrors
+    has the header's value (read from the header text)."""
+    import os
+    import re
+    from sequential_rnn_gb300 import _lib as L
+    hdr = open(os.path.join(os.path.dirname(__file__), "..", "include", "rnn.h")).read()
+    def value(expr):  # integer literals and `a << b` only
+        m = re.fullmatch(r"(\d+)\s*<<\s*(\d+)", expr.strip())
+        return int(m.group(1)) << int(m.group(2)) if m else int(expr)
+
+    vals = {}
+    for name, expr in re.findall(r"\b(RNN_[A-Z0-9_]+)\s*=\s*([^,}/\n]+)", hdr):
+        vals[name] = value(expr)
+    for name, expr in re.findall(r"#define\s+(RNN_[A-Z0-9_]+)\s+\(?(-?\d+)\)?", hdr):
+        vals[name] = int(expr)
+    mirrored = {"RNN_LSTM": L.RNN_LSTM, "RNN_GRU": L.RNN_GRU, "RNN_SLSTM": L.RNN_SLSTM,
+                "RNN_F32": L.RNN_F32, "RNN_BF16": L.RNN_BF16, "RNN_FLAG_TRAIN": L.RNN_FLAG_TRAIN,
+                "RNN_FLAG_H_BF16": L.RNN_FLAG_H_BF16,
+                "RNN_FLAG_TEST_TIMEOUT": L.RNN_FLAG_TEST_TIMEOUT,
+                "RNN_HOST_DIRECT": L.RNN_HOST_DIRECT}
+    for name, v in mirrored.items():
+        assert vals[name] == v, name
+    for code, name in L.STATUS.items():
+        assert vals[name] == code, name
