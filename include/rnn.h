@@ -118,8 +118,11 @@ int rnn_fwd(const rnn_desc_t* desc, const void* Wx, const void* R, const float* 
  *   db [NH,G*Dh] fp32 = sum_t dG_t, dh0, dc0, dn0 [B,NH,Dh] fp32
  *   (dc0: LSTM/sLSTM, dn0: sLSTM; each of dR/db/dh0/dc0/dn0 may be NULL).
  * h0, c0, n0: the forward's initial states (NULL = zeros).  dhT, dcT, dnT: upstream
- * gradients of the final states (NULL = zero).  The sLSTM stabiliser carries no
- * gradient (the output does not depend on it).  dh_seq: input dtype.  Alignment:
+ * gradients of the final states (NULL = zero).  The sLSTM stabiliser m is held at
+ * its forward values and carries no gradient: exact for any loss of h (h does not
+ * depend on m); the dcT, dnT terms are differentiated with m_T held fixed, so
+ * that the backward of consecutive time chunks, each fed the next chunk's
+ * dh0/dc0/dn0 as dhT/dcT/dnT, composes to the whole sequence's.  dh_seq: input dtype.  Alignment:
  * R, h_seq, dh_seq, dWx, stash 16 bytes; fp32 pointers 8 bytes; workspace 256.
  * The reverse recurrence runs as one thread-block cluster per head slice (as the
  * forward), then the dR contraction (tcgen05 tensor cores) and the db reduction. */

@@ -32,8 +32,8 @@ readings are used, written out below in the order the recurrence applies them:
         n_t = f*n + i,  h_t = sigmoid(o~) * c_t / n_t.
 
 Backward passes are textbook backpropagation through time of exactly these
-forward graphs (the sLSTM stabiliser m is a reparametrisation the output does
-not depend on, so it carries no gradient).
+forward graphs (the sLSTM stabiliser m is a reparametrisation the output h does
+not depend on, so it is held at its forward values and carries no gradient).
 
 The input projection that produces Wx from an input sequence x (the dense
 step in front of the recurrence; the blog page's register-caching paragraph
@@ -262,7 +262,12 @@ def slstm_backward(Wx, R, b=None, h0=None, c0=None, n0=None, m0=None, dh_seq=Non
     """Gradients of L = sum(h_seq*dh_seq) + sum(hT*dhT) + sum(cT*dcT) + sum(nT*dnT).
 
     The stabiliser m only rescales (c, n) jointly and h = o*c/n is invariant to
-    it, so m is held constant (no gradient flows through the max).
+    it, so m is held at its forward values (no gradient flows through the max).
+    For any loss of h this is the exact gradient; the upstream terms on the
+    stabilised final states cT, nT are differentiated with m_T held fixed,
+    which is the convention under which backward passes over consecutive time
+    chunks (final-state gradients of one chunk fed as dcT, dnT of the previous
+    one) compose to the whole-sequence gradient.
     """
     fw = slstm_forward(Wx, R, b, h0, c0, n0, m0, keep=True)
     R = np.asarray(R, np.float64)
@@ -304,13 +309,15 @@ def forward(cell, Wx, R, b=None, h0=None, c0=None, n0=None, m0=None, emulate_bf1
 
 
 def backward(cell, Wx, R, b=None, h0=None, c0=None, n0=None, m0=None, dh_seq=None,
-             dhT=None, dcT=None):
+             dhT=None, dcT=None, dnT=None):
+    """Gradients of sum(h_seq*dh_seq) + sum(hT*dhT) (+ sum(cT*dcT), + sum(nT*dnT))
+    for the cell; upstream terms a cell does not have are ignored."""
     if cell == "lstm":
-        return lstm_backward(Wx, R, b, h0, c0, dh_seq, dhT, dcT)
+        return lstm_backward(Wx, R, b, h0, c0, dh_seq=dh_seq, dhT=dhT, dcT=dcT)
     if cell == "gru":
-        return gru_backward(Wx, R, b, h0, dh_seq, dhT)
+        return gru_backward(Wx, R, b, h0, dh_seq=dh_seq, dhT=dhT)
     if cell == "slstm":
-        return slstm_backward(Wx, R, b, h0, c0, n0, m0, dh_seq, dhT, dcT)
+        return slstm_backward(Wx, R, b, h0, c0, n0, m0, dh_seq=dh_seq, dhT=dhT, dcT=dcT, dnT=dnT)
     raise ValueError(cell)
 
 

@@ -33,13 +33,14 @@ def S():
 def run_fb(S, d, cell="lstm"):
     dt = torch.bfloat16
     g = {k: torch.from_numpy(np.ascontiguousarray(d[k])).to("cuda", dt) for k in ("Wx", "R", "dh")}
-    for k in ("b", "h0", "c0", "n0", "m0", "dhT", "dcT"):
-        g[k] = torch.from_numpy(np.ascontiguousarray(d[k])).to("cuda", torch.float32)
+    for k in ("b", "h0", "c0", "n0", "m0", "dhT", "dcT", "dnT"):
+        if k in d:
+            g[k] = torch.from_numpy(np.ascontiguousarray(d[k])).to("cuda", torch.float32)
     sl = cell == "slstm"
     fw = S.forward(cell, g["Wx"], g["R"], g["b"], g["h0"], g["c0"], g["n0"] if sl else None,
                    g["m0"] if sl else None, train=True)
     gr = S.backward(fw, g["R"], g["h0"], g["c0"], g["dh"], g["dhT"], g["dcT"],
-                    n0=g["n0"] if sl else None)
+                    n0=g["n0"] if sl else None, dnT=g.get("dnT") if sl else None)
     torch.cuda.synchronize()
     return g, fw, gr
 
@@ -55,7 +56,7 @@ def check(S, d, label, cell="lstm"):
     ref_f = O.forward(cell, d["Wx"], d["R"], d["b"], d["h0"], d["c0"], d["n0"], d["m0"])
     if cell == "slstm":
         ref = O.slstm_backward(d["Wx"], d["R"], d["b"], d["h0"], d["c0"], d["n0"], d["m0"],
-                               dh_seq=d["dh"], dhT=d["dhT"], dcT=d["dcT"])
+                               dh_seq=d["dh"], dhT=d["dhT"], dcT=d["dcT"], dnT=d.get("dnT"))
     else:
         ref = O.backward(cell, d["Wx"], d["R"], d["b"], d["h0"], d["c0"], dh_seq=d["dh"],
                          dhT=d["dhT"], dcT=d["dcT"])
@@ -117,6 +118,8 @@ def test_backward_gru_slstm(S, cell, Dh, B, NH, T):
     d["dhT"] = rng.standard_normal(d["h0"].shape).astype(np.float32)
     d["dcT"] = (rng.standard_normal(d["h0"].shape).astype(np.float32) if cell == "slstm"
                 else np.zeros(d["h0"].shape, np.float32))
+    if cell == "slstm":
+        d["dnT"] = rng.standard_normal(d["h0"].shape).astype(np.float32)
     check(S, d, f"{cell}/Dh{Dh}/B{B}/NH{NH}/T{T}", cell)
 
 

@@ -31,6 +31,15 @@ MUTANTS = {
     # transposed gradient operand: R instead of R^T in the backward contraction
     "bwd_transpose": ("_recurrent_T",
                       lambda o: (lambda dp, R: o(dp, R[..., ::-1]))),
+    # upstream gradient of the final cell state ignored (LSTM and sLSTM)
+    "lstm_drops_dcT": ("lstm_backward", lambda o: (lambda *a, **k: o(*a, **{**k, "dcT": None}))),
+    "slstm_drops_dcT": ("slstm_backward", lambda o: (lambda *a, **k: o(*a, **{**k, "dcT": None}))),
+    # normaliser carry of the sLSTM backward started with the wrong sign
+    "slstm_dn_sign": ("slstm_backward",
+                      lambda o: (lambda *a, **k: o(*a, **{**k, "dnT": None if k.get("dnT") is None
+                                                          else -np.asarray(k["dnT"])}))),
+    # upstream gradient of the final hidden state ignored (every cell)
+    "drops_dhT": ("_bwd_common", lambda o: (lambda Wx, R, dh_seq, dhT: o(Wx, R, dh_seq, None))),
 }
 
 PINS = {
@@ -39,6 +48,7 @@ PINS = {
     "closed": lambda: (P.test_lstm_R0_closed_form(), P.test_gru_R0_closed_form(),
                        P.test_slstm_R0_weighted_average(), P.test_T1_scalar_closed_forms()),
     "fd": lambda: [P.test_backward_finite_differences(c) for c in ("lstm", "gru", "slstm")],
+    "chunks": lambda: [P.test_backward_composes_over_chunks(c) for c in ("lstm", "gru", "slstm")],
     "unstab": lambda: P.test_slstm_equals_unstabilised_form(),
     "stab_pair": lambda: P.test_slstm_stabilised_gate_pair_has_a_unit_member(),
 }

@@ -33,8 +33,9 @@ def _inp(cell, T=7, B=3, NH=2, Dh=5, seed=1, states="random", bias="normal", bac
 
 
 # ----------------------------------------------------------- torch pins ----
-def _torch_cell(cell, x, Rh, bh, h0, c0, dh=None):
-    """Run one head through torch.nn.LSTM/GRU (fp64); optionally backprop."""
+def _torch_cell(cell, x, Rh, bh, h0, c0, dh=None, dhT=None, dcT=None):
+    """Run one head through torch.nn.LSTM/GRU (fp64); optionally backprop
+    L = sum(out*dh) + sum(hn*dhT) (+ sum(cn*dcT) for the LSTM)."""
     T, B, GD = x.shape
     Dh = Rh.shape[0]
     mod = (torch.nn.LSTM if cell == "lstm" else torch.nn.GRU)(GD, Dh, dtype=torch.float64)
@@ -55,7 +56,12 @@ def _torch_cell(cell, x, Rh, bh, h0, c0, dh=None):
     if cn is not None:
         res["cT"] = cn[0].detach().numpy()
     if dh is not None:
-        (out * torch.from_numpy(dh.astype(np.float64))).sum().backward()
+        loss = (out * torch.from_numpy(dh.astype(np.float64))).sum()
+        if dhT is not None:
+            loss = loss + (hn[0] * torch.from_numpy(dhT.astype(np.float64))).sum()
+        if dcT is not None and cn is not None:
+            loss = loss + (cn[0] * torch.from_numpy(dcT.astype(np.float64))).sum()
+        loss.backward()
         res["dWx"] = xt.grad.numpy()
         res["dR"] = mod.weight_hh_l0.grad.numpy().T
         res["db"] = mod.bias_hh_l0.grad.numpy()
@@ -77,13 +83,24 @@ def test_forward_matches_torch(cell):
             np.testing.assert_allclose(o["cT"][:, h], ref["cT"], rtol=0, atol=1e-12)
 
 
+def _upstream(d, seed):
+    """Random upstream gradients of the final states (the workloads use zeros,
+    which would leave the dhT / dcT / dnT paths of the backward unchecked)."""
+    rng = np.random.default_rng(seed)
+    shp = d["h0"].shape
+    return {k: rng.standard_normal(shp) for k in ("dhT", "dcT", "dnT")}
+
+
 @pytest.mark.parametrize("cell", ["lstm", "gru"])
 def test_backward_matches_torch_autograd(cell):
     d = _inp(cell, backward=True)
-    g = O.backward(cell, d["Wx"], d["R"], d["b"], d["h0"], d["c0"], dh_seq=d["dh"])
+    up = _upstream(d, 11)
+    g = O.backward(cell, d["Wx"], d["R"], d["b"], d["h0"], d["c0"], dh_seq=d["dh"],
+                   dhT=up["dhT"], dcT=up["dcT"])
     for h in range(d["NH"]):
         ref = _torch_cell(cell, d["Wx"][:, :, h], d["R"][h], d["b"][h], d["h0"][:, h],
-                          d["c0"][:, h], dh=d["dh"][:, :, h])
+                          d["c0"][:, h], dh=d["dh"][:, :, h], dhT=up["dhT"][:, h],
+                          dcT=up["dcT"][:, h])
         np.testing.assert_allclose(g["dWx"][:, :, h], ref["dWx"], rtol=0, atol=1e-12)
         np.testing.assert_allclose(g["dR"][h], ref["dR"], rtol=0, atol=1e-11)
         np.testing.assert_allclose(g["db"][h], ref["db"], rtol=0, atol=1e-11)
@@ -263,20 +280,44 @@ def test_slstm_equals_unstabilised_form():
 
 
 # --------------------------------------------------- finite differences ----
-def _loss(cell, d, Wx, R, b, h0, c0, n0):
+def _loss(cell, d, up, Wx, R, b, h0, c0, n0, mT0=None):
+    """L = sum(h_seq*dh) + sum(hT*dhT) + sum(cT*dcT) + sum(nT*dnT) (the terms the cell has).
+
+    sLSTM: the final (c, n) are differentiated with the stabiliser held at its
+    unperturbed final value mT0.  The stabilised pair equals the unstabilised
+    one times exp(-m_T), and the unstabilised one does not depend on m at all,
+    so (c_T, n_T) at a held stabiliser are the perturbed run's (c_T, n_T) times
+    exp(m_T - mT0).  That is the convention under which backward passes over
+    consecutive time chunks compose (test_backward_composes_over_chunks).
+    """
     o = O.forward(cell, Wx, R, b, h0, c0, n0, d["m0"])
-    return float((o["h_seq"] * d["dh"]).sum())
+    loss = float((o["h_seq"] * d["dh"]).sum()) + float((o["hT"] * up["dhT"]).sum())
+    scale = 1.0 if mT0 is None else np.exp(o["mT"] - mT0)
+    if "cT" in o:
+        loss += float((o["cT"] * scale * up["dcT"]).sum())
+    if "nT" in o:
+        loss += float((o["nT"] * scale * up["dnT"]).sum())
+    return loss
 
 
 @pytest.mark.parametrize("cell", ["lstm", "gru", "slstm"])
 def test_backward_finite_differences(cell):
     d = _inp(cell, T=5, B=2, NH=2, Dh=3, seed=3, backward=True)
+    up = _upstream(d, 12)
     args = {k: d[k].astype(np.float64).copy() for k in ("Wx", "R", "b", "h0", "c0", "n0")}
     g = O.backward(cell, args["Wx"], args["R"], args["b"], args["h0"], args["c0"],
-                   args["n0"], d["m0"], dh_seq=d["dh"])
-    names = {"Wx": "dWx", "R": "dR", "b": "db", "h0": "dh0", "c0": "dc0"}
+                   args["n0"], d["m0"], dh_seq=d["dh"], dhT=up["dhT"], dcT=up["dcT"],
+                   dnT=up["dnT"])
+    names = {"Wx": "dWx", "R": "dR", "b": "db", "h0": "dh0", "c0": "dc0", "n0": "dn0"}
+    if cell != "slstm":
+        names.pop("n0")
     if cell == "gru":
         names.pop("c0")
+    mT0 = None
+    if cell == "slstm":
+        mT0 = O.forward(cell, args["Wx"], args["R"], args["b"], args["h0"], args["c0"],
+                        args["n0"], d["m0"])["mT"]
+    args["mT0"] = mT0
     rng = np.random.default_rng(0)
     eps = 1e-6
     for src, gname in names.items():
@@ -285,13 +326,38 @@ def test_backward_finite_differences(cell):
             idx = np.unravel_index(flat, x.shape)
             old = x[idx]
             x[idx] = old + eps
-            lp = _loss(cell, d, **args)
+            lp = _loss(cell, d, up, **args)
             x[idx] = old - eps
-            lm = _loss(cell, d, **args)
+            lm = _loss(cell, d, up, **args)
             x[idx] = old
             fd = (lp - lm) / (2 * eps)
             an = g[gname][idx]
             assert abs(fd - an) <= 1e-7 * max(1.0, abs(an)), (src, idx, fd, an)
+
+
+@pytest.mark.parametrize("cell", ["lstm", "gru", "slstm"])
+def test_backward_composes_over_chunks(cell):
+    """Backward over steps [0, T) of a loss on h_seq alone == backward over the
+    last chunk, whose dh0 (dc0, dn0) are fed as the upstream dhT (dcT, dnT) of
+    the first chunk's backward.  This pins every upstream-gradient path of the
+    backward (the initial-state gradients of one call and the final-state
+    inputs of the other) against the whole-sequence gradient, which the finite
+    differences and torch autograd pin."""
+    d = _inp(cell, T=9, B=3, NH=2, Dh=4, seed=5, backward=True)
+    a = (d["Wx"], d["R"], d["b"])
+    full = O.backward(cell, *a, d["h0"], d["c0"], d["n0"], d["m0"], dh_seq=d["dh"])
+    k = 4
+    f1 = O.forward(cell, d["Wx"][:k], d["R"], d["b"], d["h0"], d["c0"], d["n0"], d["m0"])
+    g2 = O.backward(cell, d["Wx"][k:], d["R"], d["b"], f1["hT"], f1.get("cT"), f1.get("nT"),
+                    f1.get("mT"), dh_seq=d["dh"][k:])
+    g1 = O.backward(cell, d["Wx"][:k], d["R"], d["b"], d["h0"], d["c0"], d["n0"], d["m0"],
+                    dh_seq=d["dh"][:k], dhT=g2["dh0"], dcT=g2.get("dc0"), dnT=g2.get("dn0"))
+    np.testing.assert_allclose(np.concatenate([g1["dWx"], g2["dWx"]]), full["dWx"], atol=1e-12)
+    np.testing.assert_allclose(g1["dR"] + g2["dR"], full["dR"], atol=1e-11)
+    np.testing.assert_allclose(g1["db"] + g2["db"], full["db"], atol=1e-11)
+    for key in ("dh0", "dc0", "dn0"):
+        if key in full:
+            np.testing.assert_allclose(g1[key], full[key], atol=1e-12)
 
 
 # ------------------------------------------------------ input projection ----
