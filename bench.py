@@ -20,6 +20,7 @@ oracle (the reference arm) on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import atexit
 import hashlib
 import json
 import os
@@ -78,23 +79,31 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples (every 50 ms) of the SM clock and throttle reasons of
+    this process's GPU while the steps run.
 
-    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+    Every GPU is queried with its UUID and the lines of ours are kept (the UUID
+    torch reports, matched without its "GPU-" prefix; with a single visible
+    GPU its line is taken).  nvidia-smi needs a few hundred ms to start, so the
+    sampler is started before the warm-up and ``wait_first`` holds the timing
+    back until the first sample has arrived; samples cover the untimed
+    clock soak and the timed region, both of which run the measured steps."""
+
+    Q = ("uuid,clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_id):
-        self.gpu = gpu_id
+    def __init__(self, uuid):
+        self.uuid = str(uuid).lower().removeprefix("gpu-")
         self.proc = None
         self.lines = []
+        self.first = threading.Event()
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except (OSError, FileNotFoundError):
@@ -104,6 +113,11 @@ class ClockSampler:
     def _read(self):
         for ln in self.proc.stdout:
             self.lines.append(ln.strip())
+            self.first.set()
+
+    def wait_first(self, timeout=5.0):
+        if self.proc is not None:
+            self.first.wait(timeout)
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -113,19 +127,24 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
+    def _ours(self):
+        rows = [[x.strip() for x in ln.split(",")] for ln in self.lines]
+        rows = [r for r in rows if len(r) >= 8]
+        uuids = {r[0].lower().removeprefix("gpu-") for r in rows}
+        if self.uuid in uuids:
+            return [r for r in rows if r[0].lower().removeprefix("gpu-") == self.uuid]
+        return rows if len(uuids) == 1 else []
+
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 7:
-                continue
+        for parts in self._ours():
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
             except ValueError:
                 continue
-            for nm, v in zip(names, parts[3:7]):
+            for nm, v in zip(names, parts[4:8]):
                 if v.lower() == "active":
                     reasons.add(nm)
         if not sm:
@@ -135,9 +154,12 @@ class ClockSampler:
 
 
 def oracle_rate(w, d, budget_s=10.0):
-    """fp64 oracle forward (+backward) on the host cores: TFLOP/s over a bounded sample."""
+    """fp64 oracle forward (+backward) on the host cores: TFLOP/s over a bounded
+    sample.  Also returns the threads it kept busy on average: process CPU time
+    (all threads, numpy's BLAS included) over wall time."""
     from oracle import rnn_oracle as O
     f_full = flops_per_step(w)
+    c0 = time.process_time()
     t0 = time.perf_counter()
     reps = 0
     while True:
@@ -149,16 +171,13 @@ def oracle_rate(w, d, budget_s=10.0):
         el = time.perf_counter() - t0
         if el >= budget_s or reps >= 1000:
             break
-    return f_full * reps / el / 1e12, reps, el
+    busy = (time.process_time() - c0) / max(el, 1e-9)
+    return f_full * reps / el / 1e12, reps, el, busy
 
 
-def blas_threads():
-    try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
-        return max(n) if n else 1
-    except Exception:
-        return os.cpu_count() or 1
+def threads_used(busy):
+    """Threads the oracle kept busy, rounded (at least 1), for ``cores``."""
+    return max(1, int(round(busy)))
 
 
 def sample_workload(w, max_T):
@@ -176,14 +195,17 @@ def run_reference(args, w, rank):
     d = workload_inputs(args.workload, T=sw["T"])
     for _ in range(args.warmup):
         oracle_rate(sw, d, budget_s=0.0)
-    times = []
+    times, busy = [], []
     for _ in range(args.steps):
-        rate, reps, el = oracle_rate(sw, d, budget_s=0.0)
+        rate, reps, el, b = oracle_rate(sw, d, budget_s=0.0)
         times.append(el)
+        busy.append(b)
     t = sum(times) / len(times)
     value = flops_per_step(sw) / t / 1e12
-    cores = blas_threads()
-    sample = f"{args.workload} with T cut to {sw['T']} steps, one oracle pass per step"
+    cores = threads_used(statistics.mean(busy))
+    sample = (f"{args.workload} with T cut to {sw['T']} steps, one oracle pass per step "
+              f"(mean of {args.steps}); {statistics.mean(busy):.2f} threads busy on average "
+              f"of {os.cpu_count()} host cores")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -298,15 +320,27 @@ def run_ours(args, w, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    clk = ClockSampler(torch.cuda.get_device_properties(dev).uuid).__enter__()
+    atexit.register(clk.__exit__, None, None, None)  # no stray nvidia-smi on an error
     w0 = time.perf_counter()
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize(dev)
     if S.rnn_read_status(ws):
         raise S.RnnError(S.rnn_read_status(ws), "warm-up (device)")
-    if args.steps is None:  # ~2 s of timed work so the clock samples see it
-        t1 = (time.perf_counter() - w0) / max(args.warmup, 3)
+    t1 = (time.perf_counter() - w0) / max(args.warmup, 3)
+    if args.steps is None:  # ~2 s of timed work
         args.steps = int(min(3000, max(20, 2.0 / max(t1, 1e-5))))
+    # untimed clock soak: the same steps for ~1 s (and until nvidia-smi has
+    # reported), so that the clock record covers the GPU under this load even
+    # when the timed region itself is a few ms long
+    clk.wait_first()
+    soak0 = time.perf_counter()
+    while time.perf_counter() - soak0 < 1.0:
+        for _ in range(max(1, int(0.05 / max(t1, 1e-5)))):
+            flush.fill_(0.0)
+            step()
+        torch.cuda.synchronize(dev)
 
     # ---- device-resident timing: events around each step, L2 flushed between
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -315,16 +349,15 @@ def run_ours(args, w, rank, world, local_rank):
     bev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)] if w["backward"] else None
     barrier()
-    uuid = str(torch.cuda.get_device_properties(dev).uuid)
-    with ClockSampler(uuid if uuid.startswith("GPU-") else f"GPU-{uuid}") as clk:
-        wall0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.fill_(float(i))
-            ev[i][0].record(stream)
-            step(bev=bev[i] if bev else None)
-            ev[i][1].record(stream)
-        barrier()
-        wall = time.perf_counter() - wall0
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        step(bev=bev[i] if bev else None)
+        ev[i][1].record(stream)
+    barrier()
+    wall = time.perf_counter() - wall0
+    clk.__exit__(None, None, None)
     per = [a.elapsed_time(b) for a, b in ev]  # ms
     t_step = sum(per) / len(per) / 1e3
     t_bwd = (sum(a.elapsed_time(b) for a, b in bev) / len(bev) / 1e3) if bev else None
@@ -452,10 +485,27 @@ def run_ours(args, w, rank, world, local_rank):
         "e2e": {"value": world * fl_step / t_e2e / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * launches_per_step,
-        "clocks": clk.summary(),
+        "clocks": {**clk.summary(),
+                   "window": "nvidia-smi every 50 ms over a 1 s untimed soak of the same steps "
+                             "and the timed region"},
         "wall_timed_s": wall,
     }
     return res
+
+
+def free_port() -> int:
+    import socket
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as so:
+        so.bind(("127.0.0.1", 0))
+        return so.getsockname()[1]
+
+
+def rank_launch_cmd(n: int, script: str, argv: list) -> list:
+    """torch.distributed.run command that starts ``script`` as n ranks on this
+    node (one per GPU), rendezvous on 127.0.0.1."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            f"--nproc-per-node={int(n)}", "--master-addr", "127.0.0.1",
+            "--master-port", str(free_port()), script, *argv]
 
 
 def main():
@@ -469,6 +519,11 @@ def main():
     ap.add_argument("--cluster", type=int, default=0, help="CTAs per head (0 = automatic)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ and args.impl == "ours":
+        # no launcher around us: start one rank per GPU ourselves
+        cmd = rank_launch_cmd(args.gpus, os.path.abspath(__file__), sys.argv[1:])
+        sys.exit(subprocess.call(cmd))
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -488,15 +543,18 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         sw = sample_workload(w, 256 if w["Dh"] <= 256 else 64)
         d = workload_inputs(args.workload, T=sw["T"])
-        rate, reps, el = oracle_rate(sw, d, budget_s=10.0)
-        cpu = {"value": rate, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": f"{args.workload} with T cut to {sw['T']}, {reps} oracle passes in {el:.1f} s"}
+        rate, reps, el, busy = oracle_rate(sw, d, budget_s=10.0)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads_used(busy), "kind": "oracle",
+               "sample": (f"{args.workload} with T cut to {sw['T']}, {reps} oracle passes in "
+                          f"{el:.1f} s; {busy:.2f} threads busy on average of {os.cpu_count()} "
+                          "host cores")}
 
     if world > 1:
         import torch
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
+        world = dist.get_world_size()  # n_gpus: the ranks that joined
     res = run_ours(args, w, rank, world, local_rank)
     if world > 1:
         import torch.distributed as dist

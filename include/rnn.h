@@ -251,15 +251,22 @@ const char* rnn_status_str(int status);
  * device status word) lives in a 4096-byte file-scope __device__ array of the
  * library, held by every GPU that loads the library until the process exits.
  * Calls needing more scratch than that return RNN_ERR_SCRATCH_LIMIT.  The first
- * call on a device looks up the array's device address (cudaGetSymbolAddress),
- * so make that first call before any stream capture.  Every call shares the
- * array and clears the status word it uses; calls that overlap on the GPU race
- * on it, and their device-side timeout status is not reported.  Allocates
- * nothing (no cudaMalloc / cudaFree, no allocating library call). */
+ * call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * and keeps it for the life of the process, so make that first call before any
+ * stream capture, and do not call cudaDeviceReset on that device afterwards (the
+ * kept address would then be stale).  Every call shares the array and clears
+ * the status word it uses.  Because the caller cannot read the array, the
+ * call's device status is delivered through `device_status`: NULL (not
+ * reported), or an int the caller owns in device memory or page-locked host
+ * memory, which receives the status word by a copy ordered on `stream` after
+ * the recurrence -- 0 when every bounded wait completed, nonzero when one ran
+ * out (RNN_ERR_TIMEOUT: outputs invalid).  Calls that overlap on the GPU race on
+ * the array, so a status delivered to one of them may belong to the other.
+ * Allocates nothing (no cudaMalloc / cudaFree, no allocating library call). */
 int rnn_fwd_noalloc(const rnn_desc_t* desc, const void* Wx, const void* R, const float* bias,
                     const float* h0, const float* c0, const float* n0, const float* m0,
                     void* h_seq, float* hT, float* cT, float* nT, float* mT, void* stash,
-                    void* stream);
+                    int* device_status, void* stream);
 
 #ifdef __cplusplus
 }

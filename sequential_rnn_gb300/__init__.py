@@ -100,11 +100,23 @@ def rnn_fwd(desc, Wx, R, bias, h0, c0, n0, m0, h_seq, hT, cT, nT, mT, stash, wor
 
 
 def rnn_fwd_noalloc(desc, Wx, R, bias, h0, c0, n0, m0, h_seq, hT, cT, nT, mT, stash,
-                    stream=None) -> int:
-    """rnn_fwd without a workspace, for callers that must not allocate device memory."""
+                    device_status=None, stream=None) -> int:
+    """rnn_fwd without a workspace, for callers that must not allocate device memory.
+
+    ``device_status``: None or an int32 tensor (device, or pinned host) whose
+    first element receives the call's device status word (0 = OK) on the stream.
+    """
+    if device_status is None:
+        sp = None
+    elif device_status.dtype != torch.int32 or device_status.numel() < 1:
+        raise ValueError("device_status must be an int32 tensor")
+    elif device_status.is_cuda:
+        sp = _ptr(device_status)
+    else:
+        sp = _host_ptr(device_status)
     return int(_lib.load().rnn_fwd_noalloc(
         ctypes.byref(desc), _ptr(Wx), _ptr(R), _ptr(bias), _ptr(h0), _ptr(c0), _ptr(n0), _ptr(m0),
-        _ptr(h_seq), _ptr(hT), _ptr(cT), _ptr(nT), _ptr(mT), _ptr(stash), _stream(stream)))
+        _ptr(h_seq), _ptr(hT), _ptr(cT), _ptr(nT), _ptr(mT), _ptr(stash), sp, _stream(stream)))
 
 
 def rnn_bwd(desc, R, h0, c0, n0, h_seq, stash, dh_seq, dhT, dcT, dnT, dWx, dR, db, dh0, dc0, dn0,

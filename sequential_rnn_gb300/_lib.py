@@ -51,7 +51,7 @@ _SIGS = {
     "rnn_sync_floor": (_I, [_DESC, _I, _P, _SZ, _P]),
     "rnn_fwd_config": (_I, [_DESC, ctypes.POINTER(ctypes.c_int32)]),
     "rnn_status_str": (ctypes.c_char_p, [_I]),
-    "rnn_fwd_noalloc": (_I, [_DESC] + [_P] * 14),
+    "rnn_fwd_noalloc": (_I, [_DESC] + [_P] * 15),
     "rnn_input_proj": (_I, [ctypes.c_int32] * 3 + [_P] * 5 + [_SZ, _P]),
     "rnn_stack_workspace_size": (_SZ, [_DESC, ctypes.c_int32, ctypes.c_int32]),
     "rnn_stack_fwd": (_I, [_DESC] + [ctypes.c_int32] * 3 + [_P] * 16 + [_SZ, _P]),

@@ -13,6 +13,9 @@
 // holds it until the process exits, and all calls share it.  A call clears the
 // part that must start at zero (the device status word); calls whose work
 // overlaps on the GPU (different streams, no ordering between them) race on it.
+// Since the caller cannot name the array, a call copies its status word, once
+// the recurrence is done, into an int the caller owns (device memory or
+// page-locked host memory) when it passes one.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -39,7 +42,8 @@ cudaError_t g_setup_err[kMaxDevices];
 extern "C" int rnn_fwd_noalloc(const rnn_desc_t* desc, const void* Wx, const void* R,
                                const float* bias, const float* h0, const float* c0,
                                const float* n0, const float* m0, void* h_seq, float* hT, float* cT,
-                               float* nT, float* mT, void* stash, void* stream) {
+                               float* nT, float* mT, void* stash, int* device_status,
+                               void* stream) {
   if (desc == nullptr) return RNN_ERR_INVALID_ARG;
   const size_t need = rnn_workspace_size(desc, 0);
   if (need == 0) return RNN_ERR_INVALID_ARG;
@@ -52,6 +56,19 @@ extern "C" int rnn_fwd_noalloc(const rnn_desc_t* desc, const void* Wx, const voi
     g_scratch_ptr[dev] = p;
   });
   if (g_setup_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) return RNN_ERR_LAUNCH;
-  return rnn_fwd(desc, Wx, R, bias, h0, c0, n0, m0, h_seq, hT, cT, nT, mT, stash,
-                 g_scratch_ptr[dev], kNoAllocScratchBytes, stream);
+  // Clear the status word here as well: a call that launches nothing (B == 0,
+  // NH == 0) must not hand on an earlier call's status.
+  if (device_status != nullptr &&
+      cudaMemsetAsync(g_scratch_ptr[dev], 0, sizeof(int), static_cast<cudaStream_t>(stream)) !=
+          cudaSuccess)
+    return RNN_ERR_LAUNCH;
+  const int st = rnn_fwd(desc, Wx, R, bias, h0, c0, n0, m0, h_seq, hT, cT, nT, mT, stash,
+                         g_scratch_ptr[dev], kNoAllocScratchBytes, stream);
+  if (st != RNN_OK || device_status == nullptr) return st;
+  // Stream-ordered copy of the status word (no allocation; cudaMemcpyDefault
+  // resolves device or page-locked host memory through unified addressing).
+  if (cudaMemcpyAsync(device_status, g_scratch_ptr[dev], sizeof(int), cudaMemcpyDefault,
+                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return RNN_ERR_LAUNCH;
+  return RNN_OK;
 }

@@ -1,0 +1,86 @@
+"""Host-side logic of bench.py (CPU only): the rank launcher behind
+``--gpus N``, the clock-record parser and the oracle's thread count.
+
+``python bench.py --gpus N`` without an outside launcher must start N ranks
+itself (one per GPU) that agree on the world size; here the same launch command
+runs a stub rank script over gloo instead of the GPU step.
+"""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+STUB = r'''
+import json, os
+import torch
+import torch.distributed as dist
+dist.init_process_group("gloo")
+t = torch.ones(1)
+dist.all_reduce(t)
+print(json.dumps({"rank": dist.get_rank(), "n_gpus": dist.get_world_size(),
+                  "sum": int(t.item()), "argv": os.sys.argv[1:]}), flush=True)
+dist.destroy_process_group()
+'''
+
+
+def test_rank_launcher_starts_n_ranks(tmp_path):
+    stub = tmp_path / "stub_rank.py"
+    stub.write_text(STUB)
+    cmd = bench.rank_launch_cmd(2, str(stub), ["--steps", "3"])
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=240, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(ln) for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert sorted(x["rank"] for x in lines) == [0, 1]
+    assert all(x["n_gpus"] == 2 and x["sum"] == 2 for x in lines)
+    assert all(x["argv"] == ["--steps", "3"] for x in lines)
+
+
+def test_bench_relaunches_itself_without_a_launcher(monkeypatch):
+    seen = {}
+
+    def fake_call(cmd):
+        seen["cmd"] = cmd
+        return 0
+
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    monkeypatch.setattr(bench.subprocess, "call", fake_call)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--gpus", "4", "--steps", "5"])
+    with pytest.raises(SystemExit) as e:
+        bench.main()
+    assert e.value.code == 0
+    cmd = seen["cmd"]
+    assert "--nproc-per-node=4" in cmd and "torch.distributed.run" in cmd
+    assert cmd[-4:] == ["--gpus", "4", "--steps", "5"]
+    assert os.path.samefile(cmd[-5], os.path.join(ROOT, "bench.py"))
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
+
+
+def test_clock_sampler_keeps_only_this_gpu():
+    c = bench.ClockSampler("abcd-1234")
+    c.lines = [
+        "GPU-abcd-1234, 2070, 2070, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "GPU-ffff-0000, 900, 2070, 0x0, Active, Not Active, Not Active, Not Active",
+        "GPU-abcd-1234, 2060, 2070, 0x4, Not Active, Not Active, Not Active, Active",
+    ]
+    s = c.summary()
+    assert s["samples"] == 2 and s["sm_mhz"] == 2065 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"]
+    # a single visible GPU whose UUID torch reports differently is still taken
+    c1 = bench.ClockSampler("zzzz")
+    c1.lines = ["GPU-abcd-1234, 1500, 2070, 0x0, Not Active, Not Active, Not Active, Not Active"]
+    assert c1.summary()["samples"] == 1
+
+
+def test_threads_used_rounds_and_floors():
+    assert bench.threads_used(0.2) == 1
+    assert bench.threads_used(1.4) == 1
+    assert bench.threads_used(11.6) == 12
