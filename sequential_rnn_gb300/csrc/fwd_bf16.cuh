@@ -22,8 +22,7 @@
 // layout, and the accumulators start from Wx + bias.  Gate math runs on the accumulator
 // registers; each thread owns whole (unit, batch) cells, so no gate exchange
 // is needed.  Sigmoid gate rows of R, Wx and bias are pre-scaled by 1/2 so a
-// sigmoid is one hardware tanh and one FMA: sigmoid(x) = (1 + tanh(x/2)) / 2;
-// LSTM/GRU gate activations of two cells share one packed fp16x2 tanh.
+// sigmoid is one hardware tanh and one FMA: sigmoid(x) = (1 + tanh(x/2)) / 2.
 //
 // Exchange of h_t: CS == 1 -> shared memory + one named barrier per step.
 // CS > 1 -> each warp stages its bf16 slice of h_t in shared memory, then its
@@ -156,9 +155,11 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   using C = FwdCfg<CELL, DH, UG, NT, KREG, HS>;
   constexpr int G = C::G, GD = C::GD, MT = C::MT, KS = C::KS, KSM = C::KSM, NB = C::NB;
   constexpr int HPB = C::HPB, NE = C::NE, NSLOT = C::NSLOT, NTILE = C::NTILE, NQ = C::NQ;
-  // A cluster step is latency-bound (few warps per SM): two k chains and plain
-  // fp32 tanh.  One CTA per head is throughput-bound: packed fp16x2 tanh.
-  constexpr bool SPLITK = C::SPLITK || CL;
+  // Two k chains per m tile, and plain fp32 tanh: on GB300 tanh.approx.f16x2
+  // takes 16 cycles of the multi-function unit per warp (two f32 tanh take the
+  // same) and adds pack / unpack conversions (12 x 64 LSTM, one CTA per head:
+  // 399 -> 383 ns per step with both changes).
+  constexpr bool SPLITK = true;
   // HS = 1 (hi and lo as separate B operands) over >= 8 k16 steps: hi and lo
   // each on two chains (even/odd k pairs).  HS = 2: hi and lo in one n8 tile.
   constexpr bool HLO = HS == 1, HN = HS == 2;
@@ -168,7 +169,6 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   // bounds it (4x256 sLSTM: 8-long chains took ~640 cycles for 32 MMAs).
   // At 8 k16 steps two chains per tile measured faster.
   constexpr bool CH4 = !HLO && CL && KS >= 16;
-  constexpr bool PACKED_TANH = !CL;
   // One CTA per head (all warps meet at a barrier every step): the next step's
   // Wx is primed while this step's MMAs are in flight, in a second accumulator
   // set.  A cluster step primes it while h_t travels to the peers instead.
@@ -417,16 +417,25 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     // Wait for the next Wx stage, move it into accumulator layout and release
     // the stage.  Runs while the step's MMAs are in flight (EARLY_PREP) or
     // after h_t is published, off the recurrence's critical path.
-    auto prep = [&]() -> bool {
-      // refill the stage the previous prime consumed (a whole step ago) with
-      // step np - 1 + PD, then wait for step np's group (PD - 1 younger ones
-      // may still be in flight)
-      if (np > 0) fetch(np - 1 + PD);
-      cp_async_wait<PD - 1>();
+    uint32_t wxr[NT][NQ * 4];  // the next step's Wx values, raw bf16 pairs
+    // First half of a prime: wait for step np's copies and load its values.
+    // Cluster variants refill the stage the previous prime consumed (a whole
+    // step ago) with step np - 1 + PD first, leaving PD - 1 younger groups in
+    // flight.  The one-CTA variant (EARLY_PREP) runs this half at the top of a
+    // step, before its MMAs (shared-memory instructions issued behind a burst of
+    // mma.sync wait for the burst), and issues the refill later in the step
+    // (late_fetch), so PD - 2 younger groups are in flight here.
+    auto prep_load = [&]() {
+      if (!EARLY_PREP) {
+        if (np > 0) fetch(np - 1 + PD);
+        cp_async_wait<PD - 1>();
+      } else {
+        if (np > 0) cp_async_wait<PD - 2>();
+        else cp_async_wait<PD - 1>();
+      }
       __syncwarp();
       const uint32_t stage = s_wx + (uint32_t)(np % PD) * stage_bytes;
       ++np;
-      uint32_t wxr[NT][NQ * 4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -444,6 +453,17 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
             wxr[nt][4 * q + 1] = r2[1];
           }
         }
+    };
+
+    // The one-CTA refill of the stage step np - 2 used (this warp's own columns:
+    // no other warp reads them) with step np - 2 + PD.  Issued after the gate
+    // math, where the load/store unit is idle (at the top of a step it cost
+    // ~35 ns more per step, 12 x 64 LSTM).
+    auto late_fetch = [&]() {
+      if (EARLY_PREP && np >= 2) fetch(np - 2 + PD);
+    };
+    // Second half: the loaded values into accumulator layout, scaled, plus bias.
+    auto prep_fma = [&]() {
 #pragma unroll
       for (int us = 0; us < NSLOT; ++us)
 #pragma unroll
@@ -467,6 +487,10 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) A[MT - 1][nt][2] = A[MT - 1][nt][3] = 0.f;
       }
+    };
+    auto prep = [&]() -> bool {
+      prep_load();
+      prep_fma();
       return true;
     };
     if (!dead && T > 0 && !prep()) dead = true;
@@ -511,6 +535,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
 #pragma unroll
               for (int q = 0; q < 4; ++q) acc3[mt][nt][q] = acc4[mt][nt][q] = 0.f;
         }
+        if (EARLY_PREP && send) prep_load();
         // ---- acc += R^T h_{t-1}
         const uint32_t hb = s_h + (uint32_t)(t & 1) * NB * HPB + lm_off;
 #pragma unroll
@@ -557,8 +582,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
             }
           }
         }
-        // next step's Wx while the MMAs run
-        if (EARLY_PREP && send && !prep()) dead = true;
+        // next step's Wx into accumulator layout while the MMAs run
+        if (EARLY_PREP && send) prep_fma();
         if (SPLITK) {
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
@@ -595,10 +620,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 r[g] = UG == 16 ? acc[g][nt][us * 2 + e] : acc[g / 2][nt][(g % 2) * 2 + e];
               float h;
               if (CELL == kLSTM) {  // r[i,f,o] hold x/2
-                const float2 t_if = PACKED_TANH ? tanh2_fast(r[0], r[1])
-                                                : make_float2(tanh_fast(r[0]), tanh_fast(r[1]));
-                const float2 t_zo = PACKED_TANH ? tanh2_fast(r[2], r[3])
-                                                : make_float2(tanh_fast(r[2]), tanh_fast(r[3]));
+                const float2 t_if = make_float2(tanh_fast(r[0]), tanh_fast(r[1]));
+                const float2 t_zo = make_float2(tanh_fast(r[2]), tanh_fast(r[3]));
                 const float ig = fmaf(0.5f, t_if.x, 0.5f);
                 const float fg = fmaf(0.5f, t_if.y, 0.5f);
                 const float zg = t_zo.x;
@@ -613,8 +636,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                   act[3][ei] = og;
                 }
               } else if (CELL == kGRU) {  // r[r,z] hold x/2; r[n] = R_n h + b_n
-                const float2 t_rz = PACKED_TANH ? tanh2_fast(r[0], r[1])
-                                                : make_float2(tanh_fast(r[0]), tanh_fast(r[1]));
+                const float2 t_rz = make_float2(tanh_fast(r[0]), tanh_fast(r[1]));
                 const float rg = fmaf(0.5f, t_rz.x, 0.5f);
                 const float zg = fmaf(0.5f, t_rz.y, 0.5f);
                 const float ng = tanh_fast(fmaf(rg, r[2], wxn[ei]));
@@ -667,6 +689,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
               st_h[ei] = h;
             }
 
+        late_fetch();
         // training stash of this step, per cell: four gate values [T,B,NH,4Dh] and
         // the state the backward needs [T,B,NH,Dh] (LSTM c_t, GRU h_t, sLSTM c_t
         // plus n_t in a third array).  GRU slots: r, z, n, R_n h + b_n.

@@ -174,14 +174,6 @@ __device__ __forceinline__ float tanh_fast(float x) {
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// Two hardware tanh at once on a packed fp16 pair (PTX tanh.approx.f16x2):
-// returns tanh(a), tanh(b) in fp32.  fp16 keeps 11 significant bits.
-__device__ __forceinline__ float2 tanh2_fast(float a, float b) {
-  __half2 x = __floats2half2_rn(a, b);
-  uint32_t xi = *reinterpret_cast<uint32_t*>(&x), yi;
-  asm("tanh.approx.f16x2 %0, %1;" : "=r"(yi) : "r"(xi));
-  return __half22float2(*reinterpret_cast<__half2*>(&yi));
-}
 // sigmoid(x) = (1 + tanh(x/2)) / 2  (identity), on the hardware tanh.
 __device__ __forceinline__ float sigmoid_fast(float x) { return fmaf(0.5f, tanh_fast(0.5f * x), 0.5f); }
 
