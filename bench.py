@@ -367,22 +367,35 @@ def run_ours(args, w, rank, world, local_rank):
     if S.rnn_read_status(ws):
         raise S.RnnError(S.rnn_read_status(ws), "timed region (device)")
 
-    # ---- sync floor of the same launch shape
+    # ---- sync floor of the same launch shape, and of every other shape the
+    #      library admits for this workload (CTAs per head 1..16): the smallest
+    #      is the floor no launch choice can go below
     fl_ws = torch.zeros(256, dtype=torch.uint8, device=dev)
-    fdesc = S.make_desc(cell, w["dtype"], T, Bsz, NH, Dh, 0, args.cluster)
     fe = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    for _ in range(3):
-        S.rnn_sync_floor(fdesc, T, fl_ws, stream)
-    fl = []
-    for _ in range(10):
-        fe[0].record(stream)
-        st = S.rnn_sync_floor(fdesc, T, fl_ws, stream)
-        fe[1].record(stream)
-        torch.cuda.synchronize(dev)
-        if st:
-            raise S.RnnError(st, "rnn_sync_floor")
-        fl.append(fe[0].elapsed_time(fe[1]) / 1e3)
-    t_floor = statistics.median(fl) / T
+
+    def sync_floor(cluster):
+        fdesc = S.make_desc(cell, w["dtype"], T, Bsz, NH, Dh, 0, cluster)
+        for _ in range(3):
+            S.rnn_sync_floor(fdesc, T, fl_ws, stream)
+        fl = []
+        for _ in range(10):
+            fe[0].record(stream)
+            st = S.rnn_sync_floor(fdesc, T, fl_ws, stream)
+            fe[1].record(stream)
+            torch.cuda.synchronize(dev)
+            if st:
+                raise S.RnnError(st, "rnn_sync_floor")
+            fl.append(fe[0].elapsed_time(fe[1]) / 1e3)
+        return statistics.median(fl) / T
+
+    t_floor = sync_floor(args.cluster)
+    floors = {}
+    for cs in ((1,) if w["dtype"] == "f32" else (1, 2, 4, 8, 16)):
+        try:
+            S.rnn_fwd_config(S.make_desc(cell, w["dtype"], T, Bsz, NH, Dh, flags, cs))
+        except S.RnnError:
+            continue  # no variant for this split
+        floors[cs] = sync_floor(cs)
 
     # ---- end to end through the C ABI with pinned host buffers: every step copies
     #      that step's Wx in from host memory and h_seq back out.  Forward: the
@@ -455,6 +468,7 @@ def run_ours(args, w, rank, world, local_rank):
     t_flop = 2.0 * Bsz * NH * Dh * G * Dh / (tflops_peak * 1e12)
     t_roof = max(t_bytes, t_flop) + t_floor
     t_meas_step = t_step / T
+    t_floor_min = min(floors.values()) if floors else t_floor
     if w["backward"]:
         # dominant launch of the training step: the reverse recurrence (rnn_bwd)
         roof_bytes = algorithmic_bytes_bwd(w)
@@ -478,6 +492,10 @@ def run_ours(args, w, rank, world, local_rank):
         "per_step_roofline": {
             "bytes_ns": t_bytes * 1e9, "flops_ns": t_flop * 1e9, "sync_floor_ns": t_floor * 1e9,
             "roofline_ns": t_roof * 1e9, "frac": t_roof / t_meas_step,
+            "floors_ns_by_ctas_per_head": {str(k): v * 1e9 for k, v in floors.items()},
+            "frac_min_floor": (max(t_bytes, t_flop) + t_floor_min) / t_meas_step,
+            "note": ("frac: the floor of the launch shape that ran; frac_min_floor: the "
+                     "smallest floor among the shapes the library admits for this workload"),
             "peaks": f"{peak_kind}: {hbm} GB/s, {tflops_peak} TFLOP/s bf16"},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
                      "frac": achieved_gbs / hbm, "traffic": ncu_traffic(args.workload, cfg),

@@ -37,7 +37,11 @@
  * MMA tile) and tanh(z~) is evaluated as 1 - 2/(e^{2z~}+1) on the
  * 2-ulp exponential instead of the ~2^-11 hardware tanh, for Dh <= 256
  * (Dh = 768 runs the plain bf16 operand: the pair does not fit on chip beside
- * R); RNN_FLAG_H_BF16 turns this off.
+ * R); RNN_FLAG_H_BF16 turns this off.  With the plain operand the deviation
+ * from the exact recurrence grows about linearly with T (~1.5e-5 per step on
+ * R ~ U(+-1/sqrt(768)) inputs, fp64 emulation), so an sLSTM with Dh = 768 and
+ * T > 768 is rejected with RNN_ERR_UNSUPPORTED unless RNN_FLAG_H_BF16 is set
+ * (the caller accepts the plain operand's drift).
  *
  * Ownership: the caller allocates and owns every buffer (device memory),
  * including the workspace and the training stash.  Nothing is allocated by

@@ -17,6 +17,7 @@ constexpr size_t kStatusBytes = 256;                          // status word + p
 constexpr unsigned long long kTimeoutNs = 2000000000ull;      // 2 s per device wait
 constexpr unsigned long long kTestTimeoutNs = 50000000ull;    // 50 ms under the test flag
 constexpr int kMaxLayers = 8;                                 // stacked layers per call
+constexpr int kSlstmPlainMaxT = 768;  // longest sLSTM (Dh > 256) sequence without RNN_FLAG_H_BF16
 
 inline int gates_of(int cell) { return cell == RNN_GRU ? 3 : 4; }
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

@@ -46,7 +46,11 @@ extern "C" int rnn_fwd_noalloc(const rnn_desc_t* desc, const void* Wx, const voi
                                void* stream) {
   if (desc == nullptr) return RNN_ERR_INVALID_ARG;
   const size_t need = rnn_workspace_size(desc, 0);
-  if (need == 0) return RNN_ERR_INVALID_ARG;
+  // a descriptor rnn_fwd refuses (invalid, or a shape without a kernel): its
+  // checks return the status before anything touches the device
+  if (need == 0)
+    return rnn_fwd(desc, Wx, R, bias, h0, c0, n0, m0, h_seq, hT, cT, nT, mT, stash, nullptr, 0,
+                   stream);
   if (need > kNoAllocScratchBytes) return RNN_ERR_SCRATCH_LIMIT;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RNN_ERR_LAUNCH;

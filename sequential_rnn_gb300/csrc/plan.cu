@@ -166,6 +166,13 @@ int check_desc(const rnn_desc_t* d) {
   if (d->dtype != RNN_F32 && d->dtype != RNN_BF16) return RNN_ERR_INVALID_ARG;
   if (d->T < 0 || d->B < 0 || d->NH < 0 || d->Dh <= 0) return RNN_ERR_INVALID_ARG;
   if (d->cluster < 0) return RNN_ERR_INVALID_ARG;
+  // sLSTM heads above 256 units take h as one bf16 operand (the hi + lo pair
+  // does not fit on chip); its error grows about linearly with the steps
+  // (exponential gating is not contractive), so longer sequences need the
+  // caller's explicit RNN_FLAG_H_BF16
+  if (d->cell == RNN_SLSTM && d->dtype == RNN_BF16 && d->Dh > 256 &&
+      !(d->flags & RNN_FLAG_H_BF16) && d->T > kSlstmPlainMaxT)
+    return RNN_ERR_UNSUPPORTED;
   return RNN_OK;
 }
 

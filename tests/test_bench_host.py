@@ -17,14 +17,16 @@ sys.path.insert(0, ROOT)
 import bench  # noqa: E402
 
 STUB = r'''
-import json, os
+import json, os, sys
 import torch
 import torch.distributed as dist
 dist.init_process_group("gloo")
 t = torch.ones(1)
 dist.all_reduce(t)
-print(json.dumps({"rank": dist.get_rank(), "n_gpus": dist.get_world_size(),
-                  "sum": int(t.item()), "argv": os.sys.argv[1:]}), flush=True)
+out = os.path.join(os.path.dirname(os.path.abspath(__file__)), f"rank{dist.get_rank()}.json")
+with open(out, "w") as f:
+    json.dump({"rank": dist.get_rank(), "n_gpus": dist.get_world_size(), "sum": int(t.item()),
+               "argv": sys.argv[1:]}, f)
 dist.destroy_process_group()
 '''
 
@@ -37,7 +39,7 @@ def test_rank_launcher_starts_n_ranks(tmp_path):
            if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=240, env=env)
     assert r.returncode == 0, r.stderr[-2000:]
-    lines = [json.loads(ln) for ln in r.stdout.splitlines() if ln.startswith("{")]
+    lines = [json.loads((tmp_path / f"rank{i}.json").read_text()) for i in range(2)]
     assert sorted(x["rank"] for x in lines) == [0, 1]
     assert all(x["n_gpus"] == 2 and x["sum"] == 2 for x in lines)
     assert all(x["argv"] == ["--steps", "3"] for x in lines)

@@ -347,3 +347,18 @@ def test_binding_constants_match_the_header():
         assert vals[name] == v, name
     for code, name in L.STATUS.items():
         assert vals[name] == code, name
+
+
+def test_long_slstm_768_needs_the_bf16_h_flag(lib):
+    """sLSTM heads above 256 units take h as one bf16 operand, whose deviation
+    from the exact recurrence grows with T: past 768 steps the call is refused
+    unless the caller sets RNN_FLAG_H_BF16 (host check, every entry point)."""
+    from sequential_rnn_gb300._lib import RNN_FLAG_H_BF16
+    assert _plan(lib, cell=2, Dh=768, NH=1, B=16, T=768)[0] == 0
+    assert _plan(lib, cell=2, Dh=768, NH=1, B=16, T=769)[0] == 2
+    assert _plan(lib, cell=2, Dh=768, NH=1, B=16, T=769, flags=RNN_FLAG_H_BF16)[0] == 0
+    assert _plan(lib, cell=2, Dh=256, NH=1, B=16, T=100000)[0] == 0   # hi + lo operand: no bound
+    assert _plan(lib, cell=0, Dh=768, NH=1, B=16, T=100000)[0] == 0   # LSTM: contractive
+    assert _fwd(lib, _desc(cell=2, Dh=768, NH=1, T=769)) == 2
+    d = _desc(cell=2, Dh=768, NH=1, T=769)
+    assert lib.rnn_fwd_noalloc(ctypes.byref(d), *([None] * 15)) == 2

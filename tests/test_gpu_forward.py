@@ -73,6 +73,42 @@ def test_workload_forward_full(S, name):
     compare(out, oracle(d), d["dtype"], name)
 
 
+@pytest.mark.parametrize("name", ["lstm_bf16_12x64_b16_t1024", "gru_bf16_6x128_b8_t2048",
+                                  "slstm_bf16_4x256_b4_t4096"])
+def test_error_per_256_step_window(S, name):
+    """max |dh| per 256-step window over the long bf16 workloads.
+
+    LSTM and GRU with R ~ U(+-1/sqrt(Dh)) are contractive on average (each
+    Dh x Dh gate block has spectral radius ~0.58, gate derivatives <= 1), so
+    per-step bf16 rounding of h must not compound: the last window's error
+    stays within a small factor of the first one's.  The sLSTM's exponential
+    gating is not contractive (its operand is the bf16 hi + lo pair); its
+    windows are recorded and held to the bar."""
+    d = workload_inputs(name)
+    out = run(S, d)
+    ref = oracle(d)["h_seq"]
+    err = np.abs(out["h_seq"].float().cpu().numpy().astype(np.float64) - ref).max(axis=(1, 2, 3))
+    win = [float(err[i:i + 256].max()) for i in range(0, len(err), 256)]
+    print(f"\n{name} max|dh| per 256-step window: " + " ".join(f"{v:.2e}" for v in win))
+    assert max(win) <= TOL["bf16"], win
+    if d["cell"] != "slstm":
+        assert max(win[-2:]) <= 3.0 * max(win[:2]) + 1e-3, win
+
+
+@pytest.mark.parametrize("B", [4, 16])
+def test_slstm_768_at_its_longest_supported_sequence(S, B):
+    """sLSTM heads of 768 units (plain bf16 h operand) at T = 768, the longest
+    sequence accepted without RNN_FLAG_H_BF16, against the plain fp64 oracle;
+    one step more is refused."""
+    d = make_inputs("slstm", "bf16", 768, B, 1, 768, seed=B, bias="zero", states="zero")
+    out = run(S, d)
+    compare(out, oracle(d), "bf16", f"slstm768/B{B}/T768")
+    longer = make_inputs("slstm", "bf16", 769, 1, 1, 768, seed=1)
+    with pytest.raises(S.RnnError) as e:
+        run(S, longer)
+    assert e.value.status == 2
+
+
 SWEEP = [
     # cell, dtype, Dh, B, NH, T
     ("lstm", "f32", 16, 3, 2, 17), ("gru", "f32", 32, 13, 1, 9), ("slstm", "f32", 64, 5, 3, 12),

@@ -480,3 +480,16 @@ def test_slstm_workload_needs_more_than_a_bf16_h_operand():
     pair = O.slstm_forward(*args, emulate_bf16_pair_h=True)["h_seq"]
     assert np.abs(one - exact).max() > 0.1
     assert np.abs(pair - exact).max() < 1e-2
+
+
+def test_slstm_768_plain_bf16_h_drift_bound():
+    """The bound behind the library's T <= 768 limit for sLSTM heads of 768
+    units (plain bf16 h operand): on R ~ U(+-1/sqrt(768)) inputs the rounded
+    recurrence stays within 1.2e-2 of the exact one over 768 steps, and keeps
+    drifting after (fp64 emulation, B = 16)."""
+    d = make_inputs("slstm", "bf16", 1024, 16, 1, 768, seed=0, bias="zero", states="zero")
+    exact = O.slstm_forward(d["Wx"], d["R"], d["b"])["h_seq"]
+    one = O.slstm_forward(d["Wx"], d["R"], d["b"], emulate_bf16_h=True)["h_seq"]
+    err = np.abs(one - exact).max(axis=(1, 2, 3))
+    assert err[:768].max() < 1.2e-2
+    assert err[768:].max() > err[:256].max() * 2
