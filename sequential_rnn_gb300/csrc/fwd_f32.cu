@@ -1,15 +1,24 @@
 // fp32 forward of the head-wise recurrence: the precision reference path.
 //
-// One CTA per (head, batch slice of up to 8 rows).  Thread k (0 <= k < G*Dh)
-// owns gate row k of the head and keeps column k of R[h] in registers for the
-// whole time loop (FlashRNN blog page, register-caching paragraph: R pinned
-// in registers inside a persistent kernel).  Per step:
-//   1. rec[b][k] = sum_j h_{t-1}[b][j] * R[j][k] + bias[k]   (fp32 FMA, h from smem)
-//   2. barrier
-//   3. each (b, j) cell thread applies the gates with accurate expf/tanhf,
-//      updates its state and writes h_t to shared memory and h_seq
-//   4. barrier
-// Wx_t rows are prefetched NSTG steps ahead with cp.async into a smem ring.
+// One CTA per (head, batch row): the rows of a batch are independent
+// recurrences (FlashRNN blog page, head-wise paragraph: heads -- and batch
+// rows -- map to separate thread blocks), so each step's latency chain is one
+// row's.  Thread (lane 4 (j % 8) + g of warp j / 8) owns gate row g*Dh + j and
+// keeps column g*Dh + j of R[h] in registers for the whole time loop (blog
+// page, register-caching paragraph), so the G gates of hidden unit j sit in
+// adjacent lanes of one warp.  Per step:
+//   1. the thread's dot product over h_{t-1} (fp32 FMA in four chains, h read
+//      from shared memory as broadcast float4);
+//   2. the G gate preactivations of unit j gathered into lane 4 (j % 8) by
+//      shuffles, which applies the cell with accurate expf / tanhf and a true
+//      division, updates its fp32 state and writes h_t to shared memory and h_seq;
+//   3. one CTA barrier (h is double-buffered by step parity).
+// (A split of each dot product over four threads -- 1024 threads for
+// Dh = 64 -- ran 990 ns per step: a barrier of 32 warps alone takes ~160 ns.)
+// Wx rows are streamed PD steps ahead into a shared-memory ring with 16-byte
+// cp.async issued by the first G*Dh/4 threads; each thread waits for its own
+// copies before the barrier that precedes their first read, and a slot is
+// refilled only after the barrier that follows its last read.
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -18,149 +27,136 @@
 namespace srnn {
 
 namespace {
-constexpr int kNB = 8;    // batch rows per CTA
-constexpr int kNSTG = 4;  // Wx ring depth (steps in flight)
+constexpr int kPD = 4;  // Wx ring depth (steps)
 
 __device__ __forceinline__ float sigm(float x) { return 1.f / (1.f + expf(-x)); }
 
 template <int CELL, int DH>
-__global__ void __launch_bounds__(256, 1) fwd_f32_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(DH * 4, 1) fwd_f32_kernel(const FwdParams p) {
   constexpr int G = CELL == kGRU ? 3 : 4;
   constexpr int GD = G * DH;
-  constexpr int EPT = (kNB * DH + GD - 1) / GD;  // cells per thread
-  __shared__ __align__(16) float hs[kNB][DH];
-  __shared__ __align__(16) float rec[kNB][GD];
-  __shared__ __align__(16) float xs[kNSTG][kNB][GD];
+  constexpr int NT = DH * 4;  // threads: 8 units x 4 gate slots per warp
+  constexpr int WCH = GD / 4;  // 16-byte chunks of one Wx row
+  static_assert(DH % 16 == 0, "four chains of whole float4s");
+  __shared__ __align__(16) float hs[2][DH];
+  __shared__ __align__(16) float xs[kPD][GD];
 
-  const int k = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = p.T, B = p.B, NH = p.NH;
-  const int head = blockIdx.x / p.nbslices, bslice = blockIdx.x % p.nbslices;
-  const int b0 = bslice * kNB;
-  const int nb = min(kNB, B - b0);
-  const float* Wx = static_cast<const float*>(p.Wx);
+  const int head = blockIdx.x / B, b = blockIdx.x % B;
+  const int g = lane & 3;                 // gate (GRU: slot 3 idle)
+  const int j = warp * 8 + (lane >> 2);   // hidden unit
+  const bool row_on = g < G;
+  const int row = g * DH + j;             // gate row within the head
+  const bool cell = g == 0;               // lane that applies the cell of unit j
+  const float* Wx = static_cast<const float*>(p.Wx) + ((size_t)b * NH + head) * GD;
+  const size_t wx_tstride = (size_t)B * NH * GD;
   const float* Rh = static_cast<const float*>(p.R) + (size_t)head * DH * GD;
-  float* hseq = static_cast<float*>(p.h_seq);
+  float* hseq = static_cast<float*>(p.h_seq) + ((size_t)b * NH + head) * DH + j;
+  const size_t hseq_tstride = (size_t)B * NH * DH;
+  const size_t si = ((size_t)b * NH + head) * DH + j;
 
-  float rcol[DH];
+  float rcol[DH];  // R[h][k][row]
 #pragma unroll
-  for (int j = 0; j < DH; ++j) rcol[j] = Rh[(size_t)j * GD + k];
-  const float bk = p.bias ? p.bias[(size_t)head * GD + k] : 0.f;
+  for (int k = 0; k < DH; ++k) rcol[k] = row_on ? Rh[(size_t)k * GD + row] : 0.f;
+  const float brow = (row_on && p.bias) ? p.bias[(size_t)head * GD + row] : 0.f;
 
-  float st_c[EPT], st_n[EPT], st_m[EPT], st_h[EPT];
-#pragma unroll
-  for (int q = 0; q < EPT; ++q) {
-    const int e = k + q * GD;
-    const int b = e / DH, j = e % DH;
-    const bool ok = e < nb * DH;
-    const size_t si = ((size_t)(b0 + b) * NH + head) * DH + j;
-    st_h[q] = (ok && p.h0) ? p.h0[si] : 0.f;
-    st_c[q] = (ok && p.c0) ? p.c0[si] : 0.f;
-    st_n[q] = (ok && p.n0) ? p.n0[si] : 0.f;
-    st_m[q] = (ok && p.m0) ? p.m0[si] : 0.f;
+  float st_c = 0.f, st_n = 0.f, st_m = 0.f, st_h = 0.f;
+  if (cell) {
+    st_h = p.h0 ? p.h0[si] : 0.f;
+    st_c = p.c0 ? p.c0[si] : 0.f;
+    st_n = p.n0 ? p.n0[si] : 0.f;
+    st_m = p.m0 ? p.m0[si] : 0.f;
   }
-  for (int e = k; e < kNB * DH; e += GD) {
-    const int b = e / DH, j = e % DH;
-    hs[b][j] = (b < nb && p.h0) ? p.h0[((size_t)(b0 + b) * NH + head) * DH + j] : 0.f;
-  }
-  for (int b = nb; b < kNB; ++b)
-    for (int s = 0; s < kNSTG; ++s) xs[s][b][k] = 0.f;
+  for (int i = tid; i < DH; i += NT) hs[0][i] = p.h0 ? p.h0[((size_t)b * NH + head) * DH + i] : 0.f;
 
   auto issue = [&](int t) {
-    if (t < T) {
-      const int s = t % kNSTG;
-      for (int b = 0; b < nb; ++b)
-        cp_async4(smem_u32(&xs[s][b][k]), Wx + (((size_t)t * B + b0 + b) * NH + head) * GD + k);
-    }
+    if (t < T && tid < WCH)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(&xs[t % kPD][4 * tid])),
+                   "l"(Wx + (size_t)t * wx_tstride + 4 * tid)
+                   : "memory");
     cp_async_commit();
   };
 #pragma unroll 1
-  for (int t = 0; t < kNSTG - 1; ++t) issue(t);
+  for (int t = 0; t < kPD; ++t) issue(t);
+  cp_async_wait<kPD - 1>();  // step 0 landed (own copies)
   __syncthreads();
 
 #pragma unroll 1
   for (int t = 0; t < T; ++t) {
-    issue(t + kNSTG - 1);
-    cp_async_wait<kNSTG - 1>();
-    const int s = t % kNSTG;
-    // 1. recurrent preactivation for gate row k, all batch rows
-    float acc[kNB];
+    // refill the slot of step t - 1 (read by every thread before the last
+    // barrier) with step t - 1 + PD
+    if (t > 0) issue(t - 1 + kPD);
+    // 1. dot product over h_{t-1}: float4 i/4 feeds chain (i/4) % 4
+    const float* hp = hs[t & 1];
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int b = 0; b < kNB; ++b) acc[b] = 0.f;
-#pragma unroll
-    for (int j = 0; j < DH; j += 4) {
-#pragma unroll
-      for (int b = 0; b < kNB; ++b) {
-        const float4 hv = *reinterpret_cast<const float4*>(&hs[b][j]);
-        acc[b] = fmaf(hv.x, rcol[j], acc[b]);
-        acc[b] = fmaf(hv.y, rcol[j + 1], acc[b]);
-        acc[b] = fmaf(hv.z, rcol[j + 2], acc[b]);
-        acc[b] = fmaf(hv.w, rcol[j + 3], acc[b]);
-      }
+    for (int i = 0; i < DH; i += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(hp + i);
+      float& c = a[(i / 4) % 4];
+      c = fmaf(x.x, rcol[i], c);
+      c = fmaf(x.y, rcol[i + 1], c);
+      c = fmaf(x.z, rcol[i + 2], c);
+      c = fmaf(x.w, rcol[i + 3], c);
     }
+    const float rec = ((a[0] + a[1]) + (a[2] + a[3])) + brow;  // R-part + bias of row `row`
+    // 2. gather unit j's gates into its cell lane
+    float pre[G];
 #pragma unroll
-    for (int b = 0; b < kNB; ++b) rec[b][k] = acc[b] + bk;
-    __syncthreads();
-    // 3. cell update
-#pragma unroll
-    for (int q = 0; q < EPT; ++q) {
-      const int e = k + q * GD;
-      if (e >= nb * DH) continue;
-      const int b = e / DH, j = e % DH;
+    for (int k = 0; k < G; ++k) pre[k] = __shfl_sync(0xffffffffu, rec, (lane & ~3) + k);
+    const float* x = xs[t % kPD];
+    if (cell) {
       float h;
-      if (CELL == kLSTM) {
-        const float ig = sigm(rec[b][j] + xs[s][b][j]);
-        const float fg = sigm(rec[b][DH + j] + xs[s][b][DH + j]);
-        const float zg = tanhf(rec[b][2 * DH + j] + xs[s][b][2 * DH + j]);
-        const float og = sigm(rec[b][3 * DH + j] + xs[s][b][3 * DH + j]);
-        st_c[q] = fg * st_c[q] + ig * zg;
-        h = og * tanhf(st_c[q]);
-      } else if (CELL == kGRU) {
-        const float rg = sigm(xs[s][b][j] + rec[b][j]);
-        const float zg = sigm(xs[s][b][DH + j] + rec[b][DH + j]);
-        const float ng = tanhf(xs[s][b][2 * DH + j] + rg * rec[b][2 * DH + j]);
-        h = (1.f - zg) * ng + zg * st_h[q];
+      if constexpr (CELL == kLSTM) {
+        const float ig = sigm(pre[0] + x[j]);
+        const float fg = sigm(pre[1] + x[DH + j]);
+        const float zg = tanhf(pre[2] + x[2 * DH + j]);
+        const float og = sigm(pre[3] + x[3 * DH + j]);
+        st_c = fg * st_c + ig * zg;
+        h = og * tanhf(st_c);
+      } else if constexpr (CELL == kGRU) {
+        const float rg = sigm(x[j] + pre[0]);
+        const float zg = sigm(x[DH + j] + pre[1]);
+        const float ng = tanhf(x[2 * DH + j] + rg * pre[2]);
+        h = (1.f - zg) * ng + zg * st_h;
       } else {
-        const float pi = rec[b][j] + xs[s][b][j];
-        const float pf = rec[b][DH + j] + xs[s][b][DH + j];
-        const float pz = rec[b][2 * DH + j] + xs[s][b][2 * DH + j];
-        const float po = rec[b][3 * DH + j] + xs[s][b][3 * DH + j];
-        const float mn = fmaxf(pf + st_m[q], pi);
+        const float pi = pre[0] + x[j], pf = pre[1] + x[DH + j];
+        const float pz = pre[2] + x[2 * DH + j], po = pre[3] + x[3 * DH + j];
+        const float mn = fmaxf(pf + st_m, pi);
         const float ig = expf(pi - mn);
-        const float fg = expf(pf + st_m[q] - mn);
-        st_c[q] = fg * st_c[q] + ig * tanhf(pz);
-        st_n[q] = fg * st_n[q] + ig;
-        st_m[q] = mn;
-        h = sigm(po) * (st_c[q] / st_n[q]);
+        const float fg = expf(pf + st_m - mn);
+        st_c = fg * st_c + ig * tanhf(pz);
+        st_n = fg * st_n + ig;
+        st_m = mn;
+        h = sigm(po) * (st_c / st_n);
       }
-      st_h[q] = h;
-      hs[b][j] = h;
-      hseq[(((size_t)t * B + b0 + b) * NH + head) * DH + j] = h;
+      st_h = h;
+      hs[(t + 1) & 1][j] = h;
+      *hseq = h;
     }
+    hseq += hseq_tstride;
+    // 3. step t + 1's Wx landed (own copies; PD - 2 younger groups may stay in
+    //    flight); one barrier makes it and h_t visible to all
+    cp_async_wait<kPD - 2>();
     __syncthreads();
   }
   cp_async_wait<0>();
-  if (T > 0) {
-#pragma unroll
-    for (int q = 0; q < EPT; ++q) {
-      const int e = k + q * GD;
-      if (e >= nb * DH) continue;
-      const int b = e / DH, j = e % DH;
-      const size_t si = ((size_t)(b0 + b) * NH + head) * DH + j;
-      if (p.hT) p.hT[si] = st_h[q];
-      if (p.cT && CELL != kGRU) p.cT[si] = st_c[q];
-      if (p.nT && CELL == kSLSTM) p.nT[si] = st_n[q];
-      if (p.mT && CELL == kSLSTM) p.mT[si] = st_m[q];
-    }
+  if (cell && T > 0) {
+    if (p.hT) p.hT[si] = st_h;
+    if (p.cT && CELL != kGRU) p.cT[si] = st_c;
+    if (p.nT && CELL == kSLSTM) p.nT[si] = st_n;
+    if (p.mT && CELL == kSLSTM) p.mT[si] = st_m;
   }
 }
 
 template <int CELL, int DH>
 int launch_t(const FwdParams& p, cudaStream_t s, bool query_only, LaunchInfo* info) {
-  constexpr int G = CELL == kGRU ? 3 : 4;
-  const int grid = p.NH * p.nbslices;
-  if (info) *info = LaunchInfo{grid, G * DH, 1, kNB, 0, 1000 + CELL * 100 + DH};
+  constexpr int NT = DH * 4;
+  const long long grid = (long long)p.NH * p.B;
+  if (grid > 0x7fffffffLL) return (int)cudaErrorInvalidValue;
+  if (info) *info = LaunchInfo{(int)grid, NT, 1, 1, 0, 1000 + CELL * 100 + DH};
   if (query_only) return 0;
-  fwd_f32_kernel<CELL, DH><<<grid, G * DH, 0, s>>>(p);
+  fwd_f32_kernel<CELL, DH><<<(int)grid, NT, 0, s>>>(p);
   return (int)cudaGetLastError();
 }
 

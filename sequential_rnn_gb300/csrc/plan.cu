@@ -188,7 +188,7 @@ int make_plan(const rnn_desc_t* d, Plan* pl) {
     pl->CS = 1;
     pl->U = d->Dh;
     pl->NT = 1;
-    pl->NB = 8;
+    pl->NB = 1;  // one CTA per (head, batch row)
   } else {
     if (!bf16_dh_supported(d->Dh)) return RNN_ERR_UNSUPPORTED;
     int cs = d->cluster;
