@@ -462,6 +462,14 @@ def run_ours(args, w, rank, world, local_rank):
 
     fl_step = flops_per_step(w)
     hbm, tflops_peak, peak_kind = load_peaks()
+    pipe = "bf16 tensor (measured cuBLAS)"
+    if w["dtype"] == "f32":
+        # the fp32 path runs on the FMA pipe (no tensor cores, no TF32): its peak
+        # from unit counts and clock -- SMs x 128 fp32 FMA lanes x 2 FLOP x SM clock
+        props = torch.cuda.get_device_properties(dev)
+        mhz = float(clk.summary().get("sm_max_mhz") or 2070.0)
+        tflops_peak = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
+        pipe = f"fp32 FMA ({props.multi_processor_count} SMs x 128 lanes x 2 FLOP x {mhz:.0f} MHz)"
     per_step_bytes, total_bytes = algorithmic_bytes_fwd(w)
     # per-step roofline: slower of bytes at HBM and flops at the tensor pipe, plus the floor
     t_bytes = per_step_bytes / (hbm * 1e9)
@@ -496,7 +504,7 @@ def run_ours(args, w, rank, world, local_rank):
             "frac_min_floor": (max(t_bytes, t_flop) + t_floor_min) / t_meas_step,
             "note": ("frac: the floor of the launch shape that ran; frac_min_floor: the "
                      "smallest floor among the shapes the library admits for this workload"),
-            "peaks": f"{peak_kind}: {hbm} GB/s, {tflops_peak} TFLOP/s bf16"},
+            "peaks": f"HBM {peak_kind} {hbm} GB/s; pipe {pipe} {tflops_peak:.1f} TFLOP/s"},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
                      "frac": achieved_gbs / hbm, "traffic": ncu_traffic(args.workload, cfg),
                      "note": roof_note},

@@ -27,16 +27,16 @@ struct StepRow {
   float ns[5];
 };
 const StepRow kStepTable[] = {
-    {RNN_LSTM, 32, 0, {332, 400, 388, 0, 0}},       {RNN_LSTM, 64, 0, {438, 416, 405, 415, 0}},
-    {RNN_LSTM, 128, 0, {0, 533, 442, 455, 505}},    {RNN_LSTM, 256, 0, {0, 0, 775, 625, 793}},
-    {RNN_LSTM, 768, 0, {0, 0, 0, 0, 1945}},         {RNN_GRU, 32, 0, {302, 381, 372, 0, 0}},
-    {RNN_GRU, 64, 0, {405, 398, 387, 397, 0}},      {RNN_GRU, 128, 0, {692, 543, 424, 431, 479}},
-    {RNN_GRU, 256, 0, {0, 1022, 761, 743, 820}},    {RNN_GRU, 768, 0, {0, 0, 0, 0, 1995}},
-    {RNN_SLSTM, 32, 0, {403, 452, 464, 0, 0}},      {RNN_SLSTM, 64, 0, {571, 507, 510, 576, 0}},
-    {RNN_SLSTM, 128, 0, {0, 897, 679, 690, 727}},   {RNN_SLSTM, 256, 0, {0, 0, 1413, 1084, 1105}},
-    {RNN_SLSTM, 768, 0, {0, 0, 0, 0, 2015}},        {RNN_SLSTM, 32, 1, {402, 449, 438, 0, 0}},
-    {RNN_SLSTM, 64, 1, {498, 477, 465, 482, 0}},    {RNN_SLSTM, 128, 1, {0, 588, 500, 509, 562}},
-    {RNN_SLSTM, 256, 1, {0, 0, 893, 678, 758}},
+    {RNN_LSTM, 32, 0, {307, 384, 374, 0, 0}},       {RNN_LSTM, 64, 0, {396, 406, 391, 406, 0}},
+    {RNN_LSTM, 128, 0, {0, 515, 432, 439, 499}},    {RNN_LSTM, 256, 0, {0, 0, 763, 615, 703}},
+    {RNN_LSTM, 768, 0, {0, 0, 0, 0, 1940}},         {RNN_GRU, 32, 0, {308, 372, 361, 0, 0}},
+    {RNN_GRU, 64, 0, {378, 386, 377, 391, 0}},      {RNN_GRU, 128, 0, {661, 520, 412, 423, 477}},
+    {RNN_GRU, 256, 0, {0, 1012, 756, 741, 811}},    {RNN_GRU, 768, 0, {0, 0, 0, 0, 1981}},
+    {RNN_SLSTM, 32, 0, {381, 426, 438, 0, 0}},      {RNN_SLSTM, 64, 0, {553, 466, 469, 498, 0}},
+    {RNN_SLSTM, 128, 0, {0, 863, 680, 668, 707}},   {RNN_SLSTM, 256, 0, {0, 0, 1404, 1077, 1092}},
+    {RNN_SLSTM, 768, 0, {0, 0, 0, 0, 2011}},        {RNN_SLSTM, 32, 1, {386, 445, 439, 0, 0}},
+    {RNN_SLSTM, 64, 1, {501, 472, 461, 478, 0}},    {RNN_SLSTM, 128, 1, {0, 586, 495, 505, 555}},
+    {RNN_SLSTM, 256, 1, {0, 0, 873, 677, 752}},
 };
 constexpr int kClusterSizes[5] = {1, 2, 4, 8, 16};
 constexpr int kMaxSmemOptin = 232448;       // dynamic shared memory per CTA (sm_103)

@@ -52,9 +52,11 @@ struct TcCfg {
   static constexpr uint32_t TMEM_COLS = 2 * BN;            // two accumulator buffers
   // bf16 output: per epilogue warp two 32-row x 64-column boxes staged for TMA stores
   static constexpr uint32_t OUT_STAGE = OUT == kOutBf16Bias ? 4 * 8192 : 0;
-  // ring + output staging + 1024 for aligning them + barriers (full, empty,
-  // tfull x2, tempty x2) + TMEM slot
-  static constexpr uint32_t SMEM = NSTG * STAGE + OUT_STAGE + 1024 + (2 * NSTG + 4) * 8 + 16;
+  // bf16 output: per epilogue warp a 32-value bias slot (the 32 columns it converts)
+  static constexpr uint32_t BIAS = OUT == kOutBf16Bias ? 4 * 32 * 4 : 0;
+  // ring + output staging + bias + 1024 for aligning them + barriers (full,
+  // empty, tfull x2, tempty x2) + TMEM slot
+  static constexpr uint32_t SMEM = NSTG * STAGE + OUT_STAGE + BIAS + 1024 + (2 * NSTG + 4) * 8 + 16;
 };
 
 struct GemmArgs {
@@ -120,7 +122,8 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t ring = (raw + 1023u) & ~1023u;  // 128-byte swizzle: 1024-byte aligned tiles
   const uint32_t out_stage = ring + NSTG * C::STAGE;  // 1024-byte aligned
-  const uint32_t bar_full = out_stage + C::OUT_STAGE, bar_empty = bar_full + 8 * NSTG;
+  const uint32_t bias_s = out_stage + C::OUT_STAGE;
+  const uint32_t bar_full = bias_s + C::BIAS, bar_empty = bar_full + 8 * NSTG;
   const uint32_t bar_tfull = bar_empty + 8 * NSTG, bar_tempty = bar_tfull + 16;
   const uint32_t tslot = bar_tempty + 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -253,6 +256,19 @@ __global__ void __launch_bounds__(192, 1)
         // 128 columns at a time as two 32 x 64 boxes in the 128-byte swizzled layout
         // (16-byte chunk j of row r at chunk j ^ (r % 8)); the TMA engine writes
         // whole row segments and drops rows / columns past the output's extent.
+        // The unit's BN bias values are loaded once per warp (lane i holds
+        // columns i, i + 32, ...; zeros past N or without a bias) and each 32-column
+        // slice is passed through the warp's own 128-byte slot in shared memory to
+        // be read as broadcasts: a global load per value and thread cost ~11 us of
+        // a 73 us projection (16384 x 3072 x 768).
+        const bool has_bias = g.bias != nullptr;
+        const uint32_t bias_w = bias_s + (uint32_t)q * 128;
+        float breg[BN / 32];
+#pragma unroll
+        for (int k = 0; k < BN / 32; ++k) {
+          const int n = n_base + 32 * k + lane;
+          breg[k] = (has_bias && n < g.N) ? __ldg(g.bias + n) : 0.f;
+        }
         const uint32_t stg = out_stage + (uint32_t)q * 8192;
 #pragma unroll 1
         for (int hh = 0; hh < BN / 128; ++hh) {
@@ -265,14 +281,29 @@ __global__ void __launch_bounds__(192, 1)
             tmem_wait_ld();
             const int n0 = n_base + hh * 128 + c * 32;
             uint32_t pk[16];
+            float bv[32];
+            if (has_bias) {
+              float bk = 0.f;  // breg[hh * 4 + c] (indices fixed per unrolled copy)
+#pragma unroll
+              for (int k = 0; k < BN / 32; ++k)
+                if (k == hh * 4 + c) bk = breg[k];
+              __syncwarp();  // the slot's previous values were read
+              asm volatile("st.shared.f32 [%0], %1;" ::"r"(bias_w + 4u * lane), "f"(bk) : "memory");
+              __syncwarp();
+#pragma unroll
+              for (int j = 0; j < 32; j += 4)
+                asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                             : "=f"(bv[j]), "=f"(bv[j + 1]), "=f"(bv[j + 2]), "=f"(bv[j + 3])
+                             : "r"(bias_w + 4u * (uint32_t)j)
+                             : "memory");
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) bv[j] = 0.f;
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              float x0 = empty_k ? 0.f : __uint_as_float(r[2 * j]);
-              float x1 = empty_k ? 0.f : __uint_as_float(r[2 * j + 1]);
-              if (g.bias && n0 + 2 * j + 1 < g.N) {
-                x0 += __ldg(g.bias + n0 + 2 * j);
-                x1 += __ldg(g.bias + n0 + 2 * j + 1);
-              }
+              const float x0 = (empty_k ? 0.f : __uint_as_float(r[2 * j])) + bv[2 * j];
+              const float x1 = (empty_k ? 0.f : __uint_as_float(r[2 * j + 1])) + bv[2 * j + 1];
               pk[j] = pack_bf16x2(x0, x1);
             }
             const uint32_t rowb = stg + (uint32_t)(c >> 1) * 4096 + (uint32_t)lane * 128;
