@@ -109,6 +109,20 @@ def test_slstm_768_at_its_longest_supported_sequence(S, B):
     assert e.value.status == 2
 
 
+@pytest.mark.parametrize("cell,dtype,Dh,B,NH,cluster", [
+    ("lstm", "bf16", 64, 64, 40, 4),    # 40 heads x 8 batch slices x 4 CTAs = 1280 CTAs
+    ("gru", "bf16", 128, 33, 12, 2),    # ragged last slice, 120 clusters of 2
+    ("lstm", "bf16", 64, 61, 24, 1),    # 192 one-CTA heads x slices
+    ("slstm", "bf16", 256, 9, 8, 8),    # hi + lo operands, 16 clusters of 8
+    ("lstm", "f32", 64, 50, 4, 0),      # fp32: one CTA per (head, batch row): 200 CTAs
+])
+def test_forward_more_ctas_than_sms(S, cell, dtype, Dh, B, NH, cluster):
+    """Launches of several waves over the SMs (heads x batch slices x CTAs per
+    head well above 152): every CTA, cluster and ragged tail matches the oracle."""
+    d = make_inputs(cell, dtype, 6, B, NH, Dh, seed=NH + B, bias="normal0.1", states="random")
+    compare(run(S, d, cluster=cluster), oracle(d), dtype, f"{cell}/{dtype}/{NH}x{Dh}/B{B}/cs{cluster}")
+
+
 SWEEP = [
     # cell, dtype, Dh, B, NH, T
     ("lstm", "f32", 16, 3, 2, 17), ("gru", "f32", 32, 13, 1, 9), ("slstm", "f32", 64, 5, 3, 12),
