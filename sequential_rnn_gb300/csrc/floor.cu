@@ -1,7 +1,7 @@
 // Sync-floor kernel: the per-step synchronisation of a forward launch with
 // nothing else (no loads, no math).  Same grid, block size and cluster shape
 // as the forward it stands for, and the same barrier kind:
-//   * fp32 path: two CTA barriers per step;
+//   * fp32 path: one CTA barrier per step;
 //   * bf16, one CTA per head slice: one named barrier over the compute warps;
 //   * bf16 cluster: each compute warp st.async's 4 bytes into every cluster
 //     CTA's mbarrier-tracked buffer and all threads wait for the phase.
@@ -76,8 +76,8 @@ __global__ void floor_cluster_kernel(int T, int CS, int NW, unsigned long long t
 }  // namespace
 
 int launch_sync_floor(const LaunchInfo& li, int T, int* status, cudaStream_t s) {
-  if (li.kernel_id >= 1000) {  // fp32 path: two CTA barriers per step
-    floor_cta_kernel<<<li.grid, li.threads, 0, s>>>(T, 2);
+  if (li.kernel_id >= 1000) {  // fp32 path: one CTA barrier per step
+    floor_cta_kernel<<<li.grid, li.threads, 0, s>>>(T, 1);
     return (int)cudaGetLastError();
   }
   const int NW = li.threads / 32;  // bf16 forward: compute warps only
