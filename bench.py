@@ -238,16 +238,41 @@ def kernel_source_hash():
     return h.hexdigest()[:12]
 
 
+def tu_source_hash(tu):
+    """Hash of one kernel translation unit under csrc and every local header it
+    includes, recursively: ncu counters taken at another hash no longer
+    describe the kernel that runs (changes elsewhere in csrc do not matter)."""
+    import re
+    csrc = os.path.join(ROOT, "sequential_rnn_gb300", "csrc")
+    seen, todo = set(), [tu]
+    while todo:
+        f = todo.pop()
+        if f in seen or not os.path.exists(os.path.join(csrc, f)):
+            continue
+        seen.add(f)
+        with open(os.path.join(csrc, f)) as fh:
+            todo += re.findall(r'^#include "([^"/]+)"', fh.read(), flags=re.M)
+    h = hashlib.sha1()
+    for f in sorted(seen):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:12]
+
+
 def ncu_traffic(workload, launch=None):
-    """DRAM bytes per launch from a committed ncu summary, if it matches these
-    sources and (when both are known) the forward's launch shape."""
+    """DRAM bytes per launch from a committed ncu summary, if it matches the
+    sources of the captured kernel (its translation unit and headers) and (when
+    both are known) the forward's launch shape."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         j = json.load(f)
     e = j.get(workload)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e:
+        return None
+    want = tu_source_hash(e["tu"]) if "tu" in e else kernel_source_hash()
+    if e.get("source_hash") != want:
         return None
     shape = e.get("launch")
     if shape and launch and any(shape[k] != launch.get(k) for k in shape):

@@ -86,3 +86,20 @@ def test_threads_used_rounds_and_floors():
     assert bench.threads_used(0.2) == 1
     assert bench.threads_used(1.4) == 1
     assert bench.threads_used(11.6) == 12
+
+
+def test_traffic_hash_follows_the_kernels_own_sources(tmp_path, monkeypatch):
+    """A committed DRAM-traffic figure stays valid while the captured kernel's
+    translation unit and the headers it includes are unchanged, and only then."""
+    csrc = tmp_path / "sequential_rnn_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "a.cu").write_text('#include "b.h"\nint a;\n')
+    (csrc / "b.h").write_text('#include "c.h"\n')
+    (csrc / "c.h").write_text("// c\n")
+    (csrc / "d.cu").write_text("int d;\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.tu_source_hash("a.cu")
+    (csrc / "d.cu").write_text("int d2;\n")          # another kernel: no effect
+    assert bench.tu_source_hash("a.cu") == h0
+    (csrc / "c.h").write_text("// c changed\n")      # an included header: invalidates
+    assert bench.tu_source_hash("a.cu") != h0
