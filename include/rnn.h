@@ -49,7 +49,9 @@
  * NULL = legacy default stream).  Host-side checks fail fast with a status
  * and launch nothing.  Device-side failures (a bounded wait that ran out) are
  * recorded in the status word at the start of the workspace; read it with
- * rnn_read_status().
+ * rnn_read_status().  Every call that returns RNN_OK with a workspace leaves
+ * its own status there -- 0 also for a call that launches nothing (B, NH or
+ * T zero) -- so the workspace needs no clearing by the caller.
  */
 #ifndef SEQUENTIAL_RNN_GB300_RNN_H
 #define SEQUENTIAL_RNN_GB300_RNN_H

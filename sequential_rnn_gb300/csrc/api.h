@@ -57,6 +57,7 @@ int launch_forward(const rnn_desc_t* d, const Plan& pl, const FwdParams& p, cuda
 FwdParams base_params(const rnn_desc_t* d, const Plan& pl);
 // Final state <- initial state (or zero) for a zero-length sequence.
 int copy_state(float* dst, const float* src, size_t n, cudaStream_t s);
+int clear_status(void* workspace, size_t workspace_bytes, cudaStream_t s);
 
 }  // namespace api
 }  // namespace srnn

@@ -76,7 +76,7 @@ int rnn_fwd(const rnn_desc_t* d, const void* Wx, const void* R, const float* bia
   int st = check_desc(d);
   if (st != RNN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (d->B == 0 || d->NH == 0) return RNN_OK;
+  if (d->B == 0 || d->NH == 0) return clear_status(workspace, workspace_bytes, s);
   Plan pl;
   if ((st = make_plan(d, &pl)) != RNN_OK) return st;
   if (workspace == nullptr || workspace_bytes < rnn_workspace_size(d, 0)) return RNN_ERR_INVALID_ARG;
@@ -87,6 +87,7 @@ int rnn_fwd(const rnn_desc_t* d, const void* Wx, const void* R, const float* bia
   const size_t nstate = (size_t)d->B * d->NH * d->Dh;
   if (d->T == 0) {
     int r;
+    if ((r = clear_status(workspace, workspace_bytes, s)) != RNN_OK) return r;
     if ((r = copy_state(hT, h0, nstate, s)) != RNN_OK) return r;
     if (d->cell != RNN_GRU && (r = copy_state(cT, c0, nstate, s)) != RNN_OK) return r;
     if (d->cell == RNN_SLSTM) {
@@ -132,7 +133,7 @@ int rnn_input_proj(int32_t M, int32_t N, int32_t K, const void* x, const void* W
   if (workspace == nullptr || workspace_bytes < kStatusBytes) return RNN_ERR_INVALID_ARG;
   if (!aligned(workspace, 256)) return RNN_ERR_MISALIGNED;
   if (K % 8 != 0 || N % 16 != 0 || M > 65535 * 128) return RNN_ERR_UNSUPPORTED;
-  if (M == 0) return RNN_OK;
+  if (M == 0) return clear_status(workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
   if (x == nullptr || W == nullptr || Wx == nullptr) return RNN_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(W, 16) || !aligned(Wx, 16) || !aligned(bias, 4))
     return RNN_ERR_MISALIGNED;
@@ -173,7 +174,8 @@ int rnn_sync_floor(const rnn_desc_t* d, int iters, void* workspace, size_t works
   int st = check_desc(d);
   if (st != RNN_OK) return st;
   if (iters < 0 || workspace == nullptr || workspace_bytes < kStatusBytes) return RNN_ERR_INVALID_ARG;
-  if (d->B == 0 || d->NH == 0 || iters == 0) return RNN_OK;
+  if (d->B == 0 || d->NH == 0 || iters == 0)
+    return clear_status(workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
   Plan pl;
   if ((st = make_plan(d, &pl)) != RNN_OK) return st;
   LaunchInfo li{};
@@ -195,7 +197,8 @@ int rnn_bwd(const rnn_desc_t* d, const void* R, const float* h0, const float* c0
   if (d->dtype != RNN_BF16) return RNN_ERR_UNSUPPORTED;
   const int Dh = d->Dh;
   if (Dh != 32 && Dh != 64 && Dh != 128 && Dh != 256 && Dh != 768) return RNN_ERR_UNSUPPORTED;
-  if (d->B == 0 || d->NH == 0) return RNN_OK;
+  if (d->B == 0 || d->NH == 0)
+    return clear_status(workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
   if (workspace == nullptr || workspace_bytes < rnn_workspace_size(d, 1)) return RNN_ERR_INVALID_ARG;
   if (!aligned(workspace, 256)) return RNN_ERR_MISALIGNED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -205,6 +208,7 @@ int rnn_bwd(const rnn_desc_t* d, const void* R, const float* h0, const float* c0
   const bool has_c = d->cell != RNN_GRU, has_n = d->cell == RNN_SLSTM;
   if (d->T == 0) {  // no steps: gradients pass straight through to the initial states
     int r;
+    if ((r = clear_status(workspace, workspace_bytes, s)) != RNN_OK) return r;
     if ((r = copy_state(dh0, dhT, nstate, s)) != RNN_OK) return r;
     if (has_c && (r = copy_state(dc0, dcT, nstate, s)) != RNN_OK) return r;
     if (has_n && (r = copy_state(dn0, dnT, nstate, s)) != RNN_OK) return r;

@@ -60,12 +60,7 @@ extern "C" int rnn_fwd_noalloc(const rnn_desc_t* desc, const void* Wx, const voi
     g_scratch_ptr[dev] = p;
   });
   if (g_setup_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) return RNN_ERR_LAUNCH;
-  // Clear the status word here as well: a call that launches nothing (B == 0,
-  // NH == 0) must not hand on an earlier call's status.
-  if (device_status != nullptr &&
-      cudaMemsetAsync(g_scratch_ptr[dev], 0, sizeof(int), static_cast<cudaStream_t>(stream)) !=
-          cudaSuccess)
-    return RNN_ERR_LAUNCH;
+  // rnn_fwd clears the status word on every path, launching or not
   const int st = rnn_fwd(desc, Wx, R, bias, h0, c0, n0, m0, h_seq, hT, cT, nT, mT, stash,
                          g_scratch_ptr[dev], kNoAllocScratchBytes, stream);
   if (st != RNN_OK || device_status == nullptr) return st;

@@ -245,6 +245,15 @@ FwdParams base_params(const rnn_desc_t* d, const Plan& pl) {
   return p;
 }
 
+// Status word of a call that launches nothing <- 0, so that reading it never
+// returns a status left in that memory before the call.  No workspace (or
+// one too small to hold the word): nothing to clear.
+int clear_status(void* workspace, size_t workspace_bytes, cudaStream_t s) {
+  if (workspace == nullptr || workspace_bytes < sizeof(int) || !aligned(workspace, 4))
+    return RNN_OK;
+  return cudaMemsetAsync(workspace, 0, sizeof(int), s) == cudaSuccess ? RNN_OK : RNN_ERR_LAUNCH;
+}
+
 // Final state <- initial state (or zero) for a zero-length sequence.
 int copy_state(float* dst, const float* src, size_t n, cudaStream_t s) {
   if (dst == nullptr) return RNN_OK;

@@ -119,7 +119,8 @@ int rnn_stack_fwd(const rnn_desc_t* d, int32_t L, int32_t Din, int32_t chunk, co
   if (L < 1 || L > kMaxLayers || chunk < 0 || Din <= 0) return RNN_ERR_INVALID_ARG;
   if (d->dtype != RNN_BF16 || (d->flags & RNN_FLAG_TRAIN) || Din % 8 != 0)
     return RNN_ERR_UNSUPPORTED;
-  if (d->B == 0 || d->NH == 0) return RNN_OK;
+  if (d->B == 0 || d->NH == 0)
+    return clear_status(workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
   if (workspace == nullptr || workspace_bytes < rnn_stack_workspace_size(d, L, chunk))
     return RNN_ERR_INVALID_ARG;
   rnn_desc_t dplan;
@@ -139,6 +140,7 @@ int rnn_stack_fwd(const rnn_desc_t* d, int32_t L, int32_t Din, int32_t chunk, co
   float* fin[4] = {hT, cT, nT, mT};
   auto slot = [&](int k) { return d->cell == RNN_GRU ? (k == 0 ? 0 : -1) : (k < ns ? k : -1); };
   if (T == 0) {
+    if ((st = clear_status(workspace, workspace_bytes, cs)) != RNN_OK) return st;
     for (int k = 0; k < 4; ++k)
       if (slot(k) >= 0 && (st = copy_state(fin[k], init[k], (size_t)L * nstate, cs)) != RNN_OK)
         return st;
@@ -283,7 +285,8 @@ int rnn_fwd_host(const rnn_desc_t* d, int32_t chunk, const void* Wx_host, const 
   if (st != RNN_OK) return st;
   if (chunk < RNN_HOST_DIRECT) return RNN_ERR_INVALID_ARG;
   if (d->flags & RNN_FLAG_TRAIN) return RNN_ERR_UNSUPPORTED;
-  if (d->B == 0 || d->NH == 0) return RNN_OK;
+  if (d->B == 0 || d->NH == 0)
+    return clear_status(workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
   if (chunk == RNN_HOST_DIRECT) {
     // one forward whose kernel streams Wx from and stores h_seq to the host
     // buffers through their device mapping; only page-locked, mapped memory
@@ -326,6 +329,7 @@ int rnn_fwd_host(const rnn_desc_t* d, int32_t chunk, const void* Wx_host, const 
   float* fin[4] = {hT, cT, nT, mT};
   auto slot = [&](int k) { return k < ns ? k : -1; };
   if (d->T == 0) {
+    if ((st = clear_status(workspace, workspace_bytes, cs)) != RNN_OK) return st;
     for (int k = 0; k < 4; ++k)
       if (slot(k) >= 0 && (st = copy_state(fin[k], init[k], nstate, cs)) != RNN_OK) return st;
     return RNN_OK;

@@ -127,12 +127,14 @@ def test_backward_argument_checks(lib):
     assert _bwd(lib, _desc(), ws=0x1010) == 3               # workspace 256-aligned
     assert _bwd(lib, _desc(), stash=0) == 1
     assert _bwd(lib, _desc(cell=2), dWx=0x7008) == 3
-    assert _bwd(lib, _desc(B=0)) == 0
+    # no work and no workspace: nothing touches the device (with a workspace the
+    # call clears its status word, a device write these made-up pointers must not get)
+    assert _bwd(lib, _desc(B=0), ws=0) == 0
 
 
 def test_empty_batch_is_noop(lib):
-    assert _fwd(lib, _desc(B=0)) == 0
-    assert _fwd(lib, _desc(NH=0)) == 0
+    assert _fwd(lib, _desc(B=0), ws=0) == 0
+    assert _fwd(lib, _desc(NH=0), ws=0) == 0
 
 
 def _proj(lib, M=300, N=3072, K=768, x=0x1000, W=0x2000, bias=0, Wx=0x3000, ws=0x8000,
@@ -159,7 +161,7 @@ def test_input_proj_argument_checks(lib):
     assert _proj(lib, W=0x2004) == 3
     assert _proj(lib, Wx=0x3002) == 3
     assert _proj(lib, bias=0x4002) == 3
-    assert _proj(lib, M=0, x=0, Wx=0) == 0                  # empty input: no-op
+    assert _proj(lib, M=0, x=0, Wx=0, ws=0) == 1            # the workspace is checked first
 
 
 def _stack(lib, desc=None, L=2, Din=96, chunk=16, x=0x1000, W0=0x2000, W=0x3000, R=0x4000,
@@ -209,7 +211,7 @@ def test_stack_argument_checks(lib):
     assert _stack(lib, x=0x1008) == 3
     assert _stack(lib, W0=0x2004) == 3
     assert _stack(lib, h0=0x6002) == 3
-    assert _stack(lib, desc=_desc(B=0)) == 0               # empty batch: no-op
+    assert _stack(lib, desc=_desc(B=0), ws=0) == 0         # empty batch: no-op
 
 
 def _plan(lib, L=1, sms=148, **kw):
@@ -307,7 +309,7 @@ def test_fwd_host_argument_checks(lib):
     assert _fwd_host(lib, hseq=0) == 1
     assert _fwd_host(lib, r=0) == 1
     assert _fwd_host(lib, r=0x2008) == 3
-    assert _fwd_host(lib, desc=_desc(B=0)) == 0
+    assert _fwd_host(lib, desc=_desc(B=0), ws=0) == 0
 
 
 def test_fwd_host_direct_mode_arguments(lib):
@@ -318,7 +320,7 @@ def test_fwd_host_direct_mode_arguments(lib):
     assert lib.rnn_fwd_host_workspace_size(ctypes.byref(d), -1) == 256
     assert lib.rnn_fwd_host_workspace_size(ctypes.byref(d), -2) == 0
     assert _fwd_host(lib, chunk=-2) == 1
-    assert _fwd_host(lib, desc=_desc(B=0), chunk=-1) == 0
+    assert _fwd_host(lib, desc=_desc(B=0), chunk=-1, ws=0) == 0
     assert _fwd_host(lib, chunk=-1) == 1
 
 
