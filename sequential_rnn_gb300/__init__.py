@@ -266,7 +266,7 @@ def input_proj(x, W, bias=None, *, stream=None, check=True):
     N = W.shape[0]
     M = x.numel() // K if K else 0
     out = torch.empty(tuple(x.shape[:-1]) + (N,), dtype=torch.bfloat16, device=x.device)
-    ws = torch.zeros(256, dtype=torch.uint8, device=x.device)
+    ws = torch.empty(256, dtype=torch.uint8, device=x.device)  # the call clears its status word
     st = rnn_input_proj(M, N, K, x, W, bias, out, ws, stream)
     if st:
         raise RnnError(st, "rnn_input_proj")

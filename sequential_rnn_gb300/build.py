@@ -19,7 +19,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsrnn.so")
 
 SOURCES = ["capi.cu", "plan.cu", "runtime.cu", "fwd_f32.cu", "fwd_bf16_lstm.cu", "fwd_bf16_gru.cu", "fwd_bf16_slstm.cu",
-           "floor.cu", "bwd_cell.cu", "grad_weights.cu", "tc_gemm.cu", "noalloc.cu"]
+           "floor.cu", "bwd_cell.cu", "grad_weights.cu", "tc_gemm.cu", "tc_gemm_pair.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

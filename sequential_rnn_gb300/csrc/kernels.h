@@ -162,6 +162,11 @@ int launch_input_proj_tc(const void* x, const void* W, const float* bias, void* 
                          int K, int* status, unsigned long long timeout_ns, cudaStream_t s,
                          int max_ctas = 0);
 int sm_count();
+// CTA-pair input projection (tc_gemm_pair.cu), N >= 256: -1 when a pair cannot
+// be launched (the caller takes the one-CTA kernel), else 0 or a CUDA error.
+int launch_input_proj_pair(const void* x, const void* W, const float* bias, void* Wx, int M, int N,
+                           int K, int* status, unsigned long long timeout_ns, cudaStream_t s,
+                           int max_ctas);
 int launch_db_reduce(const float* part, float* db, int nslices, int n, cudaStream_t s);
 
 }  // namespace srnn

@@ -35,6 +35,7 @@
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tc.cuh"
+#include "tc_epi.cuh"
 
 namespace srnn {
 namespace {
@@ -252,81 +253,9 @@ __global__ void __launch_bounds__(192, 1)
       const bool empty_k = w.kb_hi == w.kb_lo;
       const int n_base = w.n_base * BN;
       if constexpr (OUT == kOutBf16Bias) {
-        // bf16 (+ bias) through shared memory and TMA stores: the warp's 32 rows x
-        // 128 columns at a time as two 32 x 64 boxes in the 128-byte swizzled layout
-        // (16-byte chunk j of row r at chunk j ^ (r % 8)); the TMA engine writes
-        // whole row segments and drops rows / columns past the output's extent.
-        // The unit's BN bias values are loaded once per warp (lane i holds
-        // columns i, i + 32, ...; zeros past N or without a bias) and each 32-column
-        // slice is passed through the warp's own 128-byte slot in shared memory to
-        // be read as broadcasts: a global load per value and thread cost ~11 us of
-        // a 73 us projection (16384 x 3072 x 768).
-        const bool has_bias = g.bias != nullptr;
-        const uint32_t bias_w = bias_s + (uint32_t)q * 128;
-        float breg[BN / 32];
-#pragma unroll
-        for (int k = 0; k < BN / 32; ++k) {
-          const int n = n_base + 32 * k + lane;
-          breg[k] = (has_bias && n < g.N) ? __ldg(g.bias + n) : 0.f;
-        }
-        const uint32_t stg = out_stage + (uint32_t)q * 8192;
-#pragma unroll 1
-        for (int hh = 0; hh < BN / 128; ++hh) {
-          if (lane == 0) bulk_wait_read_all();  // the previous boxes left this buffer
-          __syncwarp();
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];  // columns n_base + 128 hh + 32 c .. + 31 of this thread's row
-            tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN + hh * 128 + c * 32), r);
-            tmem_wait_ld();
-            const int n0 = n_base + hh * 128 + c * 32;
-            uint32_t pk[16];
-            float bv[32];
-            if (has_bias) {
-              float bk = 0.f;  // breg[hh * 4 + c] (indices fixed per unrolled copy)
-#pragma unroll
-              for (int k = 0; k < BN / 32; ++k)
-                if (k == hh * 4 + c) bk = breg[k];
-              __syncwarp();  // the slot's previous values were read
-              asm volatile("st.shared.f32 [%0], %1;" ::"r"(bias_w + 4u * lane), "f"(bk) : "memory");
-              __syncwarp();
-#pragma unroll
-              for (int j = 0; j < 32; j += 4)
-                asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-                             : "=f"(bv[j]), "=f"(bv[j + 1]), "=f"(bv[j + 2]), "=f"(bv[j + 3])
-                             : "r"(bias_w + 4u * (uint32_t)j)
-                             : "memory");
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) bv[j] = 0.f;
-            }
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float x0 = (empty_k ? 0.f : __uint_as_float(r[2 * j])) + bv[2 * j];
-              const float x1 = (empty_k ? 0.f : __uint_as_float(r[2 * j + 1])) + bv[2 * j + 1];
-              pk[j] = pack_bf16x2(x0, x1);
-            }
-            const uint32_t rowb = stg + (uint32_t)(c >> 1) * 4096 + (uint32_t)lane * 128;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint32_t chunk = (uint32_t)(((c & 1) * 4 + k) ^ (lane & 7));
-              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + chunk * 16),
-                           "r"(pk[4 * k]), "r"(pk[4 * k + 1]), "r"(pk[4 * k + 2]), "r"(pk[4 * k + 3])
-                           : "memory");
-            }
-          }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the TMA engine
-          __syncwarp();
-          if (lane == 0) {
-            const int mr = w.m_base + q * 32;
-#pragma unroll
-            for (int b = 0; b < 2; ++b) {
-              const int nc = n_base + hh * 128 + b * 64;
-              if (nc < g.N && mr < g.M) tma_store_2d(&mC, nc, mr, stg + (uint32_t)b * 4096);
-            }
-            bulk_commit();
-          }
-        }
+        epilogue_bf16_bias<BN>(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN), g.bias,
+                               n_base, g.N, w.m_base + q * 32, g.M, empty_k,
+                               out_stage + (uint32_t)q * 8192, bias_s + (uint32_t)q * 128, &mC);
       } else {
       float* cf = static_cast<float*>(g.C) + w.z * g.c_stride_z + (size_t)row * g.ldc;
 #pragma unroll 1
@@ -389,6 +318,8 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+}  // namespace
+
 // ------------------------------------------------------------ host side --
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -429,6 +360,8 @@ int num_sms() {
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
   return n > 0 ? n : 1;
 }
+
+namespace {
 
 // grid: one CTA per SM (at most one per unit, at most max_ctas if > 0)
 template <bool A_MN, bool B_MN, int OUT, int BN>
@@ -504,6 +437,10 @@ int launch_input_proj_tc(const void* x, const void* W, const float* bias, void* 
                          int K, int* status, unsigned long long timeout_ns, cudaStream_t s,
                          int max_ctas) {
   const bool wide = N >= 256;
+  if (wide) {  // 256 x 256 tiles on CTA pairs, unless no pair can be launched here
+    const int e = launch_input_proj_pair(x, W, bias, Wx, M, N, K, status, timeout_ns, s, max_ctas);
+    if (e != -1) return e;
+  }
   CUtensorMap a0, b0, c0;
   int e = make_map(&a0, x, (uint64_t)M, (uint64_t)K, (uint64_t)K, 64, 128);
   if (e) return e;
