@@ -7,11 +7,15 @@
 // keeps column g*Dh + j of R[h] in registers for the whole time loop (blog
 // page, register-caching paragraph), so the G gates of hidden unit j sit in
 // adjacent lanes of one warp.  Per step:
-//   1. the thread's dot product over h_{t-1} (fp32 FMA in four chains, h read
-//      from shared memory as broadcast float4);
-//   2. the G gate preactivations of unit j gathered into lane 4 (j % 8) by
-//      shuffles, which applies the cell with accurate expf / tanhf and a true
-//      division, updates its fp32 state and writes h_t to shared memory and h_seq;
+//   1. the thread's dot product over h_{t-1}: packed fp32 FMAs (fma.rn.f32x2,
+//      each lane of the pair rounded as a scalar fma) in eight chains, h read
+//      from shared memory as broadcast float4;
+//   2. each thread activates its own gate with accurate tanhf (a sigmoid as
+//      1/2 + tanh(x/2)/2, so the four lanes of a unit run the same code), and
+//      the unit's lane 4 (j % 8) gathers the G values by shuffles, applies the
+//      cell, updates its fp32 state and writes h_t to shared memory and h_seq
+//      (GRU: the reset gate reaches the n lane by one shuffle first; sLSTM:
+//      the stabilised exponential gates stay on the cell lane, which holds m);
 //   3. one CTA barrier (h is double-buffered by step parity).
 // (A split of each dot product over four threads -- 1024 threads for
 // Dh = 64 -- ran 990 ns per step: a barrier of 32 warps alone takes ~160 ns.)
@@ -29,7 +33,18 @@ namespace srnn {
 namespace {
 constexpr int kPD = 4;  // Wx ring depth (steps)
 
-__device__ __forceinline__ float sigm(float x) { return 1.f / (1.f + expf(-x)); }
+// two fp32 FMAs in one instruction: (a.x b.x + c.x, a.y b.y + c.y), each rounded once
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+  return (unsigned long long)__float_as_uint(lo) | ((unsigned long long)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ float lo2(unsigned long long v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi2(unsigned long long v) { return __uint_as_float((uint32_t)(v >> 32)); }
 
 template <int CELL, int DH>
 __global__ void __launch_bounds__(DH * 4, 1) fwd_f32_kernel(const FwdParams p) {
@@ -56,9 +71,11 @@ __global__ void __launch_bounds__(DH * 4, 1) fwd_f32_kernel(const FwdParams p) {
   const size_t hseq_tstride = (size_t)B * NH * DH;
   const size_t si = ((size_t)b * NH + head) * DH + j;
 
-  float rcol[DH];  // R[h][k][row]
+  unsigned long long rc2[DH / 2];  // (R[h][2i][row], R[h][2i + 1][row])
 #pragma unroll
-  for (int k = 0; k < DH; ++k) rcol[k] = row_on ? Rh[(size_t)k * GD + row] : 0.f;
+  for (int i = 0; i < DH / 2; ++i)
+    rc2[i] = row_on ? pack2(Rh[(size_t)(2 * i) * GD + row], Rh[(size_t)(2 * i + 1) * GD + row])
+                    : 0ull;
   const float brow = (row_on && p.bias) ? p.bias[(size_t)head * GD + row] : 0.f;
 
   float st_c = 0.f, st_n = 0.f, st_m = 0.f, st_h = 0.f;
@@ -87,48 +104,56 @@ __global__ void __launch_bounds__(DH * 4, 1) fwd_f32_kernel(const FwdParams p) {
     // refill the slot of step t - 1 (read by every thread before the last
     // barrier) with step t - 1 + PD
     if (t > 0) issue(t - 1 + kPD);
-    // 1. dot product over h_{t-1}: float4 i/4 feeds chain (i/4) % 4
+    // 1. dot product over h_{t-1}: float4 i/4 feeds pair chains 2 ((i/4) % 2) + {0, 1}
     const float* hp = hs[t & 1];
-    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    unsigned long long a2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
     for (int i = 0; i < DH; i += 4) {
       const float4 x = *reinterpret_cast<const float4*>(hp + i);
-      float& c = a[(i / 4) % 4];
-      c = fmaf(x.x, rcol[i], c);
-      c = fmaf(x.y, rcol[i + 1], c);
-      c = fmaf(x.z, rcol[i + 2], c);
-      c = fmaf(x.w, rcol[i + 3], c);
+      const int c = 2 * ((i / 4) % 2);
+      a2[c] = ffma2(pack2(x.x, x.y), rc2[i / 2], a2[c]);
+      a2[c + 1] = ffma2(pack2(x.z, x.w), rc2[i / 2 + 1], a2[c + 1]);
     }
-    const float rec = ((a[0] + a[1]) + (a[2] + a[3])) + brow;  // R-part + bias of row `row`
-    // 2. gather unit j's gates into its cell lane
-    float pre[G];
-#pragma unroll
-    for (int k = 0; k < G; ++k) pre[k] = __shfl_sync(0xffffffffu, rec, (lane & ~3) + k);
+    const float rec = (((lo2(a2[0]) + hi2(a2[0])) + (lo2(a2[1]) + hi2(a2[1]))) +
+                       ((lo2(a2[2]) + hi2(a2[2])) + (lo2(a2[3]) + hi2(a2[3])))) +
+                      brow;  // R-part + bias of row `row`
+    // 2. this lane's gate, then the unit's G values gathered into its cell lane
     const float* x = xs[t % kPD];
+    const float xg = row_on ? x[row] : 0.f;
+    const int base = lane & ~3;
+    float v;
+    if constexpr (CELL == kLSTM) {  // i, f, o: sigmoid; z: tanh
+      const float th = tanhf(g == 2 ? rec + xg : 0.5f * (rec + xg));
+      v = g == 2 ? th : fmaf(0.5f, th, 0.5f);
+    } else if constexpr (CELL == kGRU) {  // r, z: sigmoid; n = tanh(x_n + r (R_n h + b_n))
+      const float sg = fmaf(0.5f, tanhf(0.5f * (xg + rec)), 0.5f);
+      const float r = __shfl_sync(0xffffffffu, sg, base);
+      const float nt = tanhf(fmaf(r, rec, xg));
+      v = g == 2 ? nt : sg;
+    } else {  // sLSTM: i~, f~ raw (stabilised on the cell lane), z: tanh, o: sigmoid
+      const float pre = rec + xg;
+      const float th = tanhf(g == 3 ? 0.5f * pre : pre);
+      v = g < 2 ? pre : (g == 2 ? th : fmaf(0.5f, th, 0.5f));
+    }
+    float gv[G];
+#pragma unroll
+    for (int k = 0; k < G; ++k) gv[k] = __shfl_sync(0xffffffffu, v, base + k);
     if (cell) {
       float h;
       if constexpr (CELL == kLSTM) {
-        const float ig = sigm(pre[0] + x[j]);
-        const float fg = sigm(pre[1] + x[DH + j]);
-        const float zg = tanhf(pre[2] + x[2 * DH + j]);
-        const float og = sigm(pre[3] + x[3 * DH + j]);
-        st_c = fg * st_c + ig * zg;
-        h = og * tanhf(st_c);
+        st_c = fmaf(gv[1], st_c, gv[0] * gv[2]);
+        h = gv[3] * tanhf(st_c);
       } else if constexpr (CELL == kGRU) {
-        const float rg = sigm(x[j] + pre[0]);
-        const float zg = sigm(x[DH + j] + pre[1]);
-        const float ng = tanhf(x[2 * DH + j] + rg * pre[2]);
-        h = (1.f - zg) * ng + zg * st_h;
+        h = (1.f - gv[1]) * gv[2] + gv[1] * st_h;
       } else {
-        const float pi = pre[0] + x[j], pf = pre[1] + x[DH + j];
-        const float pz = pre[2] + x[2 * DH + j], po = pre[3] + x[3 * DH + j];
+        const float pi = gv[0], pf = gv[1];
         const float mn = fmaxf(pf + st_m, pi);
         const float ig = expf(pi - mn);
         const float fg = expf(pf + st_m - mn);
-        st_c = fg * st_c + ig * tanhf(pz);
+        st_c = fg * st_c + ig * gv[2];
         st_n = fg * st_n + ig;
         st_m = mn;
-        h = sigm(po) * (st_c / st_n);
+        h = gv[3] * (st_c / st_n);
       }
       st_h = h;
       hs[(t + 1) & 1][j] = h;
