@@ -44,6 +44,7 @@ def check(got, ref, label):
     (1, 16, 8),            # smallest shape
     (257, 384, 1000),      # many k blocks, K tail
     (2048, 3072, 768),     # the 12 x 64 LSTM's projection at T*B = 2048
+    (16384, 256, 64),      # 256-wide pair tiles (192-wide ones would leave pairs two tiles)
 ])
 def test_input_proj_matches_oracle(S, M, N, K):
     d = make_projection_inputs(M, N, K, seed=M + N + K)
