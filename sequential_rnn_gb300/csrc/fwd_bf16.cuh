@@ -690,30 +690,6 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
             }
 
         late_fetch();
-        // training stash of this step, per cell: four gate values [T,B,NH,4Dh] and
-        // the state the backward needs [T,B,NH,Dh] (LSTM c_t, GRU h_t, sLSTM c_t
-        // plus n_t in a third array).  GRU slots: r, z, n, R_n h + b_n.
-        if (TR) {
-#pragma unroll
-          for (int us = 0; us < NSLOT; ++us)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int ei = (us * NT + nt) * 2 + e;
-                const int n = nt * 8 + 2 * (lane & 3) + e;
-                if (n < nvalid) {
-                  const int j = u0 + ub + (lane >> 2) + 8 * us;
-                  const size_t row = ((size_t)t * B + b0 + n) * NH + head;
-                  float* sg = p.stash_gates + row * 4 * DH + j;
-#pragma unroll
-                  for (int g = 0; g < 4; ++g) sg[g * DH] = act[TR ? g : 0][TR ? ei : 0];
-                  p.stash_c[row * DH + j] = CELL == kGRU ? st_h[ei] : st_c[ei];
-                  if (CELL == kSLSTM) p.stash_n[row * DH + j] = st_n[ei];
-                }
-              }
-        }
-
         // ---- publish h_t
         const uint32_t nbuf = s_h + (uint32_t)((t + 1) & 1) * NB * HPB;
         uint32_t xv[4] = {0u, 0u, 0u, 0u};  // cluster: this lane's 16-byte chunk of h_t
@@ -772,6 +748,31 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 }
               }
         }
+        // training stash of this step (after h_t is on its way: nothing of the
+        // recurrence waits for it), per cell: four gate values [T,B,NH,4Dh] and
+        // the state the backward needs [T,B,NH,Dh] (LSTM c_t, GRU h_t, sLSTM c_t
+        // plus n_t in a third array).  GRU slots: r, z, n, R_n h + b_n.
+        if (TR) {
+#pragma unroll
+          for (int us = 0; us < NSLOT; ++us)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int ei = (us * NT + nt) * 2 + e;
+                const int n = nt * 8 + 2 * (lane & 3) + e;
+                if (n < nvalid) {
+                  const int j = u0 + ub + (lane >> 2) + 8 * us;
+                  const size_t row = ((size_t)t * B + b0 + n) * NH + head;
+                  float* sg = p.stash_gates + row * 4 * DH + j;
+#pragma unroll
+                  for (int g = 0; g < 4; ++g) sg[g * DH] = act[TR ? g : 0][TR ? ei : 0];
+                  p.stash_c[row * DH + j] = CELL == kGRU ? st_h[ei] : st_c[ei];
+                  if (CELL == kSLSTM) p.stash_n[row * DH + j] = st_n[ei];
+                }
+              }
+        }
+
         // ---- prime the next step's accumulators while other warps finish
         if (!EARLY_PREP && send && !prep()) dead = true;
         if (CL) {
