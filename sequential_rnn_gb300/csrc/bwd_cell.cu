@@ -83,7 +83,11 @@ struct BwdK {
   static constexpr uint32_t DB = DB_ALIAS ? DG : ((RX + RX_BYTES + 127) & ~127u);
   static constexpr uint32_t BAR = ((DB_ALIAS ? RX + RX_BYTES : DB + DB_BYTES) + 15) & ~15u;
   static constexpr uint32_t FLAG = BAR + 16;
-  static constexpr uint32_t TOTAL = FLAG + 16;
+  // cluster reduce-scatter: per warp two 256-byte buffers, one m16 tile's
+  // partials [batch row][16 units] bf16 each, sent as 16-byte chunks
+  static constexpr uint32_t STG = (FLAG + 16 + 127) & ~127u;
+  static constexpr uint32_t STG_BYTES = CS > 1 ? (uint32_t)NW * 2 * kNB * 16 * 2 : 0u;
+  static constexpr uint32_t TOTAL = STG + STG_BYTES;
   static constexpr bool SPLIT = MTW <= 2;      // two k chains when registers allow
   // Per-cell inputs: loaded two steps ahead into registers where registers
   // allow (PFD = 2).  At Dh = 768 (168 registers) the allocator spills values
@@ -127,6 +131,7 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
   const int nvalid = min(kNB, B - b0);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t s_rf = sbase + K::RF, s_dg = sbase + K::DG, s_rx = sbase + K::RX;
+  const uint32_t s_stg = sbase + K::STG + (uint32_t)warp * (2 * kNB * 16 * 2);
   const uint32_t bar_r = sbase + K::BAR;  // two: partial buffers 0 / 1
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + K::FLAG);
   const unsigned long long tlim = p.timeout_ns;
@@ -403,13 +408,19 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
         }
       }
     }
-    // ---- reduce-scatter: rows k (unit) go to the CTA owning k
+    // ---- reduce-scatter: rows k (unit) go to the CTA owning k.  Cluster: a
+    // tile's 16 units x 8 batch rows are staged as bf16 in one of the warp's two
+    // buffers and leave as 16 chunks of 8 units (16 bytes), one st.async.v4 per
+    // lane of the first half-warp (four-byte words per lane were 4x the remote
+    // stores); a tile of 16 units never straddles two owners (U % 16 == 0).
 #pragma unroll
     for (int mt = 0; mt < MTW; ++mt) {
       const int n = 2 * (lane & 3);
+      const int kt = (warp * MTW + mt) * 16;  // first unit of this tile
+      const uint32_t stg = s_stg + (uint32_t)(mt & 1) * (kNB * 16 * 2);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        const int k = (warp * MTW + mt) * 16 + (lane >> 2) + 8 * half;
+        const int k = kt + (lane >> 2) + 8 * half;
         const float v0 = acc[mt][2 * half] + (SPLIT ? acc2[SPLIT ? mt : 0][2 * half] : 0.f);
         const float v1 =
             acc[mt][2 * half + 1] + (SPLIT ? acc2[SPLIT ? mt : 0][2 * half + 1] : 0.f);
@@ -420,12 +431,23 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
         const float p0 = kev ? v0 : other, p1 = kev ? other : v1;
         const int nn = n + (kev ? 0 : 1), ke = k & ~1;
         if (CL) {
-          const int owner = ke / U, ku = ke % U;
-          const uint32_t buf = (uint32_t)(s & 1) * (CS * U * kNB * 2);
-          const uint32_t laddr = s_rx + buf + (uint32_t)((crank * kNB + nn) * U + ku) * 2;
-          st_async_b32(mapa(laddr, owner), pack_bf16x2(p0, p1), mapa(bar_r + 8 * (s & 1), owner));
+          asm volatile("st.shared.b32 [%0], %1;" ::"r"(stg + (uint32_t)(nn * 32 + (ke - kt) * 2)),
+                       "r"(pack_bf16x2(p0, p1))
+                       : "memory");
         } else {
           *reinterpret_cast<float2*>(smem + K::RX + (nn * U + ke) * 4) = make_float2(p0, p1);
+        }
+      }
+      if (CL) {
+        __syncwarp();  // the tile is staged (and the buffer's previous chunks were read)
+        if (lane < 16) {
+          const int cn = lane >> 1, k0 = kt + 8 * (lane & 1);
+          uint32_t v[4];
+          lds128(v, stg + (uint32_t)(cn * 32 + (lane & 1) * 16));
+          const int owner = k0 / U, ku = k0 % U;
+          const uint32_t buf = (uint32_t)(s & 1) * (CS * U * kNB * 2);
+          const uint32_t laddr = s_rx + buf + (uint32_t)((crank * kNB + cn) * U + ku) * 2;
+          st_async_v4(mapa(laddr, owner), v, mapa(bar_r + 8 * (s & 1), owner));
         }
       }
     }
