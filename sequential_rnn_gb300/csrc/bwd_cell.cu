@@ -413,6 +413,8 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
     // buffers and leave as 16 chunks of 8 units (16 bytes), one st.async.v4 per
     // lane of the first half-warp (four-byte words per lane were 4x the remote
     // stores); a tile of 16 units never straddles two owners (U % 16 == 0).
+    // Rows 4-7 keep their two 16-byte halves swapped, so the staging writes of
+    // rows n and n + 4 (32 bytes apart x 4) fall on different banks.
 #pragma unroll
     for (int mt = 0; mt < MTW; ++mt) {
       const int n = 2 * (lane & 3);
@@ -431,7 +433,8 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
         const float p0 = kev ? v0 : other, p1 = kev ? other : v1;
         const int nn = n + (kev ? 0 : 1), ke = k & ~1;
         if (CL) {
-          asm volatile("st.shared.b32 [%0], %1;" ::"r"(stg + (uint32_t)(nn * 32 + (ke - kt) * 2)),
+          const int kl = ke - kt, ch = (kl >> 3) ^ ((nn >> 2) & 1);  // physical 16-byte half
+          asm volatile("st.shared.b32 [%0], %1;" ::"r"(stg + (uint32_t)(nn * 32 + ch * 16 + (kl & 7) * 2)),
                        "r"(pack_bf16x2(p0, p1))
                        : "memory");
         } else {
@@ -443,7 +446,7 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
         if (lane < 16) {
           const int cn = lane >> 1, k0 = kt + 8 * (lane & 1);
           uint32_t v[4];
-          lds128(v, stg + (uint32_t)(cn * 32 + (lane & 1) * 16));
+          lds128(v, stg + (uint32_t)(cn * 32 + (((lane & 1) ^ ((cn >> 2) & 1)) * 16)));
           const int owner = k0 / U, ku = k0 % U;
           const uint32_t buf = (uint32_t)(s & 1) * (CS * U * kNB * 2);
           const uint32_t laddr = s_rx + buf + (uint32_t)((crank * kNB + cn) * U + ku) * 2;
