@@ -92,7 +92,10 @@ typedef enum {
   RNN_ERR_LAUNCH = 4,      /* the CUDA launch itself failed */
   RNN_ERR_TIMEOUT = 5,     /* device status: a bounded wait ran out, outputs invalid */
   RNN_ERR_NO_CLUSTER = 6,  /* the device cannot co-schedule the needed thread-block cluster */
-  RNN_ERR_SCRATCH_LIMIT = 7 /* rnn_fwd_noalloc: the call needs more scratch than its array holds */
+  RNN_ERR_SCRATCH_LIMIT = 7, /* rnn_fwd_noalloc: the call needs more scratch than its array holds */
+  RNN_ERR_BOUNDS = 8         /* device status, bounds-check builds only (libsrnn_bc.so, compiled with
+                                -DRNN_BOUNDS_CHECK): a kernel index fell outside its buffer; the
+                                access was skipped, outputs invalid */
 } rnn_status_t;
 
 /* Bytes of device workspace rnn_fwd (pass 0) / rnn_bwd (pass 1) need.
@@ -232,7 +235,8 @@ int rnn_stack_fwd(const rnn_desc_t* desc, int32_t L, int32_t Din, int32_t chunk,
 int rnn_plan(const rnn_desc_t* desc, int32_t L, int32_t sms, int32_t* out5);
 
 /* Synchronises `stream`, reads the device status word of `workspace` into
- * *device_status (RNN_OK or RNN_ERR_TIMEOUT).  Returns RNN_OK if the read
+ * *device_status (RNN_OK, RNN_ERR_TIMEOUT, or in bounds-check builds
+ * RNN_ERR_BOUNDS; a timeout is reported first).  Returns RNN_OK if the read
  * itself worked, else RNN_ERR_LAUNCH. */
 int rnn_read_status(const void* workspace, void* stream, int* device_status);
 

@@ -10,7 +10,9 @@ import ctypes
 import os
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libsrnn.so")
+# SRNN_BOUNDS_CHECK=1 loads the bounds-check build (libsrnn_bc.so) instead
+LIB_PATH = os.path.join(_PKG, "libsrnn_bc.so" if os.environ.get("SRNN_BOUNDS_CHECK") == "1"
+                        else "libsrnn.so")
 
 RNN_LSTM, RNN_GRU, RNN_SLSTM = 0, 1, 2
 RNN_F32, RNN_BF16 = 0, 1
@@ -20,7 +22,7 @@ RNN_FLAG_TEST_TIMEOUT = 1 << 30
 RNN_HOST_DIRECT = -1  # rnn_fwd_host chunk: the kernel reads / writes the mapped host buffers
 STATUS = {0: "RNN_OK", 1: "RNN_ERR_INVALID_ARG", 2: "RNN_ERR_UNSUPPORTED",
           3: "RNN_ERR_MISALIGNED", 4: "RNN_ERR_LAUNCH", 5: "RNN_ERR_TIMEOUT",
-          6: "RNN_ERR_NO_CLUSTER", 7: "RNN_ERR_SCRATCH_LIMIT"}
+          6: "RNN_ERR_NO_CLUSTER", 7: "RNN_ERR_SCRATCH_LIMIT", 8: "RNN_ERR_BOUNDS"}
 CELLS = {"lstm": RNN_LSTM, "gru": RNN_GRU, "slstm": RNN_SLSTM}
 DTYPES = {"f32": RNN_F32, "bf16": RNN_BF16}
 

@@ -4,6 +4,10 @@ Each CUDA translation unit is compiled in parallel with nvcc
 (-gencode arch=compute_103a,code=sm_103a), then linked with the static CUDA
 runtime into sequential_rnn_gb300/libsrnn.so.  Objects go to
 sequential_rnn_gb300/_build/.  Usage:  python -m sequential_rnn_gb300.build
+
+The bounds-check variant (-DRNN_BOUNDS_CHECK: every computed index checked,
+violations reported as RNN_ERR_BOUNDS) goes to libsrnn_bc.so via
+_build_bc/:  python -m sequential_rnn_gb300.build -bc
 """
 from __future__ import annotations
 
@@ -17,6 +21,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsrnn.so")
+LIB_BC = os.path.join(PKG, "libsrnn_bc.so")
 
 SOURCES = ["capi.cu", "plan.cu", "runtime.cu", "fwd_f32.cu", "fwd_bf16_lstm.cu", "fwd_bf16_gru.cu", "fwd_bf16_slstm.cu",
            "floor.cu", "bwd_cell.cu", "grad_weights.cu", "tc_gemm.cu", "tc_gemm_pair.cu", "noalloc.cu"]
@@ -32,8 +37,11 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, bounds_check: bool = False) -> str:
+    bdir = BUILD + "_bc" if bounds_check else BUILD
+    lib = LIB_BC if bounds_check else LIB
+    flags = FLAGS + (["-DRNN_BOUNDS_CHECK"] if bounds_check else [])
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
     srcs = [s for s in SOURCES if os.path.exists(os.path.join(CSRC, s))]
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(ROOT, "include", "rnn.h")]
@@ -41,11 +49,11 @@ def build(verbose: bool = False, force: bool = False) -> str:
     procs = []
     objs = []
     for s in srcs:
-        obj = os.path.join(BUILD, s.replace(".cu", ".o"))
+        obj = os.path.join(bdir, s.replace(".cu", ".o"))
         objs.append(obj)
         if not force and os.path.exists(obj) and os.path.getmtime(obj) >= newest_dep:
             continue
-        cmd = [cc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, s), "-o", obj]
+        cmd = [cc, *ARCH, *flags, "-c", os.path.join(CSRC, s), "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
         procs.append((s, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
@@ -59,14 +67,14 @@ def build(verbose: bool = False, force: bool = False) -> str:
     if failed:
         msg = "\n".join(f"--- {s}\n{o}" for s, o in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
-    if force or not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
-        cmd = [cc, *ARCH, "-shared", "-o", LIB + ".tmp", *objs, "-cudart", "static"]
+    if force or not os.path.exists(lib) or any(os.path.getmtime(o) > os.path.getmtime(lib) for o in objs):
+        cmd = [cc, *ARCH, "-shared", "-o", lib + ".tmp", *objs, "-cudart", "static"]
         r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + r.stdout.decode(errors="replace"))
-        os.replace(LIB + ".tmp", LIB)
-    return LIB
+        os.replace(lib + ".tmp", lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv))
+    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv, bounds_check="-bc" in sys.argv))

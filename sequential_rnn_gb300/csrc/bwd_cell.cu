@@ -34,6 +34,7 @@
 #include <cstdint>
 
 #include "kernels.h"
+#include "check.cuh"
 #include "ptx.cuh"
 
 namespace srnn {
@@ -136,6 +137,9 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + K::FLAG);
   const unsigned long long tlim = p.timeout_ns;
   constexpr uint32_t kTx = (uint32_t)CS * U * kNB * 2;  // partial bytes landing per step
+  // element counts of the global buffers (bounds-check build)
+  const long long n_state = (long long)B * NH * DH, n_seq = (long long)T * n_state;
+  const long long n_g = (long long)T * B * NH * GD, n_r = (long long)NH * DH * GD;
 
   if (tid == 0) {
     mbar_init(bar_r, 1);
@@ -163,17 +167,20 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
     for (int ks = 0; ks < KSW; ++ks) {
       const int c0 = ks * 16 + 2 * (lane & 3);
       auto col = [&](int c) { return (c / U) * DH + u0 + (c % U); };
+      auto rv = [&](int r, int c) -> uint32_t {
+        const long long e = (long long)r * GD + col(c);
+        return bc_ok((long long)head * DH * GD + e, n_r, p.status) ? (uint32_t)Rb[e] : 0u;
+      };
       uint32_t a[4];
-      a[0] = (uint32_t)Rb[(size_t)ra * GD + col(c0)] | ((uint32_t)Rb[(size_t)ra * GD + col(c0 + 1)] << 16);
-      a[1] = (uint32_t)Rb[(size_t)rb * GD + col(c0)] | ((uint32_t)Rb[(size_t)rb * GD + col(c0 + 1)] << 16);
-      a[2] = (uint32_t)Rb[(size_t)ra * GD + col(c0 + 8)] |
-             ((uint32_t)Rb[(size_t)ra * GD + col(c0 + 9)] << 16);
-      a[3] = (uint32_t)Rb[(size_t)rb * GD + col(c0 + 8)] |
-             ((uint32_t)Rb[(size_t)rb * GD + col(c0 + 9)] << 16);
+      a[0] = rv(ra, c0) | (rv(ra, c0 + 1) << 16);
+      a[1] = rv(rb, c0) | (rv(rb, c0 + 1) << 16);
+      a[2] = rv(ra, c0 + 8) | (rv(ra, c0 + 9) << 16);
+      a[3] = rv(rb, c0 + 8) | (rv(rb, c0 + 9) << 16);
       if (ks < KREG) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) areg[mt][ks < KREG ? ks : 0][q] = a[q];
-      } else {
+      } else if (bc_ok((long long)(rf_warp - s_rf) + (mt * KSM + (ks - KREG)) * 512 + 15, K::RF_BYTES,
+                       p.status)) {  // the step loop reads the same offsets back
         asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
                          rf_warp + (uint32_t)(mt * KSM + (ks - KREG)) * 512),
                      "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3])
@@ -192,8 +199,8 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
     const int ci = tid + e * NTH;
     cu[e] = ci % U;
     cn[e] = ci / U;
-    cok[e] = cn[e] < nvalid;
     const size_t si = ((size_t)(b0 + cn[e]) * NH + head) * DH + u0 + cu[e];
+    cok[e] = cn[e] < nvalid && bc_ok((long long)si, n_state, p.status);
     dcar[e] = (CELL != kGRU && cok[e] && p.dcT) ? p.dcT[si] : 0.f;
     dncar[e] = (CELL == kSLSTM && cok[e] && p.dnT) ? p.dnT[si] : 0.f;
     dhv[e] = (cok[e] && p.dhT) ? p.dhT[si] : 0.f;  // dh_rec of the last step
@@ -215,6 +222,14 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
     const size_t row = ((size_t)t * B + b0 + cn[e]) * NH + head;
     const int j = u0 + cu[e];
     const size_t si0 = ((size_t)(b0 + cn[e]) * NH + head) * DH + j;  // initial-state index
+    if (!bc_ok((long long)(row * 4 * DH + 3 * DH + j), 4 * n_seq, p.status) ||
+        !bc_ok((long long)(row * DH + j), n_seq, p.status) ||
+        !(t > 0 ? bc_ok((long long)((row - tstep) * DH + j), n_seq, p.status)
+               : bc_ok((long long)si0, n_state, p.status))) {
+#pragma unroll
+      for (int q = 0; q < NV; ++q) v[q] = 0.f;
+      return;
+    }
     const float* sg = p.stash_gates + row * 4 * DH + j;
 #pragma unroll
     for (int g = 0; g < 4; ++g) v[g] = sg[g * DH];
@@ -237,6 +252,9 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
     if (t < 0 || !cok[e]) return;
     const size_t row = ((size_t)t * B + b0 + cn[e]) * NH + head;
     const int j = u0 + cu[e];
+    if (!bc_ok((long long)(row * 4 * DH + 3 * DH + j), 4 * n_seq, p.status) ||
+        !bc_ok((long long)(row * DH + j), n_seq, p.status))
+      return;
     const float* sg = p.stash_gates + row * 4 * DH + j;
 #pragma unroll
     for (int g = 0; g < 4; ++g) prefetch_l1(sg + g * DH);
@@ -352,7 +370,7 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
           asm volatile("st.shared.u16 [%0], %1;" ::"r"(s_dg + cn[e] * DGP + (g * U + cu[e]) * 2),
                        "h"(*reinterpret_cast<const uint16_t*>(&vg))
                        : "memory");
-          if (cok[e]) {
+          if (cok[e] && bc_ok((long long)(row * GD + g * DH + u0 + cu[e]), n_g, p.status)) {
             dwx[row * GD + g * DH + u0 + cu[e]] = __float2bfloat16_rn(dx[g]);
             if (CELL == kGRU && drec) drec[row * GD + g * DH + u0 + cu[e]] = vg;
           }
@@ -450,7 +468,8 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
           const int owner = k0 / U, ku = k0 % U;
           const uint32_t buf = (uint32_t)(s & 1) * (CS * U * kNB * 2);
           const uint32_t laddr = s_rx + buf + (uint32_t)((crank * kNB + cn) * U + ku) * 2;
-          st_async_v4(mapa(laddr, owner), v, mapa(bar_r + 8 * (s & 1), owner));
+          if (bc_ok((long long)(laddr - s_rx) + 15, K::RX_BYTES, p.status) && bc_ok(owner, CS, p.status))
+            st_async_v4(mapa(laddr, owner), v, mapa(bar_r + 8 * (s & 1), owner));
         }
       }
     }
@@ -477,6 +496,7 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
     for (int e = 0; e < EPT; ++e) {
       if (!cok[e]) continue;
       const size_t si = ((size_t)(b0 + cn[e]) * NH + head) * DH + u0 + cu[e];
+      if (!bc_ok((long long)si, n_state, p.status)) continue;
       if (p.dh0) p.dh0[si] = dhv[e] + (CELL == kGRU ? dcar[e] : 0.f);
       if (p.dc0 && CELL != kGRU) p.dc0[si] = dcar[e];
       if (p.dn0 && CELL == kSLSTM) p.dn0[si] = dncar[e];
@@ -494,7 +514,9 @@ __global__ void __launch_bounds__(BwdK<CELL, DH>::NTH, 1) bwd_cell_kernel(const 
       const int g = i / U, u = i % U;
       float sum = 0.f;
       for (int n = 0; n < kNB; ++n) sum += dbs[(n * G + g) * U + u];
-      p.db_part[((size_t)bslice * NH + head) * GD + g * DH + u0 + u] = sum;
+      if (bc_ok(((long long)bslice * NH + head) * GD + g * DH + u0 + u, (long long)p.nbslices * NH * GD,
+                p.status))
+        p.db_part[((size_t)bslice * NH + head) * GD + g * DH + u0 + u] = sum;
     }
   }
   if (CL) cluster_sync();

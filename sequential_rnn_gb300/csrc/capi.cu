@@ -25,6 +25,7 @@ const char* rnn_status_str(int status) {
     case RNN_ERR_TIMEOUT: return "device wait timed out";
     case RNN_ERR_NO_CLUSTER: return "thread-block cluster cannot be scheduled";
     case RNN_ERR_SCRATCH_LIMIT: return "needs more scratch than the no-allocation entry point holds";
+    case RNN_ERR_BOUNDS: return "an index fell outside its buffer (bounds-check build)";
     default: return "unknown status";
   }
 }
@@ -165,7 +166,8 @@ int rnn_read_status(const void* workspace, void* stream, int* device_status) {
   if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return RNN_ERR_LAUNCH;
   if (cudaStreamSynchronize(s) != cudaSuccess) return RNN_ERR_LAUNCH;
-  *device_status = (v & kStatusTimeout) ? RNN_ERR_TIMEOUT : RNN_OK;
+  *device_status =
+      (v & kStatusTimeout) ? RNN_ERR_TIMEOUT : ((v & kStatusBounds) ? RNN_ERR_BOUNDS : RNN_OK);
   return RNN_OK;
 }
 

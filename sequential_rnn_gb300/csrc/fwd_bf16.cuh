@@ -41,6 +41,7 @@
 #include <cuda_runtime.h>
 
 #include "kernels.h"
+#include "check.cuh"
 #include "ptx.cuh"
 
 namespace srnn {
@@ -195,6 +196,10 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
   const uint32_t stage_bytes = (uint32_t)NB * WP;
   const uint32_t hpart = 2u * NB * HPB;  // byte offset of the lo part of h
   const uint32_t htx = (uint32_t)C::HPARTS * NB * DH * 2;  // h bytes landing per step (cluster)
+  // element counts of the global buffers (bounds-check build)
+  const long long n_state = (long long)B * NH * DH, n_hseq = (long long)T * n_state;
+  const long long n_wx = (long long)T * B * NH * GD, n_r = (long long)NH * DH * GD;
+  const long long n_h_smem = 2ll * C::HPARTS * NB * HPB;  // h buffers (bytes from L.h)
 
   // ------------------------------------------------------------- set-up --
   if (tid == 0) {
@@ -219,14 +224,17 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     const int nb = HN ? (n & 3) : n;
     float v0 = 0.f, v1 = 0.f;
     if (p.h0 != nullptr && nb < nvalid) {
-      const float* src = p.h0 + ((size_t)(b0 + nb) * NH + head) * DH + j;
-      v0 = src[0];
-      v1 = src[1];
+      const long long e = ((long long)(b0 + nb) * NH + head) * DH + j;
+      if (bc_ok(e + 1, n_state, p.status)) {
+        v0 = p.h0[e];
+        v1 = p.h0[e + 1];
+      }
     }
     if (HN && n >= 4) {
       v0 -= bf16_round(v0);
       v1 -= bf16_round(v1);
     }
+    if (!bc_ok((long long)n * HPB + j * 2 + 3, n_h_smem, p.status)) continue;
     *reinterpret_cast<uint32_t*>(smem + L.h + n * HPB + j * 2) = pack_bf16x2(v0, v1);
     if (HLO)
       *reinterpret_cast<uint32_t*>(smem + L.h + hpart + n * HPB + j * 2) =
@@ -255,6 +263,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
     const uint32_t rf_warp = s_rf + (uint32_t)warp * MT * KSM * 512 + lane * 16;
     auto rval = [&](int k, int col, float sc) -> uint32_t {
       if (col < 0) return 0u;
+      if (!bc_ok((long long)head * DH * GD + (long long)k * GD + col, n_r, p.status)) return 0u;
       const uint16_t v = Rb[(size_t)k * GD + col];
       if (sc == 1.f) return v;
       const __nv_bfloat16 x = __float2bfloat16_rn(__uint_as_float((uint32_t)v << 16) * sc);
@@ -281,6 +290,9 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
           for (int q = 0; q < 4; ++q) areg[mt][ks < KREG ? ks : 0][q] = a[q];
         } else {
           const uint32_t addr = rf_warp + (uint32_t)(mt * KSM + (ks - KREG)) * 512;
+          // the step loop reads the same offsets back
+          if (!bc_ok((long long)(addr - s_rf) + 15, (long long)(L.stg > L.rf ? L.stg - L.rf : 0), p.status))
+            continue;
           asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a[0]), "r"(a[1]),
                        "r"(a[2]), "r"(a[3])
                        : "memory");
@@ -296,7 +308,10 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
       const int j = u0 + ub + (lane >> 2) + 8 * us;
 #pragma unroll
       for (int g = 0; g < G; ++g)
-        sbias[g][us] = C::gate_scale(g) * (p.bias ? p.bias[(size_t)head * GD + g * DH + j] : 0.f);
+        sbias[g][us] = C::gate_scale(g) *
+                       ((p.bias && bc_ok((long long)head * GD + g * DH + j, (long long)NH * GD, p.status))
+                            ? p.bias[(size_t)head * GD + g * DH + j]
+                            : 0.f);
       // HN: the lo columns (lanes with lane & 2) start from zero; the shuffle
       // adds them onto the hi columns, which carry Wx and the bias
       if (HN && (lane & 2)) {
@@ -316,7 +331,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
           const int n = (nt * 8 + 2 * (lane & 3) + e) & (HN ? 3 : 255);
           const int j = u0 + ub + (lane >> 2) + 8 * us;
           const size_t si = ((size_t)(b0 + n) * NH + head) * DH + j;
-          const bool ok = n < nvalid;
+          const bool ok = n < nvalid && bc_ok((long long)si, n_state, p.status);
           st_c[ei] = (ok && p.c0) ? p.c0[si] : 0.f;
           st_n[ei] = (ok && p.n0) ? p.n0[si] : 0.f;
           st_m[ei] = (ok && p.m0) ? p.m0[si] : 0.f;
@@ -400,7 +415,11 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
         const __nv_bfloat16* src = wx_base + (size_t)tt * wx_tstride;
 #pragma unroll
         for (int i = 0; i < WCI; ++i)
-          if (wok[i]) cp_async16(stage + wdst[i], src + wsrc[i]);
+          if (wok[i] &&
+              bc_ok(((long long)b0 * NH + head) * GD + (long long)tt * wx_tstride + wsrc[i] + 7, n_wx,
+                    p.status) &&
+              bc_ok((long long)(stage - s_wx) + wdst[i] + 15, (long long)PD * stage_bytes, p.status))
+            cp_async16(stage + wdst[i], src + wsrc[i]);
       }
       cp_async_commit();
     };
@@ -538,8 +557,14 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
         if (EARLY_PREP && send) prep_load();
         // ---- acc += R^T h_{t-1}
         const uint32_t hb = s_h + (uint32_t)(t & 1) * NB * HPB + lm_off;
+        // (bounds-check build) the last 16 bytes this lane's ldmatrix reads; on
+        // failure the step's contraction is skipped and the CTA stops
+        const bool h_ok = bc_ok((long long)(hb - s_h) + (HLO ? hpart : 0) + (NT - 1) * 8 * HPB +
+                                    (KS / 2 - 1) * 64 + 15,
+                                n_h_smem, p.status);
+        if (!h_ok) dead = true;
 #pragma unroll
-        for (int kp = 0; kp < KS / 2; ++kp) {
+        for (int kp = 0; kp < (h_ok ? KS / 2 : 0); ++kp) {
           uint32_t bfr[NT][4], bfl[HLO ? NT : 1][4];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) ldmatrix_x4(bfr[nt], hb + nt * 8 * HPB + kp * 64);
@@ -722,7 +747,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
           if (send) {
             const uint32_t lbar = bar_h + 8 * ((t + 1) & 1);
             const uint32_t ldst = nbuf + x_dst;
-            for (int rk = x_r0; rk < CS; rk += RSTEP) st_async_v4(mapa(ldst, rk), xv, mapa(lbar, rk));
+            if (bc_ok((long long)(ldst - s_h) + 15, n_h_smem, p.status))
+              for (int rk = x_r0; rk < CS; rk += RSTEP) st_async_v4(mapa(ldst, rk), xv, mapa(lbar, rk));
           }
         } else {
           // own cells into the next buffer (also at the last step: h_seq is stored
@@ -764,6 +790,9 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
                 if (n < nvalid) {
                   const int j = u0 + ub + (lane >> 2) + 8 * us;
                   const size_t row = ((size_t)t * B + b0 + n) * NH + head;
+                  if (!bc_ok((long long)(row * 4 * DH + 3 * DH + j), 4 * n_hseq, p.status) ||
+                      !bc_ok((long long)(row * DH + j), n_hseq, p.status))
+                    continue;
                   float* sg = p.stash_gates + row * 4 * DH + j;
 #pragma unroll
                   for (int g = 0; g < 4; ++g) sg[g * DH] = act[TR ? g : 0][TR ? ei : 0];
@@ -777,7 +806,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
         if (!EARLY_PREP && send && !prep()) dead = true;
         if (CL) {
           // this warp's h_seq chunk, after the exchange is on its way
-          if (x_store)
+          if (x_store &&
+              bc_ok((long long)(hseq_x - static_cast<__nv_bfloat16*>(p.h_seq)) + 7, n_hseq, p.status))
             asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(hseq_x), "r"(xv[0]),
                          "r"(xv[1]), "r"(xv[2]), "r"(xv[3])
                          : "memory");
@@ -792,7 +822,8 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
       }
       if (!CL) {
         // h_seq rows of this warp's slice after the barrier: they overlap the next step
-        if (ch_store) {
+        if (ch_store &&
+            bc_ok((long long)(hseq_ch - static_cast<__nv_bfloat16*>(p.h_seq)) + 7, n_hseq, p.status)) {
           uint32_t v[4];
           lds128(v, s_h + (uint32_t)((t + 1) & 1) * NB * HPB + ch_off);
           asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(hseq_ch), "r"(v[0]), "r"(v[1]),
@@ -814,6 +845,7 @@ __global__ void __launch_bounds__(FwdCfg<CELL, DH, UG, NT, KREG, HS>::MAXT, 1)
             if (n >= nvalid) continue;
             const int j = u0 + ub + (lane >> 2) + 8 * us;
             const size_t si = ((size_t)(b0 + n) * NH + head) * DH + j;
+            if (!bc_ok((long long)si, n_state, p.status)) continue;
             if (p.hT) p.hT[si] = hv[ei];
             if (p.cT && CELL != kGRU) p.cT[si] = st_c[ei];
             if (p.nT && CELL == kSLSTM) p.nT[si] = st_n[ei];

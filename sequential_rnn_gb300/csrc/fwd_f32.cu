@@ -25,6 +25,7 @@
 // refilled only after the barrier that follows its last read.
 #include <cuda_runtime.h>
 
+#include "check.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -70,25 +71,39 @@ __global__ void __launch_bounds__(DH * 4, 1) fwd_f32_kernel(const FwdParams p) {
   float* hseq = static_cast<float*>(p.h_seq) + ((size_t)b * NH + head) * DH + j;
   const size_t hseq_tstride = (size_t)B * NH * DH;
   const size_t si = ((size_t)b * NH + head) * DH + j;
+  // element counts of the global buffers (bounds-check build)
+  const long long n_state = (long long)B * NH * DH, n_hseq = (long long)T * n_state;
+  const long long n_wx = (long long)T * B * NH * GD, n_r = (long long)NH * DH * GD;
+  // (lanes without a gate row -- GRU slot 3 -- load nothing)
+  const bool r_ok = !row_on || bc_ok((long long)head * DH * GD + (long long)(DH - 1) * GD + row, n_r, p.status);
+  const bool s_ok = bc_ok((long long)si, n_state, p.status);
 
   unsigned long long rc2[DH / 2];  // (R[h][2i][row], R[h][2i + 1][row])
 #pragma unroll
   for (int i = 0; i < DH / 2; ++i)
-    rc2[i] = row_on ? pack2(Rh[(size_t)(2 * i) * GD + row], Rh[(size_t)(2 * i + 1) * GD + row])
-                    : 0ull;
-  const float brow = (row_on && p.bias) ? p.bias[(size_t)head * GD + row] : 0.f;
+    rc2[i] = (row_on && r_ok)
+                 ? pack2(Rh[(size_t)(2 * i) * GD + row], Rh[(size_t)(2 * i + 1) * GD + row])
+                 : 0ull;
+  const float brow =
+      (row_on && p.bias && bc_ok((long long)head * GD + row, (long long)NH * GD, p.status))
+          ? p.bias[(size_t)head * GD + row]
+          : 0.f;
 
   float st_c = 0.f, st_n = 0.f, st_m = 0.f, st_h = 0.f;
-  if (cell) {
+  if (cell && s_ok) {
     st_h = p.h0 ? p.h0[si] : 0.f;
     st_c = p.c0 ? p.c0[si] : 0.f;
     st_n = p.n0 ? p.n0[si] : 0.f;
     st_m = p.m0 ? p.m0[si] : 0.f;
   }
-  for (int i = tid; i < DH; i += NT) hs[0][i] = p.h0 ? p.h0[((size_t)b * NH + head) * DH + i] : 0.f;
+  for (int i = tid; i < DH; i += NT)
+    hs[0][i] = (p.h0 && bc_ok(((long long)b * NH + head) * DH + i, n_state, p.status))
+                   ? p.h0[((size_t)b * NH + head) * DH + i]
+                   : 0.f;
 
   auto issue = [&](int t) {
-    if (t < T && tid < WCH)
+    if (t < T && tid < WCH &&
+        bc_ok(((long long)b * NH + head) * GD + (long long)t * wx_tstride + 4 * tid + 3, n_wx, p.status))
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(&xs[t % kPD][4 * tid])),
                    "l"(Wx + (size_t)t * wx_tstride + 4 * tid)
                    : "memory");
@@ -157,7 +172,7 @@ __global__ void __launch_bounds__(DH * 4, 1) fwd_f32_kernel(const FwdParams p) {
       }
       st_h = h;
       hs[(t + 1) & 1][j] = h;
-      *hseq = h;
+      if (bc_ok((long long)(hseq - static_cast<float*>(p.h_seq)), n_hseq, p.status)) *hseq = h;
     }
     hseq += hseq_tstride;
     // 3. step t + 1's Wx landed (own copies; PD - 2 younger groups may stay in
@@ -167,6 +182,7 @@ __global__ void __launch_bounds__(DH * 4, 1) fwd_f32_kernel(const FwdParams p) {
   }
   cp_async_wait<0>();
   if (cell && T > 0) {
+    if (!s_ok) return;
     if (p.hT) p.hT[si] = st_h;
     if (p.cT && CELL != kGRU) p.cT[si] = st_c;
     if (p.nT && CELL == kSLSTM) p.nT[si] = st_n;

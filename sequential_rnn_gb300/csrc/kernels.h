@@ -57,7 +57,9 @@ inline int prepare_launch(int (&state)[64][5], Kern kern, uint32_t smem, int thr
 }
 
 enum : int { kLSTM = 0, kGRU = 1, kSLSTM = 2 };
-enum : int { kStatusTimeout = 1 };  // bits of the device status word
+// bits of the device status word: a bounded wait ran out; (bounds-check builds)
+// an index fell outside its buffer
+enum : int { kStatusTimeout = 1, kStatusBounds = 2 };
 
 // Arguments of one forward launch.  Grid: one CTA per (head, batch slice,
 // cluster rank); blockIdx.x = ((head * nbslices) + bslice) * CS + rank.

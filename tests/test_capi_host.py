@@ -61,8 +61,8 @@ def _fwd(lib, desc, ws=0x1000, ws_bytes=256, wx=0x2000, r=0x3000, hseq=0x4000, s
 
 
 def test_status_strings(lib):
-    for s in range(8):
-        assert lib.rnn_status_str(s)
+    for s in range(9):
+        assert lib.rnn_status_str(s) and lib.rnn_status_str(s) != b"unknown status"
     assert lib.rnn_status_str(99) == b"unknown status"
 
 
