@@ -175,6 +175,30 @@ def oracle_rate(w, d, budget_s=10.0):
     return f_full * reps / el / 1e12, reps, el, busy
 
 
+SINGLE_THREAD_ENV = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS",
+                     "BLIS_NUM_THREADS", "VECLIB_MAXIMUM_THREADS", "NUMEXPR_NUM_THREADS")
+
+
+def oracle_rate_single_thread(workload, max_T, budget_s):
+    """The oracle's rate on one host thread: a child process whose BLAS thread
+    pools are limited to one before numpy loads (no GPU work in it)."""
+    env = dict(os.environ)
+    for k in SINGLE_THREAD_ENV:
+        env[k] = "1"
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "from synth import workload_inputs; "
+            "w = bench.sample_workload(dict(bench.WORKLOADS[%r]), %d); "
+            "d = workload_inputs(%r, T=w['T']); "
+            "r, reps, el, busy = bench.oracle_rate(w, d, budget_s=%r); "
+            "print(json.dumps({'value': r, 'reps': reps, 'seconds': el, 'busy': busy}))"
+            % (ROOT, workload, max_T, workload, budget_s))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=600)
+    if r.returncode != 0:
+        return None
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
 def threads_used(busy):
     """Threads the oracle kept busy, rounded (at least 1), for ``cores``."""
     return max(1, int(round(busy)))
@@ -599,6 +623,12 @@ def main():
                "sample": (f"{args.workload} with T cut to {sw['T']}, {reps} oracle passes in "
                           f"{el:.1f} s; {busy:.2f} threads busy on average of {os.cpu_count()} "
                           "host cores")}
+        one = oracle_rate_single_thread(args.workload, sw["T"], 5.0)
+        if one is not None:
+            cpu["single_thread"] = {
+                "value": one["value"], "unit": "TFLOP/s", "cores": 1,
+                "sample": (f"same sample, BLAS thread pools limited to one: {one['reps']} passes "
+                           f"in {one['seconds']:.1f} s ({one['busy']:.2f} threads busy)")}
 
     if world > 1:
         import torch

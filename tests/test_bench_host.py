@@ -103,3 +103,10 @@ def test_traffic_hash_follows_the_kernels_own_sources(tmp_path, monkeypatch):
     assert bench.tu_source_hash("a.cu") == h0
     (csrc / "c.h").write_text("// c changed\n")      # an included header: invalidates
     assert bench.tu_source_hash("a.cu") != h0
+
+
+def test_single_thread_oracle_baseline_keeps_one_thread_busy():
+    """The cpu_baseline's one-thread figure really runs the oracle on one thread."""
+    one = bench.oracle_rate_single_thread("lstm_f32_1x64_b4_t256", 32, 0.5)
+    assert one is not None and one["value"] > 0 and one["reps"] >= 1
+    assert one["busy"] < 1.5, one
