@@ -60,6 +60,8 @@ constexpr uint16_t kBoth = 0x3;               // CTA mask of the pair
 struct PairArgs {
   int M, N;             // output rows / columns
   int tiles_m, tiles_n; // 256 x 256 tiles
+  int full;             // tiles run whole: tile u by pair u % pairs
+  int halves;           // the other tiles, split into 256 x 128 halves: half h by pair h
   int nkb;              // 64-deep k blocks
   const float* bias;    // [N] or null
   int* status;
@@ -87,6 +89,32 @@ __device__ __forceinline__ bool wait_pair(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// A pair's i-th work unit: 256 rows from m0, 256 columns from n0 (half: 128).
+struct PairUnit {
+  int m0, n0;
+  bool half;
+};
+// Pair p runs tiles p, p + pairs, ... below g.full, then half p if p < g.halves:
+// the last wave's tiles are split so that no pair runs a whole extra tile.
+__device__ __forceinline__ int pair_units(const PairArgs& g, int p, int pairs) {
+  return (p < g.full ? (g.full - p + pairs - 1) / pairs : 0) + (p < g.halves ? 1 : 0);
+}
+__device__ __forceinline__ PairUnit pair_unit(const PairArgs& g, int p, int pairs, int i) {
+  const int u = p + i * pairs;
+  PairUnit w;
+  if (u < g.full) {
+    w.m0 = (u / g.tiles_n) * PBM;
+    w.n0 = (u % g.tiles_n) * PBN;
+    w.half = false;
+  } else {
+    const int t = g.full + p / 2;
+    w.m0 = (t / g.tiles_n) * PBM;
+    w.n0 = (t % g.tiles_n) * PBN + (p & 1) * (PBN / 2);
+    w.half = true;
+  }
+  return w;
+}
+
 __global__ void __launch_bounds__(P_THREADS, 1)
     tc_proj_pair_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB,
                         const __grid_constant__ CUtensorMap mC, const PairArgs g) {
@@ -108,7 +136,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: the CTA that issues the MMAs
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-  const int nunits = g.tiles_m * g.tiles_n;
+  const int nunits = pair_units(g, pair, npairs);
   const unsigned long long tlim = g.timeout_ns;
 
   if (threadIdx.x == 32) {
@@ -145,9 +173,10 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       const uint32_t lead_full = mapa(bar_full, 0);
       int it = 0;  // ring position across all tiles
       bool stop = false;
-      for (int u = pair; u < nunits && !stop; u += npairs) {
-        const int mt = u / g.tiles_n, nt = u % g.tiles_n;
-        const int ma = mt * PBM + (int)rank * 128, nb = nt * PBN + (int)rank * 128;
+      for (int i = 0; i < nunits && !stop; ++i) {
+        const PairUnit w = pair_unit(g, pair, npairs, i);
+        // a half unit's pair MMA reads the first 64 of each CTA's 128 staged W rows
+        const int ma = w.m0 + (int)rank * 128, nb = w.n0 + (int)rank * (w.half ? 64 : 128);
         for (int kb = 0; kb < g.nkb; ++kb, ++it) {
           const int s = it % PNSTG, ph = it / PNSTG;
           // both CTAs' MMAs on this stage's previous contents completed
@@ -176,10 +205,12 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer --
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(PBM, PBN, false, false);
-      int it = 0, i = 0;
+      constexpr uint32_t idesc_full = idesc_bf16_f32(PBM, PBN, false, false);
+      constexpr uint32_t idesc_half = idesc_bf16_f32(PBM, PBN / 2, false, false);
+      int it = 0;
       bool stop = false;
-      for (int u = pair; u < nunits && !stop; u += npairs, ++i) {
+      for (int i = 0; i < nunits && !stop; ++i) {
+        const uint32_t idesc = pair_unit(g, pair, npairs, i).half ? idesc_half : idesc_full;
         const int a = i & 1;
         // both CTAs' epilogues have drained this accumulator buffer (tile i - 2)
         if (i >= 2 && !wait_pair(bar_tempty + 8 * a, ((i >> 1) - 1) & 1, abort_flag, g.status, tlim))
@@ -213,15 +244,15 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     const int hc = (warp - 2) >> 2;   // column half of the tile
     const int e = warp - 2;           // staging buffer / bias slot
     const uint32_t lead_tempty = mapa(bar_tempty, 0);
-    int i = 0;
-    for (int u = pair; u < nunits; u += npairs, ++i) {
+    for (int i = 0; i < nunits; ++i) {
       const int a = i & 1;
       if (!wait_pair(bar_tfull + 8 * a, (i >> 1) & 1, abort_flag, g.status, tlim)) break;
       tc_fence_after();
-      const int mt = u / g.tiles_n, nt = u % g.tiles_n;
-      epilogue_bf16_bias_128(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * PBN + hc * 128),
-                             g.bias, nt * PBN + hc * 128, g.N, mt * PBM + (int)rank * 128 + q * 32,
-                             g.M, out_stage + (uint32_t)e * 4096, bias_s + (uint32_t)e * 128, &mC);
+      const PairUnit w = pair_unit(g, pair, npairs, i);
+      if (!w.half || hc == 0)  // a half unit's 128 columns: the first four warps
+        epilogue_bf16_bias_128(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * PBN + hc * 128),
+                               g.bias, w.n0 + hc * 128, g.N, w.m0 + (int)rank * 128 + q * 32, g.M,
+                               out_stage + (uint32_t)e * 4096, bias_s + (uint32_t)e * 128, &mC);
       // accumulator buffer a may be overwritten by tile i + 2
       tc_fence_before();
       __syncwarp();
@@ -292,6 +323,12 @@ int launch_input_proj_pair(const void* x, const void* W, const float* bias, void
   const long long npairs = units < cap / 2 ? units : cap / 2;
   if (units == 0) return 0;
   if (npairs < 1) return -1;
+  // the last wave's r tiles as 2r halves when they fit one wave: 768 tiles over
+  // 76 pairs -> 8 pairs would run an 11th whole tile, 16 run half of one instead
+  const long long rem = units % npairs;
+  const bool split = rem > 0 && 2 * rem <= npairs;
+  g.full = (int)(split ? units - rem : units);
+  g.halves = (int)(split ? 2 * rem : 0);
   CUtensorMap a, b, c;
   int r = make_map(&a, x, (uint64_t)M, (uint64_t)K, (uint64_t)K, 64, 128);
   if (r) return r;
