@@ -45,6 +45,8 @@ def check(got, ref, label):
     (257, 384, 1000),      # many k blocks, K tail
     (2048, 3072, 768),     # the 12 x 64 LSTM's projection at T*B = 2048
     (16384, 256, 64),      # 256-wide pair tiles (192-wide ones would leave pairs two tiles)
+    (4096, 3072, 256),     # 192 pair tiles over 76 pairs: uneven waves, too many to split
+    (2048, 2944, 64),      # 96 tiles: the last 20 run as halves, one half wholly past N
 ])
 def test_input_proj_matches_oracle(S, M, N, K):
     d = make_projection_inputs(M, N, K, seed=M + N + K)
