@@ -47,6 +47,7 @@ def check(got, ref, label):
     (16384, 256, 64),      # 256-wide pair tiles (192-wide ones would leave pairs two tiles)
     (4096, 3072, 256),     # 192 pair tiles over 76 pairs: uneven waves, too many to split
     (2048, 2944, 64),      # 96 tiles: the last 20 run as halves, one half wholly past N
+    (1280, 3904, 200),     # 80 tiles: the last 4 run as halves, one wholly past N; K tail
 ])
 def test_input_proj_matches_oracle(S, M, N, K):
     d = make_projection_inputs(M, N, K, seed=M + N + K)
@@ -73,7 +74,8 @@ def test_input_proj_full_size_sampled_rows(S):
     got = S.input_proj(x, W, b)
     torch.cuda.synchronize()
     rows = np.random.default_rng(0).choice(M, 96, replace=False)
-    rows = np.concatenate([rows, [0, 127, 128, M - 1]])
+    # + rows of the last m tile, whose last eight tiles run as half tiles on 76 pairs
+    rows = np.concatenate([rows, [0, 127, 128, M - 256, M - 129, M - 1]])
     ref = O.input_projection(d["x"][rows], d["W"], d["b"])
     check(got[torch.from_numpy(rows).cuda()], ref, "full size")
 
