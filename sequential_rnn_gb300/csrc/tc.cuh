@@ -128,6 +128,18 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+// The same load multicast to the CTAs of `mask` (same shared-memory offset in
+// each); each destination's bytes complete on the mbarrier at `bar`'s offset in
+// the even CTA of the destination's own pair (`bar` names an even CTA's
+// barrier: the pair-relative CTA bit of the address selects the pair member).
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, int c0,
+                                                    int c1, uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
+      : "memory");
+}
 // Pair MMA, issued by one thread of the even CTA: A rows 0..M/2-1 and B rows
 // (N) 0..N/2-1 from this CTA's shared memory, the other halves from the peer's
 // at the same offsets; D rows 0..M/2-1 in this CTA's TMEM, the rest in the peer's.

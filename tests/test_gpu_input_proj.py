@@ -48,6 +48,9 @@ def check(got, ref, label):
     (4096, 3072, 256),     # 192 pair tiles over 76 pairs: uneven waves, too many to split
     (2048, 2944, 64),      # 96 tiles: the last 20 run as halves, one half wholly past N
     (1280, 3904, 200),     # 80 tiles: the last 4 run as halves, one wholly past N; K tail
+    (2048, 1024, 2048),    # K >= 2048: two pairs per cluster share x (multicast)
+    (1000, 1536, 2104),    # the same with ragged rows and a K tail
+    (5120, 1024, 2048),    # 40 two-pair units: more than one wave, the last ones as halves
 ])
 def test_input_proj_matches_oracle(S, M, N, K):
     d = make_projection_inputs(M, N, K, seed=M + N + K)
