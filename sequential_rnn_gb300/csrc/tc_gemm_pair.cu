@@ -22,8 +22,9 @@
 //             per tile).  Eight warps, not four: with four the drain of a tile
 //             took longer than its MMAs (~10k cycles against ~6k per tile).
 //
-// Two pairs per cluster (four SMs) when N spans two 256-column blocks: the
-// pairs take neighbouring column blocks of the same 256 rows, so they stage
+// Two pairs per cluster (four SMs) for deep sums (K >= 2048) when N spans two
+// 256-column blocks: the pairs take neighbouring column blocks of the same 256
+// rows, so they stage
 // the same x rows; CTA r of each pair fetches half of those 128 rows and
 // multicasts them into CTA r of both pairs (their bytes complete on each
 // destination pair's even-CTA barrier), and every stage is released only when
