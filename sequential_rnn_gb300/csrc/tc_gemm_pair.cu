@@ -24,9 +24,9 @@
 //
 // Two pairs per cluster (four SMs) for deep sums (K >= 2048) when N spans two
 // 256-column blocks: the pairs take neighbouring column blocks of the same 256
-// rows, so they stage
-// the same x rows; CTA r of each pair fetches half of those 128 rows and
-// multicasts them into CTA r of both pairs (their bytes complete on each
+// rows, so they stage the same x rows; CTA r of each pair fetches half of
+// those 128 rows and multicasts them into CTA r of both pairs (their bytes
+// complete on each
 // destination pair's even-CTA barrier), and every stage is released only when
 // both pairs' MMAs have read it.  x then crosses from L2 once per two tiles:
 // 24 KB instead of 32 KB of operands per SM and k block.
