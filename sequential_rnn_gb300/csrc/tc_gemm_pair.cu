@@ -26,10 +26,9 @@
 // 256-column blocks: the pairs take neighbouring column blocks of the same 256
 // rows, so they stage the same x rows; CTA r of each pair fetches half of
 // those 128 rows and multicasts them into CTA r of both pairs (their bytes
-// complete on each
-// destination pair's even-CTA barrier), and every stage is released only when
-// both pairs' MMAs have read it.  x then crosses from L2 once per two tiles:
-// 24 KB instead of 32 KB of operands per SM and k block.
+// complete on each destination pair's even-CTA barrier), and every stage is
+// released only when both pairs' MMAs have read it.  x then crosses from L2
+// once per two tiles: 24 KB instead of 32 KB of operands per SM and k block.
 //
 // Every wait is bounded; a wait that runs out sets the status word and stops
 // the CTA's loops, and the teardown lets every copy and commit that targets a
